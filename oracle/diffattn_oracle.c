@@ -1,0 +1,280 @@
+/*
+ * Float64 CPU oracle for the differential-attention head forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load, link or
+ * call this file.  Its only users are the tests under tests/, the smoke()
+ * check in __graft_entry__.py and the cpu_baseline / reference leg of
+ * bench.py.  It shares no code, header, table or constant with the CUDA
+ * library, and it includes nothing from it.
+ *
+ * What it computes (source: "Differential Transformer", Ultralytics glossary,
+ * section "How differential attention works"; the Japanese, Portuguese and
+ * Arabic editions of that page say the same thing):
+ *
+ *   map1 = softmax over keys of (Q1 K1^T / sqrt(d))
+ *   map2 = softmax over keys of (Q2 K2^T / sqrt(d))
+ *   out  = (map1 - lambda * map2) V            V has 2d columns
+ *
+ * followed, in the real model (same section, closing paragraph), by a
+ * per-head normalisation of each head's output and a multiplication by
+ * (1 - lambda_init), with lambda_init(l) = 0.8 - 0.6 exp(-0.3 (l - 1)).
+ *
+ * Readings of what the page leaves open (each is listed with its reason in
+ * the design notes of this repository):
+ *   - d in the 1/sqrt(d) scale is the width of one query/key half, as in the
+ *     page's worked example (n = 6, d = 8, v of width 2d).
+ *   - causal = 1 means key j is visible to query i iff j <= i (square,
+ *     top-left aligned); the same mask is applied to both maps.
+ *   - the per-head normalisation is the RMS form over the 2d output channels
+ *     of one (batch, head, token): y = o / sqrt(mean(o^2) + eps) * w[h, c],
+ *     then times (1 - lambda_init).  No mean subtraction, no bias.
+ *   - layers are numbered from 1 (the formula uses l - 1; l = 1 gives 0.2).
+ *
+ * The code is deliberately plain: one query row at a time, both maps
+ * materialised in full for that row, max-subtracted softmax, no blocking, no
+ * fusion, no reordering.  All arithmetic is IEEE float64.  Rows are
+ * independent, so OpenMP spreads whole rows over host cores; that changes
+ * nothing in any row's arithmetic.
+ *
+ * Tensor layout: q1, k1, q2, k2 are [B, H, N, d] and v, out are [B, H, N, 2d],
+ * all contiguous row-major float64.  lambda is [H]; w is [H, 2d] or NULL
+ * (meaning all ones).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* lambda_init(l) = 0.8 - 0.6 * exp(-0.3 * (l - 1)); "Differential
+ * Transformer", section "How differential attention works", last paragraph. */
+double oracle_lambda_init(int layer)
+{
+    return 0.8 - 0.6 * exp(-0.3 * (double)(layer - 1));
+}
+
+/* Is key j visible to query i?  Causal reading: j <= i. */
+static int visible(int64_t i, int64_t j, int causal)
+{
+    return causal ? (j <= i) : 1;
+}
+
+/* One softmax row over the visible keys: logits s[j] = (q . k_j) / sqrt(d),
+ * p[j] = exp(s[j] - max) / sum.  Invisible keys get weight exactly 0. */
+static void softmax_row(int64_t i, int64_t N, int d, const double *q_row,
+                        const double *k, int causal, double *p)
+{
+    const double scale = 1.0 / sqrt((double)d);
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < N; ++j) {
+        if (!visible(i, j, causal)) {
+            p[j] = -INFINITY;
+            continue;
+        }
+        double s = 0.0;
+        for (int c = 0; c < d; ++c)
+            s += q_row[c] * k[j * d + c];
+        p[j] = s * scale;
+        if (p[j] > mx)
+            mx = p[j];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        if (!visible(i, j, causal)) {
+            p[j] = 0.0;
+            continue;
+        }
+        p[j] = exp(p[j] - mx);
+        sum += p[j];
+    }
+    for (int64_t j = 0; j < N; ++j)
+        p[j] /= sum;
+}
+
+/* Row i of the differential map of one head: w[j] = map1[i][j] - lambda *
+ * map2[i][j].  Scratch p1, p2 hold N doubles each. */
+static void diff_row(int64_t i, int64_t N, int d, const double *q1,
+                     const double *k1, const double *q2, const double *k2,
+                     double lam, int causal, double *p1, double *p2, double *w)
+{
+    softmax_row(i, N, d, q1 + i * d, k1, causal, p1);
+    softmax_row(i, N, d, q2 + i * d, k2, causal, p2);
+    for (int64_t j = 0; j < N; ++j)
+        w[j] = p1[j] - lam * p2[j];
+}
+
+/* out_row = (map1 - lambda map2)[i, :] V, then optionally the per-head RMS
+ * normalisation and the (1 - lambda_init) scale. */
+static void out_row(int64_t i, int64_t N, int d, const double *q1,
+                    const double *k1, const double *q2, const double *k2,
+                    const double *v, double lam, int causal, int headnorm,
+                    const double *w_head, double eps, double lambda_init,
+                    double *scratch, double *o)
+{
+    double *p1 = scratch, *p2 = scratch + N, *wrow = scratch + 2 * N;
+    const int dv = 2 * d;
+    diff_row(i, N, d, q1, k1, q2, k2, lam, causal, p1, p2, wrow);
+    for (int c = 0; c < dv; ++c)
+        o[c] = 0.0;
+    for (int64_t j = 0; j < N; ++j)
+        for (int c = 0; c < dv; ++c)
+            o[c] += wrow[j] * v[j * dv + c];
+    if (!headnorm)
+        return;
+    double ms = 0.0;
+    for (int c = 0; c < dv; ++c)
+        ms += o[c] * o[c];
+    ms /= (double)dv;
+    const double r = 1.0 / sqrt(ms + eps);
+    for (int c = 0; c < dv; ++c) {
+        const double g = w_head ? w_head[c] : 1.0;
+        o[c] = o[c] * r * g * (1.0 - lambda_init);
+    }
+}
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* Number of host threads OpenMP will use for the next parallel region. */
+int oracle_max_threads(int nthreads)
+{
+    set_threads(nthreads);
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Full forward: every (b, h, i).  Returns 0 on success, -1 on bad arguments,
+ * -2 if scratch could not be allocated. */
+int oracle_fwd(int B, int H, int64_t N, int d, const double *q1,
+               const double *k1, const double *q2, const double *k2,
+               const double *v, const double *lam, int causal, int headnorm,
+               const double *w, double eps, double lambda_init, double *out,
+               int nthreads)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0)
+        return -1;
+    const int64_t BH = (int64_t)B * H;
+    const int dv = 2 * d;
+    int err = 0;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double *scratch = (double *)malloc(sizeof(double) * (size_t)(3 * N + 1));
+        if (!scratch) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < BH * N; ++r) {
+            if (!scratch)
+                continue;
+            const int64_t bh = r / N, i = r % N;
+            const int h = (int)(bh % H);
+            const int64_t qk = bh * N * d, vo = bh * N * dv;
+            out_row(i, N, d, q1 + qk, k1 + qk, q2 + qk, k2 + qk, v + vo,
+                    lam[h], causal, headnorm, w ? w + (int64_t)h * dv : NULL,
+                    eps, lambda_init, scratch, out + vo + i * dv);
+        }
+        free(scratch);
+    }
+    return err;
+}
+
+/* Selected rows only: for r in [0, nrows), compute the output row of head
+ * bh_idx[r] (a flat b*H + h index) and query row_idx[r] into
+ * out_rows[r * 2d .. r * 2d + 2d).  Same arithmetic as oracle_fwd. */
+int oracle_fwd_rows(int B, int H, int64_t N, int d, const double *q1,
+                    const double *k1, const double *q2, const double *k2,
+                    const double *v, const double *lam, int causal,
+                    int headnorm, const double *w, double eps,
+                    double lambda_init, int64_t nrows, const int64_t *bh_idx,
+                    const int64_t *row_idx, double *out_rows, int nthreads)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0 || nrows < 0)
+        return -1;
+    const int64_t BH = (int64_t)B * H;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (bh_idx[r] < 0 || bh_idx[r] >= BH || row_idx[r] < 0 || row_idx[r] >= N)
+            return -1;
+    const int dv = 2 * d;
+    int err = 0;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double *scratch = (double *)malloc(sizeof(double) * (size_t)(3 * N + 1));
+        if (!scratch) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            if (!scratch)
+                continue;
+            const int64_t bh = bh_idx[r], i = row_idx[r];
+            const int h = (int)(bh % H);
+            const int64_t qk = bh * N * d, vo = bh * N * dv;
+            out_row(i, N, d, q1 + qk, k1 + qk, q2 + qk, k2 + qk, v + vo,
+                    lam[h], causal, headnorm, w ? w + (int64_t)h * dv : NULL,
+                    eps, lambda_init, scratch, out_rows + r * dv);
+        }
+        free(scratch);
+    }
+    return err;
+}
+
+/* The whole differential map of one head, wmap[i * N + j] = map1 - lambda
+ * map2 (0 where the key is masked).  This is the quantity the page's worked
+ * example prints facts about (row sums, count of negative weights). */
+int oracle_diff_map(int64_t N, int d, const double *q1, const double *k1,
+                    const double *q2, const double *k2, double lam, int causal,
+                    double *wmap)
+{
+    if (N < 0 || d <= 0)
+        return -1;
+    double *scratch = (double *)malloc(sizeof(double) * (size_t)(2 * N + 1));
+    if (!scratch)
+        return -2;
+    for (int64_t i = 0; i < N; ++i)
+        diff_row(i, N, d, q1, k1, q2, k2, lam, causal, scratch, scratch + N,
+                 wmap + i * N);
+    free(scratch);
+    return 0;
+}
+
+/* Per-head RMS normalisation alone, applied to given rows x[R, dv] of head
+ * h_idx[r]: y = x / sqrt(mean(x^2) + eps) * w[h, c] * (1 - lambda_init).
+ * The same steps out_row takes after the weighted value sum. */
+int oracle_headnorm(int64_t R, int dv, int H, const double *x,
+                    const int64_t *h_idx, const double *w, double eps,
+                    double lambda_init, double *y)
+{
+    if (R < 0 || dv <= 0 || H <= 0)
+        return -1;
+    for (int64_t r = 0; r < R; ++r) {
+        if (h_idx[r] < 0 || h_idx[r] >= H)
+            return -1;
+        const double *xr = x + r * dv;
+        double ms = 0.0;
+        for (int c = 0; c < dv; ++c)
+            ms += xr[c] * xr[c];
+        ms /= (double)dv;
+        const double inv = 1.0 / sqrt(ms + eps);
+        for (int c = 0; c < dv; ++c) {
+            const double g = w ? w[h_idx[r] * dv + c] : 1.0;
+            y[r * dv + c] = xr[c] * inv * g * (1.0 - lambda_init);
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,266 @@
+"""Pins for the float64 oracle: facts fixed by the page and by mathematics.
+
+Each pin takes a loaded oracle library handle and returns (ok, detail).  They
+are gathered here so that the same checks run against the real oracle
+(``test_oracle.py``: every pin must hold) and against deliberately broken copies
+of it (``test_oracle_mutants.py``: every planted mistake must trip at least one
+pin).  Sources, all on the "Differential Transformer" glossary page (Ultralytics;
+ja/pt/ar editions), section "How differential attention works":
+
+  * the worked example and its printed result (row sums 0.20, 13 of 36
+    weights negative);
+  * each softmax map sums to 1, so each row of map1 - lambda map2 sums to
+    1 - lambda, and weights may be negative;
+  * each map is ordinary softmax attention (so lambda = 0, or identical maps,
+    reduce to ordinary scaled-dot-product attention);
+  * each head's output is normalised on its own and then multiplied by
+    (1 - lambda_init), lambda_init(l) = 0.8 - 0.6 exp(-0.3 (l - 1)).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+from tests import bruteforce
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(None, 1)
+            vals[k] = v
+    return vals
+
+
+def _rand(seed, B, H, N, d):
+    rng = np.random.default_rng(seed)
+    q1, k1, q2, k2 = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    v = rng.standard_normal((B, H, N, 2 * d))
+    return rng, q1, k1, q2, k2, v
+
+
+def _sdpa(q, k, v, causal):
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x))
+    return F.scaled_dot_product_attention(t(q), t(k), t(v), is_causal=causal).numpy()
+
+
+def pin_pages_example(lib):
+    """The page's worked example: rows sum to 0.20 and 13 of 36 weights are negative."""
+    g = _read_golden("pages_example.txt")
+    gen = torch.Generator().manual_seed(int(g["seed"]))
+    n, d, lam = int(g["n"]), int(g["d"]), float(g["lambda"])
+    q1, k1, q2, k2 = torch.randn(4, n, d, generator=gen).double().numpy()
+    wmap = oracle.diff_map(q1, k1, q2, k2, lam, causal=False, lib=lib)
+    sums = wmap.sum(-1)
+    neg = int((wmap < 0).sum())
+    ok = (np.all(np.abs(sums - float(g["row_sum"])) < 1e-12) and neg == int(g["negative"])
+          and wmap.size == int(g["total"]))
+    return ok, f"row sums {sums}, negatives {neg} of {wmap.size}"
+
+
+def pin_row_sum(lib):
+    """Every row of map1 - lambda map2 sums to 1 - lambda (causal or not)."""
+    _, q1, k1, q2, k2, _ = _rand(11, 1, 1, 37, 16)
+    worst = 0.0
+    for causal in (False, True):
+        for lam in (0.0, 0.37, 0.8, 1.0, 1.6):
+            wmap = oracle.diff_map(q1[0, 0], k1[0, 0], q2[0, 0], k2[0, 0], lam, causal=causal,
+                                   lib=lib)
+            worst = max(worst, float(np.max(np.abs(wmap.sum(-1) - (1.0 - lam)))))
+            if causal and np.any(np.triu(wmap, 1) != 0.0):
+                return False, "masked weight is nonzero"
+    return worst < 1e-12, f"max |row sum - (1 - lambda)| = {worst:.3e}"
+
+
+def pin_lambda_zero_is_sdpa(lib):
+    """lambda = 0 leaves map1 V alone: ordinary softmax attention with scale 1/sqrt(d)."""
+    _, q1, k1, q2, k2, v = _rand(12, 2, 3, 33, 16)
+    worst = 0.0
+    for causal in (False, True):
+        o = oracle.fwd(q1, k1, q2, k2, v, np.zeros(3), causal=causal, headnorm=False, lib=lib)
+        worst = max(worst, float(np.max(np.abs(o - _sdpa(q1, k1, v, causal)))))
+    return worst < 1e-12, f"max err vs SDPA {worst:.3e}"
+
+
+def pin_identical_maps(lib):
+    """q2 = q1, k2 = k1 gives (1 - lambda_h) times ordinary attention, per head."""
+    rng, q1, k1, _, _, v = _rand(13, 2, 3, 29, 8)
+    lam = rng.uniform(-0.5, 1.5, size=3)
+    worst = 0.0
+    for causal in (False, True):
+        o = oracle.fwd(q1, k1, q1, k1, v, lam, causal=causal, headnorm=False, lib=lib)
+        ref = (1.0 - lam)[None, :, None, None] * _sdpa(q1, k1, v, causal)
+        worst = max(worst, float(np.max(np.abs(o - ref))))
+    return worst < 1e-12, f"max err {worst:.3e}"
+
+
+def pin_headnorm_lambda_free(lib):
+    """With identical maps and eps = 0 the normalised head output does not depend on
+    lambda (< 1): the (1 - lambda) factor cancels in the RMS normalisation."""
+    rng, q1, k1, _, _, v = _rand(14, 1, 2, 21, 8)
+    w = rng.uniform(0.5, 1.5, size=(2, 16))
+    outs = [oracle.fwd(q1, k1, q1, k1, v, np.full(2, lam), causal=True, headnorm=True, w=w,
+                       eps=0.0, lambda_init_value=0.35, lib=lib) for lam in (0.0, 0.3, 0.9)]
+    worst = max(float(np.max(np.abs(o - outs[0]))) for o in outs[1:])
+    return worst < 1e-11, f"max spread over lambda {worst:.3e}"
+
+
+def pin_causal_edges(lib):
+    """Causal: row 0 sees only key 0, so o_0 = (1 - lambda) v_0; the last row sees all
+    keys, so it equals the non-causal last row."""
+    rng, q1, k1, q2, k2, v = _rand(15, 1, 2, 19, 8)
+    lam = np.array([0.8, 0.25])
+    oc = oracle.fwd(q1, k1, q2, k2, v, lam, causal=True, headnorm=False, lib=lib)
+    on = oracle.fwd(q1, k1, q2, k2, v, lam, causal=False, headnorm=False, lib=lib)
+    e0 = float(np.max(np.abs(oc[0, :, 0] - (1.0 - lam)[:, None] * v[0, :, 0])))
+    e1 = float(np.max(np.abs(oc[0, :, -1] - on[0, :, -1])))
+    differs = float(np.max(np.abs(oc[0, :, 1:-1] - on[0, :, 1:-1])))
+    return e0 < 1e-14 and e1 < 1e-12 and differs > 1e-3, f"row0 {e0:.1e} last {e1:.1e}"
+
+
+def pin_headnorm_is_rms_norm(lib):
+    """The head normalisation equals torch rms_norm over the 2d channels with the
+    head's weight, times (1 - lambda_init); checked through the full forward and
+    through the standalone normalisation entry."""
+    rng, q1, k1, q2, k2, v = _rand(16, 2, 3, 17, 8)
+    lam = rng.uniform(0.1, 0.9, size=3)
+    w = rng.uniform(0.5, 1.5, size=(3, 16))
+    li = 0.6
+    worst = 0.0
+    for eps in (1e-5, 0.3):
+        raw = oracle.fwd(q1, k1, q2, k2, v, lam, causal=True, headnorm=False, lib=lib)
+        y = oracle.fwd(q1, k1, q2, k2, v, lam, causal=True, headnorm=True, w=w, eps=eps,
+                       lambda_init_value=li, lib=lib)
+        ref = np.empty_like(raw)
+        for h in range(3):
+            ref[:, h] = F.rms_norm(torch.from_numpy(raw[:, h]), (16,), torch.from_numpy(w[h]),
+                                   eps).numpy() * (1.0 - li)
+        worst = max(worst, float(np.max(np.abs(y - ref))))
+        flat = raw.reshape(-1, 16)
+        hidx = np.tile(np.repeat(np.arange(3), 17), 2)
+        y2 = oracle.headnorm(flat, hidx, w, H=3, eps=eps, lambda_init_value=li, lib=lib)
+        worst = max(worst, float(np.max(np.abs(y2 - ref.reshape(-1, 16)))))
+    return worst < 1e-12, f"max err vs rms_norm {worst:.3e}"
+
+
+def pin_headnorm_closed_form(lib):
+    """With weight 1: mean_c y^2 = (1 - lambda_init)^2 ms / (ms + eps), ms = mean_c o^2."""
+    rng, q1, k1, q2, k2, v = _rand(17, 1, 2, 23, 8)
+    lam = np.array([0.5, 0.9])
+    eps, li = 0.05, 0.25
+    raw = oracle.fwd(q1, k1, q2, k2, v, lam, causal=False, headnorm=False, lib=lib)
+    y = oracle.fwd(q1, k1, q2, k2, v, lam, causal=False, headnorm=True, eps=eps,
+                   lambda_init_value=li, lib=lib)
+    ms = (raw ** 2).mean(-1)
+    err = float(np.max(np.abs((y ** 2).mean(-1) - (1 - li) ** 2 * ms / (ms + eps))))
+    return err < 1e-12, f"max err {err:.3e}"
+
+
+def pin_permutation(lib):
+    """Non-causal: permuting the rows of K1, K2 and V together leaves the output unchanged."""
+    rng, q1, k1, q2, k2, v = _rand(18, 1, 2, 25, 8)
+    lam = np.array([0.7, 0.2])
+    perm = rng.permutation(25)
+    o = oracle.fwd(q1, k1, q2, k2, v, lam, causal=False, headnorm=False, lib=lib)
+    op = oracle.fwd(q1, k1[:, :, perm], q2, k2[:, :, perm], v[:, :, perm], lam, causal=False,
+                    headnorm=False, lib=lib)
+    err = float(np.max(np.abs(o - op)))
+    return err < 1e-12, f"max err {err:.3e}"
+
+
+def pin_linear_in_v(lib):
+    """Without the normalisation the output is linear in V."""
+    rng, q1, k1, q2, k2, v = _rand(19, 1, 2, 14, 8)
+    v2 = rng.standard_normal(v.shape)
+    lam = np.array([0.8, 0.4])
+    f = lambda vv: oracle.fwd(q1, k1, q2, k2, vv, lam, causal=True, headnorm=False, lib=lib)
+    err = float(np.max(np.abs(f(2.5 * v - 0.75 * v2) - (2.5 * f(v) - 0.75 * f(v2)))))
+    return err < 1e-12, f"max err {err:.3e}"
+
+
+def pin_zero_queries(lib):
+    """Zero queries give uniform maps: o_i = (1 - lambda) mean of the visible v_j."""
+    rng, _, k1, _, k2, v = _rand(20, 1, 2, 11, 8)
+    q = np.zeros_like(k1)
+    lam = np.array([0.8, -0.3])
+    worst = 0.0
+    for causal in (False, True):
+        o = oracle.fwd(q, k1, q, k2, v, lam, causal=causal, headnorm=False, lib=lib)
+        if causal:
+            ref = np.cumsum(v, axis=2) / np.arange(1, 12)[None, None, :, None]
+        else:
+            ref = np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape)
+        ref = (1.0 - lam)[None, :, None, None] * ref
+        worst = max(worst, float(np.max(np.abs(o - ref))))
+    return worst < 1e-13, f"max err {worst:.3e}"
+
+
+def pin_bruteforce(lib):
+    """Pure-Python loops on tiny shapes agree to 1e-12."""
+    worst = 0.0
+    for seed, (B, H, N, d), causal in [(21, (1, 1, 1, 1), True), (22, (1, 2, 5, 3), False),
+                                       (23, (2, 2, 16, 8), True), (24, (1, 3, 9, 4), False)]:
+        rng, q1, k1, q2, k2, v = _rand(seed, B, H, N, d)
+        lam = rng.uniform(-0.2, 1.2, size=H)
+        w = rng.uniform(0.5, 1.5, size=(H, 2 * d))
+        for headnorm in (False, True):
+            o = oracle.fwd(q1, k1, q2, k2, v, lam, causal=causal, headnorm=headnorm, w=w,
+                           eps=1e-3, lambda_init_value=0.45, lib=lib)
+            for b in range(B):
+                for h in range(H):
+                    ref = bruteforce.head_forward(q1[b, h].tolist(), k1[b, h].tolist(),
+                                                  q2[b, h].tolist(), k2[b, h].tolist(),
+                                                  v[b, h].tolist(), float(lam[h]), causal,
+                                                  headnorm, w[h].tolist(), 1e-3, 0.45)
+                    worst = max(worst, float(np.max(np.abs(o[b, h] - np.array(ref)))))
+    return worst < 1e-12, f"max err {worst:.3e}"
+
+
+def pin_lambda_init(lib):
+    """lambda_init(1) = 0.8 - 0.6 = 0.2; it rises with depth towards 0.8."""
+    vals = [oracle.lambda_init(l, lib=lib) for l in range(1, 60)]
+    ok = (abs(vals[0] - 0.2) < 1e-15 and all(b > a for a, b in zip(vals, vals[1:]))
+          and abs(oracle.lambda_init(400, lib=lib) - 0.8) < 1e-15
+          and abs(vals[1] - (0.8 - 0.6 / math.e ** 0.3)) < 1e-15)
+    return ok, f"l=1 {vals[0]!r}, l=2 {vals[1]!r}, l=59 {vals[-1]!r}"
+
+
+def pin_rows_match_full(lib):
+    """The selected-rows entry computes the same rows as the full forward."""
+    rng, q1, k1, q2, k2, v = _rand(25, 2, 3, 20, 8)
+    lam = rng.uniform(0.1, 0.9, size=3)
+    w = rng.uniform(0.5, 1.5, size=(3, 16))
+    kw = dict(causal=True, headnorm=True, w=w, eps=1e-5, lambda_init_value=0.3, lib=lib)
+    full = oracle.fwd(q1, k1, q2, k2, v, lam, **kw)
+    bh = rng.integers(0, 6, size=40)
+    ri = rng.integers(0, 20, size=40)
+    rows = oracle.fwd_rows(q1, k1, q2, k2, v, lam, bh, ri, **kw)
+    err = float(np.max(np.abs(rows - full.reshape(6, 20, 16)[bh, ri])))
+    return err == 0.0, f"max err {err:.3e}"
+
+
+PINS = {name[4:]: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
+
+
+def run_pins(lib):
+    """Run every pin; returns {name: (ok, detail)}.  An exception counts as a failure."""
+    res = {}
+    for name, fn in PINS.items():
+        try:
+            with np.errstate(all="ignore"):
+                ok, detail = fn(lib)
+            res[name] = (bool(ok), detail)
+        except Exception as e:  # a crash is a failed pin
+            res[name] = (False, f"{type(e).__name__}: {e}")
+    return res

@@ -1,0 +1,60 @@
+"""Plant plausible mistakes in copies of the C oracle and check that the pins catch each.
+
+Every mutant is a textual edit of a temporary copy of oracle/diffattn_oracle.c,
+compiled with gcc on the CPU; the real oracle is never modified.  A mutant that
+passes every pin would show a hole in the pins.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from tests import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "diffattn_oracle.c")
+
+# (name, original text, mutated text)
+MUTANTS = [
+    ("plus_lambda", "w[j] = p1[j] - lam * p2[j];", "w[j] = p1[j] + lam * p2[j];"),
+    ("no_scale", "const double scale = 1.0 / sqrt((double)d);", "const double scale = 1.0;"),
+    ("scale_by_2d", "const double scale = 1.0 / sqrt((double)d);",
+     "const double scale = 1.0 / sqrt((double)(2 * d));"),
+    ("strict_mask", "return causal ? (j <= i) : 1;", "return causal ? (j < i || j == 0) : 1;"),
+    ("reversed_mask", "return causal ? (j <= i) : 1;", "return causal ? (j >= i) : 1;"),
+    ("causal_ignored", "return causal ? (j <= i) : 1;", "return 1;"),
+    ("transposed_k", "s += q_row[c] * k[j * d + c];", "s += q_row[c] * k[c * N + j];"),
+    ("map2_uses_q1", "softmax_row(i, N, d, q2 + i * d, k2, causal, p2);",
+     "softmax_row(i, N, d, q1 + i * d, k2, causal, p2);"),
+    ("unnormalised_map", "p[j] /= sum;", "p[j] /= 1.0;"),
+    ("v_columns_reversed", "o[c] += wrow[j] * v[j * dv + c];",
+     "o[c] += wrow[j] * v[j * dv + (dv - 1 - c)];"),
+    ("norm_over_d", "ms /= (double)dv;", "ms /= (double)(dv / 2);"),
+    ("eps_outside_sqrt", "const double r = 1.0 / sqrt(ms + eps);",
+     "const double r = 1.0 / (sqrt(ms) + eps);"),
+    ("no_lambda_init_scale", "o[c] = o[c] * r * g * (1.0 - lambda_init);",
+     "o[c] = o[c] * r * g;"),
+    ("lambda_init_not_one_based", "exp(-0.3 * (double)(layer - 1))", "exp(-0.3 * (double)(layer))"),
+    ("lambda_init_sign", "0.8 - 0.6 * exp(", "0.8 + 0.6 * exp("),
+    ("lambda_of_head0", "lam[h], causal, headnorm, w ? w + (int64_t)h * dv : NULL,\n"
+     "                    eps, lambda_init, scratch, out + vo + i * dv);",
+     "lam[0], causal, headnorm, w ? w + (int64_t)h * dv : NULL,\n"
+     "                    eps, lambda_init, scratch, out + vo + i * dv);"),
+    ("weight_of_head0", "lam[h], causal, headnorm, w ? w + (int64_t)h * dv : NULL,\n"
+     "                    eps, lambda_init, scratch, out + vo + i * dv);",
+     "lam[h], causal, headnorm, w ? w : NULL,\n"
+     "                    eps, lambda_init, scratch, out + vo + i * dv);"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, orig, mut):
+    text = open(SRC).read()
+    assert text.count(orig) >= 1, f"mutation site for {name} not found"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(orig, mut))
+    lib_path = oracle.build(force=True, src=str(src), out=str(tmp_path / "libmutant.so"))
+    lib = oracle.load(lib_path)
+    res = pins.run_pins(lib)
+    failed = [k for k, (ok, _) in res.items() if not ok]
+    assert failed, f"mutant {name} passed every pin"
