@@ -1,0 +1,409 @@
+"""Benchmark of the differential-attention head forward on GB300.
+
+One step = one pass of the whole hot path (the fused bf16 forward, including
+the head-norm epilogue) over one batch of the needle-style causal workload
+B=2, H=16, N=4096, d=64 (value width 128).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Metric: algorithmic TFLOP/s with 8*d flops per visible (query, key) pair
+(2*d for each of the two Q K^T maps, 4*d for one combined map times V of
+width 2d) and the causal half convention B*H*N^2/2 pairs.  Under torchrun each
+rank runs its own copy of the workload (weak scaling, no data-path
+collective); value = flops of all ranks / max over ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+WORKLOAD = "needle_4k"
+METRIC = "diff-attn fwd TFLOP/s (causal, bf16) and % of GB300 tensor peak, 1 GPU"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["differential_attention_attn_gb300/csrc/fwd_bf16_sm103.cu",
+                  "differential_attention_attn_gb300/csrc/ptx.cuh"]
+
+
+def alg_flops(B, H, N, d, causal=True) -> float:
+    pairs = B * H * N * N * (0.5 if causal else 1.0)
+    return 8.0 * d * pairs
+
+
+def alg_bytes(B, H, N, d, elem=2) -> float:
+    # q1, k1, q2, k2 (4 * d) + v (2d) in, out (2d) out, per token per head
+    return float(B * H * N * (4 * d + 2 * d + 2 * d) * elem)
+
+
+def row_flops(i, d, causal=True) -> float:
+    return 8.0 * d * ((i + 1) if causal else 1)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None if that summary was taken on a different kernel source."""
+    path = os.path.join(PROFILES, f"traffic_fwd_bf16_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#") and " " in line:
+                k, v = line.split(None, 1)
+                vals[k] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (100 ms period)."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t_start = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    @staticmethod
+    def _ts(s):
+        from datetime import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.strptime(s.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append((self._ts(f[0]), float(f[2]), float(f[3]), f[5:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "none"}
+        inside = [r for r in rows if r[0] is not None and t0 - 0.1 <= r[0] <= t1 + 0.1]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "whole run (timed region shorter than the sampling period)"
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def cpu_baseline(w, seconds: float, seed: int = 3):
+    """Time the float64 oracle on a bounded, seeded sample of the workload's rows.
+
+    Rows are drawn uniformly over (head, query) so that their mean causal length
+    matches the workload's; the value is algorithmic TFLOP/s of those rows."""
+    import oracle
+    from tests import harness
+
+    args, kw = harness.oracle_args(w)
+    rng = np.random.default_rng(seed)
+    BH, N = w.B * w.H, w.N
+    cores = oracle.max_threads(0)
+
+    def run(n):
+        bh = rng.integers(0, BH, size=n)
+        ri = rng.integers(0, N, size=n)
+        t = time.perf_counter()
+        oracle.fwd_rows(*args, bh, ri, **kw)
+        dt = time.perf_counter() - t
+        return dt, float(sum(row_flops(int(i), w.d, w.causal) for i in ri))
+
+    n = 2 * cores
+    dt, fl = run(n)
+    while dt < 0.5 and n < 1 << 20:
+        n *= 4
+        dt, fl = run(n)
+    n_final = max(n, int(n * seconds / max(dt, 1e-6)))
+    dt, fl = run(n_final)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_final} query rows drawn uniformly over the {BH} heads x {N} rows "
+                      f"of {w.name} (causal), full float64 oracle per row; {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: rank 0 only, host cores, bounded samples."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from differential_attention_attn_gb300 import workloads as W
+    from tests import harness
+
+    w = W.make(WORKLOAD)
+    oargs, kw = harness.oracle_args(w)
+    rng = np.random.default_rng(11)
+    BH, N = w.B * w.H, w.N
+    cores = oracle.max_threads(0)
+
+    def step(n):
+        bh = rng.integers(0, BH, size=n)
+        ri = rng.integers(0, N, size=n)
+        t = time.perf_counter()
+        oracle.fwd_rows(*oargs, bh, ri, **kw)
+        return time.perf_counter() - t, float(sum(row_flops(int(i), w.d) for i in ri))
+
+    n = 2 * cores
+    dt, _ = step(n)
+    target = 1.0  # seconds of CPU work per step
+    n = max(n, int(n * target / max(dt, 1e-6)))
+    for _ in range(max(args.warmup, 0)):
+        step(n)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = step(n)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dv": 2 * w.d,
+                   "causal": True, "headnorm": True,
+                   "sample_per_step": f"{n} query rows drawn uniformly over heads x rows"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} rows per step x {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    from differential_attention_attn_gb300 import ops
+    from differential_attention_attn_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ops.load()
+
+    w = W.make(WORKLOAD, seed_offset=rank)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    li = float(np.float32(w.lambda_init_override if w.layer is None
+                          else ops.lambda_init(w.layer)))
+    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device=dev)
+    norm_w = None if w.w is None else torch.tensor(w.w, dtype=torch.float32, device=dev)
+    host = [t.contiguous() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    set_bytes = sum(t.numel() * t.element_size() for t in host) + B * H * N * 2 * d * 2
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    sets = []
+    for _ in range(n_sets):
+        ins = [t.to(dev) for t in host]
+        out = torch.empty((B, H, N, 2 * d), dtype=torch.bfloat16, device=dev)
+        sets.append((ins, out))
+    stream = torch.cuda.current_stream()
+    kw = dict(causal=True, headnorm=True, norm_w=norm_w, eps=float(np.float32(w.eps)),
+              lambda_init=li, stream=stream)
+
+    def step(i):
+        ins, out = sets[i % n_sets]
+        ops.fwd(*ins, lam, out=out, **kw)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+
+    # e2e: the same call through the public API with host buffers, copies timed.
+    pinned = [t.pin_memory() for t in host]
+    dev_in = [torch.empty_like(t, device=dev) for t in host]
+    dev_out = torch.empty((B, H, N, 2 * d), dtype=torch.bfloat16, device=dev)
+    host_out = torch.empty((B, H, N, 2 * d), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        for dst, src in zip(dev_in, pinned):
+            dst.copy_(src, non_blocking=True)
+        ops.fwd(*dev_in, lam, out=dev_out, **kw)
+        host_out.copy_(dev_out, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, args.steps)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+
+    times = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_total, e2e_ms = float(times[0]), float(times[1])
+    flops_step = alg_flops(B, H, N, d)
+    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    launch_ms = ms_total / args.steps
+    achieved = flops_step / (launch_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = read_peaks()
+    peak = float(peaks["bf16_tflops"])
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": d, "dv": 2 * d,
+                   "causal": True, "headnorm": True,
+                   "flops_convention": "8*d per visible pair, B*H*N^2/2 pairs",
+                   "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
+                         f"(> {L2_BYTES / 1e6:.0f} MB L2)",
+                   "parallelism": f"weak x{world} (one full workload per rank)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak,
+                     "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS bf16 GEMM)",
+                     "kernel": "diffattn_fwd_bf16_sm103_kernel",
+                     "alg_flops_per_launch": flops_step,
+                     "alg_bytes_per_launch": alg_bytes(B, H, N, d),
+                     "achieved_gbs": alg_bytes(B, H, N, d) / (launch_ms * 1e-3) / 1e9,
+                     "traffic": read_traffic(WORKLOAD)},
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
+                "d2h_bytes_per_step": int(host_out.numel() * host_out.element_size())},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

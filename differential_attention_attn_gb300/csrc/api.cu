@@ -1,0 +1,100 @@
+// C ABI of libdiffattn: argument validation, dispatch and status codes.
+// Every entry point is declared, with its contract, in include/diffattn.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace {
+
+using namespace diffattn;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Fields shared by every entry point.
+diffattn_status check_desc(const diffattn_desc *desc) {
+  if (desc == nullptr) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->B < 0 || desc->H < 0 || desc->N < 0 || desc->d <= 0) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->dtype != DIFFATTN_BF16 && desc->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID_ARG;
+  if (!(desc->eps >= 0.f) || !std::isfinite(desc->eps) || !std::isfinite(desc->lambda_init))
+    return DIFFATTN_ERR_INVALID_ARG;
+  // B * H * N * 2d elements must be addressable with 64-bit offsets.
+  const double elems = static_cast<double>(desc->B) * static_cast<double>(desc->H) *
+                       static_cast<double>(desc->N) * 2.0 * static_cast<double>(desc->d);
+  if (elems > 9.0e18) return DIFFATTN_ERR_INVALID_ARG;
+  return DIFFATTN_OK;
+}
+
+// The bf16 kernel is built for sm_103a only.
+diffattn_status check_sm103() {
+  static int cached[64];  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return DIFFATTN_ERR_CUDA;
+    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return cached[dev] == 1 ? DIFFATTN_OK : DIFFATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
+                             const void *q2, const void *k2, const void *v, const float *lambda,
+                             const float *norm_w, void *out, void *stream) {
+  diffattn_status st = check_desc(desc);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out) return DIFFATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (desc->dtype == DIFFATTN_BF16) {
+    if (desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(out))
+      return DIFFATTN_ERR_INVALID_ARG;
+    if ((st = check_sm103()) != DIFFATTN_OK) return st;
+    return launch_fwd_bf16_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w, out, s);
+  }
+  if (desc->d > kF32MaxD || desc->N > kF32MaxN) return DIFFATTN_ERR_UNSUPPORTED;
+  return launch_fwd_f32(*desc, static_cast<const float *>(q1), static_cast<const float *>(k1),
+                        static_cast<const float *>(q2), static_cast<const float *>(k2),
+                        static_cast<const float *>(v), lambda, norm_w, static_cast<float *>(out),
+                        s);
+}
+
+diffattn_status diffattn_headnorm(const diffattn_desc *desc, const float *x, const float *norm_w,
+                                  void *out, void *stream) {
+  diffattn_status st = check_desc(desc);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!x || !out) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->d > kF32MaxD) return DIFFATTN_ERR_UNSUPPORTED;
+  return launch_headnorm(*desc, x, norm_w, out, static_cast<cudaStream_t>(stream));
+}
+
+double diffattn_lambda_init(int layer) {
+  return 0.8 - 0.6 * std::exp(-0.3 * (static_cast<double>(layer) - 1.0));
+}
+
+const char *diffattn_strerror(diffattn_status status) {
+  switch (status) {
+    case DIFFATTN_OK: return "ok";
+    case DIFFATTN_ERR_INVALID_ARG: return "invalid argument";
+    case DIFFATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DIFFATTN_ERR_CUDA: return "CUDA error";
+    case DIFFATTN_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+int diffattn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,504 @@
+// Fused differential-attention head forward, bf16 in / bf16 out, fp32
+// accumulation, for sm_103a (GB300): TMA loads, tcgen05 MMAs with TMEM
+// accumulators, two online softmax states per query row and a fused RMS
+// head-norm epilogue.
+//
+// The method ("Differential Transformer", Ultralytics glossary, section "How
+// differential attention works"): two softmax maps per head from two
+// query/key halves, combined as (map1 - lambda map2) V with V twice as wide
+// as a half; each head's output normalised on its own, then scaled by
+// (1 - lambda_init).  The page notes that each map is ordinary softmax
+// attention; that is what makes the flash-style online softmax below valid
+// for each map separately.
+//
+// Work item: one (batch*head, 128-row query tile).  Per key tile of 128 keys:
+//   S1 = Q1 K1^T, S2 = Q2 K2^T              tcgen05 SS MMAs into TMEM
+//   P_k = exp2(S_k * log2(e)/sqrt(d) - m_k)  per map, thread-per-row softmax
+//   O1 += P1 V, O2 += P2 V                   tcgen05 TS MMAs (P read from TMEM)
+// and at the end o = O1/l1 - lambda O2/l2, then the RMS norm over the 128
+// value channels, the weight, the (1 - lambda_init) scale and a bf16 store.
+//
+// One accumulator per map is needed: the two maps have independent running
+// maxima and sums, so a single running (P1 - lambda P2) V cannot be
+// renormalised exactly once the final sums are known.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator and MMA issuer (one lane)
+//   warps 2-3   idle
+//   warps 4-7   softmax of map 1 (thread t owns query row t: TMEM lane t)
+//   warps 8-11  softmax of map 2
+// The epilogue is split by value columns: map-1 warps do columns 0-63, map-2
+// warps columns 64-127, exchanging 1/l and partial sums of squares through
+// shared memory.
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0,128) S1 (P1 as packed bf16 over its first 64 columns)
+//   [128,256) S2 (P2 likewise)   [256,384) O1   [384,512) O2
+//
+// MMA issue order per key tile j keeps the tensor pipe busy while the
+// softmax of the other map runs:  S1_j, PV2_{j-1}, S2_j, PV1_j.  tcgen05 MMAs
+// from one thread execute in order, so S_k of tile j+1 never overwrites P_k
+// of tile j before PV_k of tile j has read it, and the commit that publishes
+// S_k of tile j also certifies that PV_k of tile j-1 is complete (which the
+// softmax needs before it rescales O_k).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace diffattn {
+namespace {
+
+constexpr int BM = 128;          // query rows per tile (TMEM lanes)
+constexpr int BN = 128;          // keys per key tile
+constexpr int HD = 64;           // query/key half width d
+constexpr int DV = 2 * HD;       // value width 2d
+constexpr int STAGES = 2;        // K/V pipeline depth
+constexpr int NUM_THREADS = 384;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+
+constexpr uint32_t TILE_QK_BYTES = BM * HD * 2;     // 16 KB: one [128 x 64] bf16 tile
+constexpr uint32_t TILE_V_BYTES = BN * DV * 2;      // 32 KB: two [128 x 64] column blocks
+constexpr uint32_t OFF_Q1 = 0;
+constexpr uint32_t OFF_Q2 = OFF_Q1 + TILE_QK_BYTES;
+constexpr uint32_t OFF_STAGES = OFF_Q2 + TILE_QK_BYTES;
+constexpr uint32_t STAGE_K1 = 0;
+constexpr uint32_t STAGE_K2 = TILE_QK_BYTES;
+constexpr uint32_t STAGE_V = 2 * TILE_QK_BYTES;
+constexpr uint32_t STAGE_BYTES = 2 * TILE_QK_BYTES + TILE_V_BYTES;
+constexpr uint32_t OFF_CTRL = OFF_STAGES + STAGES * STAGE_BYTES;
+
+struct Ctrl {
+  uint64_t q_full;
+  uint64_t k_full[STAGES];
+  uint64_t v_full[STAGES];
+  uint64_t kv_empty[STAGES];
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr uint32_t SMEM_BYTES = OFF_CTRL + sizeof(Ctrl) + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
+static_assert(OFF_STAGES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "SW128 tiles need 1 KB alignment");
+
+constexpr uint32_t TMEM_COLS = 512;
+__host__ __device__ constexpr uint32_t tm_s(int k) { return 128u * k; }        // S_k / P_k
+__host__ __device__ constexpr uint32_t tm_o(int k) { return 256u + 128u * k; }  // O_k
+
+constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;   // 2 s per pipeline wait
+constexpr uint64_t DRAIN_TIMEOUT_NS = 200000000ull;   // 0.2 s to drain in-flight copies
+
+struct Params {
+  int64_t BH;
+  int32_t H;
+  int32_t N;
+  int32_t n_qtiles;
+  int32_t n_ktiles;
+  int32_t causal;
+  int32_t headnorm;
+  float scale_log2;   // log2(e) / sqrt(d)
+  float eps;
+  float out_scale;    // 1 - lambda_init
+  const float *lambda;
+  const float *norm_w;
+  __nv_bfloat16 *out;
+  int32_t *status;
+};
+
+__device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > DRAIN_TIMEOUT_NS) return false;
+  }
+  return true;
+}
+
+// K-major SW128 operand descriptor of a [rows x 64] bf16 tile, advanced to
+// the 16-element K slice `kk`.
+__device__ __forceinline__ uint64_t desc_kmajor(const uint8_t *tile, int kk) {
+  return smem_desc_sw128(smem_u32(tile) + kk * 32, 16, 1024);
+}
+
+// MN-major SW128 descriptor of the V tile ([128 keys x 128 values] stored as
+// two [128 x 64] column blocks 16 KB apart), advanced to keys [16 kk, 16 kk + 16).
+__device__ __forceinline__ uint64_t desc_v(const uint8_t *vtile, int kk) {
+  return smem_desc_sw128(smem_u32(vtile) + kk * 16 * 128, TILE_QK_BYTES, 1024);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    diffattn_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
+                                   const __grid_constant__ CUtensorMap tm_k1,
+                                   const __grid_constant__ CUtensorMap tm_q2,
+                                   const __grid_constant__ CUtensorMap tm_k2,
+                                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + OFF_CTRL);
+  volatile int *abort_flag = &ctrl->abort;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // Heaviest tiles first: all heads' last query tiles, then the previous ones.
+  const int64_t item = blockIdx.x;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(item / p.BH);
+  const int64_t bh = item % p.BH;
+  const int h = static_cast<int>(bh % p.H);
+  const int q0 = qt * BM;
+  const int n_kv = p.causal ? (qt + 1) : p.n_ktiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctrl->k_full[s], 1);
+      mbar_init(&ctrl->v_full[s], 1);
+      mbar_init(&ctrl->kv_empty[s], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&ctrl->s_full[k], 1);
+      mbar_init(&ctrl->p_ready[k], BM);
+    }
+    mbar_init(&ctrl->o_done, 1);
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q1);
+    tma_prefetch_desc(&tm_k1);
+    tma_prefetch_desc(&tm_q2);
+    tma_prefetch_desc(&tm_k2);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      mbar_arrive_expect_tx(&ctrl->q_full, 2 * TILE_QK_BYTES);
+      tma_load_3d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, q0, static_cast<int32_t>(bh));
+      tma_load_3d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, q0, static_cast<int32_t>(bh));
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % STAGES;
+        const uint32_t u = static_cast<uint32_t>(j / STAGES);
+        if (u > 0 && !mbar_wait(&ctrl->kv_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
+          break;
+        uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
+        const int32_t y = j * BN;
+        mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * TILE_QK_BYTES);
+        tma_load_3d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, static_cast<int32_t>(bh));
+        tma_load_3d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, static_cast<int32_t>(bh));
+        mbar_arrive_expect_tx(&ctrl->v_full[s], TILE_V_BYTES);
+        tma_load_3d(st + STAGE_V, &tm_v, &ctrl->v_full[s], 0, y, static_cast<int32_t>(bh));
+        tma_load_3d(st + STAGE_V + TILE_QK_BYTES, &tm_v, &ctrl->v_full[s], HD, y,
+                    static_cast<int32_t>(bh));
+        issued[s] = u + 1;
+      }
+      // Never leave with a copy in flight: wait (bounded) for every issued load.
+      drain_wait(&ctrl->q_full, 0);
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued[s] > 0) {
+          drain_wait(&ctrl->k_full[s], (issued[s] - 1) & 1);
+          drain_wait(&ctrl->v_full[s], (issued[s] - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
+      const uint8_t *sq[2] = {smem + OFF_Q1, smem + OFF_Q2};
+      auto qk = [&](int k, const uint8_t *st) {
+        const uint8_t *kt = st + (k == 0 ? STAGE_K1 : STAGE_K2);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(tmem + tm_s(k), desc_kmajor(sq[k], kk), desc_kmajor(kt, kk), IDESC_QK,
+                       kk > 0);
+      };
+      auto pv = [&](int k, const uint8_t *st, bool accumulate) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_bf16_ts(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, desc_v(st + STAGE_V, kk),
+                       IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag, WAIT_TIMEOUT_NS);
+      tc_fence_after_sync();
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % STAGES;
+        const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1;
+        const uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
+        if (!(ok = mbar_wait(&ctrl->k_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+        tc_fence_after_sync();
+        qk(0, st);
+        umma_commit(&ctrl->s_full[0]);
+        if (j > 0) {
+          if (!(ok = mbar_wait(&ctrl->p_ready[1], (j - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+            break;
+          tc_fence_after_sync();
+          const int sp = (j - 1) % STAGES;
+          pv(1, smem + OFF_STAGES + sp * STAGE_BYTES, j - 1 > 0);
+          umma_commit(&ctrl->kv_empty[sp]);
+        }
+        qk(1, st);
+        umma_commit(&ctrl->s_full[1]);
+        if (!(ok = mbar_wait(&ctrl->v_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+        if (!(ok = mbar_wait(&ctrl->p_ready[0], j & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+        tc_fence_after_sync();
+        pv(0, st, j > 0);
+      }
+      if (ok && n_kv > 0) {
+        const int jl = n_kv - 1;
+        if (mbar_wait(&ctrl->p_ready[1], jl & 1, abort_flag, WAIT_TIMEOUT_NS)) {
+          tc_fence_after_sync();
+          const int sl = jl % STAGES;
+          pv(1, smem + OFF_STAGES + sl * STAGE_BYTES, jl > 0);
+          umma_commit(&ctrl->kv_empty[sl]);
+          umma_commit(&ctrl->o_done);
+        }
+      }
+      // Never free tensor memory under a running MMA: wait for all of them.
+      umma_commit(&ctrl->drain);
+      drain_wait(&ctrl->drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax
+    const int k = (warp - 4) / 4;        // which map
+    const int r = (warp % 4) * 32 + lane;  // query row within the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + tm_s(k);
+    const uint32_t t_o = tmem + lane_addr + tm_o(k);
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY;  // reference maximum (log2 units) used by the exponentials
+    float l_run = 0.f;        // running sum of exp2(x - m_run)
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = mbar_wait(&ctrl->s_full[k], j & 1, abort_flag, WAIT_TIMEOUT_NS);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t sr[2][64];
+      tmem_ld_x64(t_s, sr[0]);
+      tmem_ld_x64(t_s + 64, sr[1]);
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c / 64][c % 64]);
+      const int kv0 = j * BN;
+      if (p.causal && kv0 + BN > q0 + r + 1) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (kv0 + c > q0 + r) s[c] = -INFINITY;
+      }
+      if (!p.causal && kv0 + BN > p.N) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (kv0 + c >= p.N) s[c] = -INFINITY;
+      }
+      float mt = s[0];
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mt = fmaxf(mt, s[c]);
+      const float m_new = fmaxf(m_run, mt * sl2);
+      float alpha = 1.f;
+      if (j == 0) {
+        m_run = m_new;
+      } else if (m_new > m_run + RESCALE_THRESHOLD) {
+        alpha = ex2_approx(m_run - m_new);
+        m_run = m_new;
+      }
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        // O_k of this row is complete up to tile j-1 (certified by s_full).
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(t_o + c0, o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st_x32(t_o + c0, o);
+        }
+      }
+      l_run *= alpha;
+      const float msub = m_run;
+      float rs = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < BN / 2; ++c) {
+        const float a = ex2_approx(fmaf(s[2 * c], sl2, -msub));
+        const float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -msub));
+        rs += a + b;
+        pk[c / 32][c % 32] = pack_bf16x2(a, b);
+      }
+      l_run += rs;
+      tmem_st_x32(t_s, pk[0]);
+      tmem_st_x32(t_s + 32, pk[1]);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->p_ready[k]);
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    if (ok) ok = mbar_wait(&ctrl->o_done, 0, abort_flag, WAIT_TIMEOUT_NS);
+    // Both warpgroups take the same branch: the barrier ORs every thread's view.
+    const bool failed = named_barrier_or(1, 256, !ok || *abort_flag != 0);
+    if (!failed) {
+      tc_fence_after_sync();
+      float *xch = reinterpret_cast<float *>(smem + OFF_Q1);  // Q tiles are dead now
+      xch[k * BM + r] = 1.f / l_run;
+      named_barrier_sync(1, 256);
+      const float inv1 = xch[r];
+      const float c2 = p.lambda[h] * xch[BM + r];
+      const int col0 = k * (DV / 2);
+      uint32_t o1r[64], o2r[64];
+      tmem_ld_x64(tmem + lane_addr + tm_o(0) + col0, o1r);
+      tmem_ld_x64(tmem + lane_addr + tm_o(1) + col0, o2r);
+      float o[64];
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        o[c] = __uint_as_float(o1r[c]) * inv1 - __uint_as_float(o2r[c]) * c2;
+        ss = fmaf(o[c], o[c], ss);
+      }
+      if (p.headnorm) {
+        xch[2 * BM + k * BM + r] = ss;
+        named_barrier_sync(1, 256);
+        const float tot = xch[2 * BM + r] + xch[3 * BM + r];
+        const float rr = rsqrtf(tot * (1.f / DV) + p.eps) * p.out_scale;
+        const float *w = p.norm_w ? p.norm_w + static_cast<int64_t>(h) * DV + col0 : nullptr;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? __ldg(w + c) : 1.f);
+      }
+      if (q0 + r < p.N) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (bh * p.N + q0 + r) * DV + col0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint4 pkt;
+          pkt.x = pack_bf16x2(o[8 * v + 0], o[8 * v + 1]);
+          pkt.y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
+          pkt.z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
+          pkt.w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
+          dst[v] = pkt;
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && *abort_flag && p.status != nullptr)
+    atomicExch(p.status, static_cast<int32_t>(DIFFATTN_ERR_TIMEOUT));
+}
+
+// cuTensorMapEncodeTiled is a driver entry point; it is looked up through the
+// runtime so that the library itself does not link against the driver.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+CUresult encode_tile_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t n,
+                         uint64_t bh) {
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (encode == nullptr) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[3] = {inner, n, bh};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * n};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
+                                      const void *q2, const void *k2, const void *v,
+                                      const float *lambda, const float *norm_w, void *out,
+                                      cudaStream_t stream) {
+  const int64_t BH = desc.B * desc.H;
+  const int64_t N = desc.N;
+  const int64_t n_qtiles = (N + BM - 1) / BM;
+  if (BH * n_qtiles > INT32_MAX || N > INT32_MAX / 2 || desc.H > INT32_MAX)
+    return DIFFATTN_ERR_UNSUPPORTED;
+
+  CUtensorMap maps[5];
+  const void *bases[5] = {q1, k1, q2, k2, v};
+  for (int i = 0; i < 5; ++i) {
+    const uint64_t inner = (i == 4) ? DV : HD;
+    if (encode_tile_map(&maps[i], bases[i], inner, static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(BH)) != CUDA_SUCCESS)
+      return DIFFATTN_ERR_CUDA;
+  }
+
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+      return DIFFATTN_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+
+  Params p;
+  p.BH = BH;
+  p.H = static_cast<int32_t>(desc.H);
+  p.N = static_cast<int32_t>(N);
+  p.n_qtiles = static_cast<int32_t>(n_qtiles);
+  p.n_ktiles = static_cast<int32_t>(n_qtiles);
+  p.causal = desc.causal ? 1 : 0;
+  p.headnorm = desc.headnorm ? 1 : 0;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
+  p.eps = desc.eps;
+  p.out_scale = 1.0f - desc.lambda_init;
+  p.lambda = lambda;
+  p.norm_w = norm_w;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.status = desc.status_dev;
+
+  dim3 grid(static_cast<unsigned>(BH * n_qtiles));
+  diffattn_fwd_bf16_sm103_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+}  // namespace diffattn

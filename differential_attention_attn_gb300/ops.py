@@ -1,0 +1,169 @@
+"""ctypes binding of libdiffattn (include/diffattn.h): argument marshalling only.
+
+Every computation runs inside the library's CUDA kernels.  PyTorch supplies
+device memory and the current stream; this module only checks that tensors
+have the layout the C ABI documents, then passes raw pointers.  If the shared
+library has not been built, the first call raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdiffattn.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "diffattn.h")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+BF16, F32 = 0, 1
+_DTYPE_CODE = {torch.bfloat16: BF16, torch.float32: F32}
+
+
+class DiffAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libdiffattn status {status}: {message}")
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    """Mirror of `diffattn_desc` in include/diffattn.h."""
+    _fields_ = [
+        ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
+        ("d", ctypes.c_int32), ("dtype", ctypes.c_int32), ("causal", ctypes.c_int32),
+        ("headnorm", ctypes.c_int32), ("eps", ctypes.c_float), ("lambda_init", ctypes.c_float),
+        ("status_dev", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libdiffattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        vp, fp = ctypes.c_void_p, ctypes.c_void_p
+        dp = ctypes.POINTER(Desc)
+        lib.diffattn_fwd.restype = ctypes.c_int
+        lib.diffattn_fwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp]
+        lib.diffattn_headnorm.restype = ctypes.c_int
+        lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
+        lib.diffattn_lambda_init.restype = ctypes.c_double
+        lib.diffattn_lambda_init.argtypes = [ctypes.c_int]
+        lib.diffattn_strerror.restype = ctypes.c_char_p
+        lib.diffattn_strerror.argtypes = [ctypes.c_int]
+        lib.diffattn_version.restype = ctypes.c_int
+        lib.diffattn_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def declared_symbols(header: str = HEADER_PATH) -> list[str]:
+    """Names of the functions include/diffattn.h declares."""
+    text = open(header).read()
+    return sorted(set(re.findall(r"\b(diffattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def strerror(status: int) -> str:
+    return load().diffattn_strerror(int(status)).decode()
+
+
+def lambda_init(layer: int) -> float:
+    """lambda_init(l) = 0.8 - 0.6 exp(-0.3 (l - 1)), computed by the library."""
+    return float(load().diffattn_lambda_init(int(layer)))
+
+
+def _check(status: int):
+    if status != OK:
+        raise DiffAttnError(status, strerror(status))
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(B, H, N, d, dtype_code, causal, headnorm, eps, lambda_init_value, status=None):
+    return Desc(int(B), int(H), int(N), int(d), int(dtype_code), int(bool(causal)),
+                int(bool(headnorm)), float(eps), float(lambda_init_value),
+                None if status is None else status.data_ptr())
+
+
+def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_w=None,
+        eps: float = 1e-5, lambda_init: float = 0.0, out=None, status=None, stream=None,
+        raw_status: bool = False):
+    """Differential-attention head forward through `diffattn_fwd`.
+
+    q1, k1, q2, k2: [B, H, N, d]; v: [B, H, N, 2d] (all bf16 or all fp32, CUDA,
+    contiguous); lam: float32 [H]; norm_w: float32 [H, 2d] or None.  Returns
+    `out` [B, H, N, 2d] (allocated by torch when not given).  With
+    raw_status=True the status code is returned instead of raising.
+    """
+    if q1.dim() != 4:
+        raise ValueError("q1 must be [B, H, N, d]")
+    B, H, N, d = q1.shape
+    dtype = q1.dtype
+    if dtype not in _DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, shape in (("k1", k1, (B, H, N, d)), ("q2", q2, (B, H, N, d)),
+                           ("k2", k2, (B, H, N, d)), ("v", v, (B, H, N, 2 * d))):
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name} must be {shape} {dtype}")
+    tensors = [q1, k1, q2, k2, v, lam] + ([norm_w] if norm_w is not None else [])
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=dtype, device=q1.device)
+    tensors.append(out)
+    for t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if lam.dtype != torch.float32 or lam.numel() != H:
+        raise ValueError("lam must be float32 [H]")
+    if norm_w is not None and (norm_w.dtype != torch.float32 or norm_w.numel() != H * 2 * d):
+        raise ValueError("norm_w must be float32 [H, 2d]")
+    if tuple(out.shape) != (B, H, N, 2 * d) or out.dtype != dtype:
+        raise ValueError("out must be [B, H, N, 2d] of the input dtype")
+    desc = make_desc(B, H, N, d, _DTYPE_CODE[dtype], causal, headnorm, eps, lambda_init, status)
+    st = load().diffattn_fwd(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
+                             _ptr(lam), _ptr(norm_w), _ptr(out), _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return out
+
+
+def headnorm(x, *, H: int, norm_w=None, eps: float = 1e-5, lambda_init: float = 0.0,
+             out_dtype=torch.bfloat16, out=None, stream=None):
+    """Per-head RMS normalisation through `diffattn_headnorm`.
+
+    x: float32 [B, H, N, 2d] CUDA; returns [B, H, N, 2d] in out_dtype.
+    """
+    if x.dim() != 4 or x.dtype != torch.float32:
+        raise ValueError("x must be float32 [B, H, N, 2d]")
+    B, Hx, N, dv = x.shape
+    if Hx != H or dv % 2:
+        raise ValueError("x must be [B, H, N, 2d]")
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    for t in [x, out] + ([norm_w] if norm_w is not None else []):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    desc = make_desc(B, H, N, dv // 2, _DTYPE_CODE[out.dtype], False, True, eps, lambda_init)
+    _check(load().diffattn_headnorm(ctypes.byref(desc), _ptr(x), _ptr(norm_w), _ptr(out),
+                                    _stream_handle(stream)))
+    return out

@@ -1,0 +1,99 @@
+"""The C-ABI library: it loads, exports what include/diffattn.h declares, and
+its host-side validation answers without touching a GPU."""
+import ctypes
+
+import pytest
+
+import oracle
+from differential_attention_attn_gb300 import build as libbuild
+from differential_attention_attn_gb300 import ops
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return ops.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = ops.declared_symbols()
+    assert set(names) == {"diffattn_fwd", "diffattn_headnorm", "diffattn_lambda_init",
+                          "diffattn_strerror", "diffattn_version"} or len(names) >= 5
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/diffattn.h but not exported"
+
+
+def test_desc_layout_matches_header():
+    # int64 x3, int32 x4, float x2, pointer: 56 bytes on LP64.
+    assert ctypes.sizeof(ops.Desc) == 56
+    assert ops.Desc.status_dev.offset == 48
+
+
+def test_strerror_and_version(lib):
+    for code in range(5):
+        assert isinstance(ops.strerror(code), str) and ops.strerror(code)
+    assert ops.strerror(99) == "unknown status"
+    assert lib.diffattn_version() >= 100
+
+
+@pytest.mark.parametrize("layer", [1, 2, 5, 12, 24, 100])
+def test_lambda_init_matches_oracle(lib, layer):
+    assert ops.lambda_init(layer) == pytest.approx(oracle.lambda_init(layer), abs=1e-15)
+
+
+FAKE = 0x10000  # never dereferenced: validation rejects or returns before any launch
+
+
+def _call(lib, desc, ptrs=None, lam=FAKE, out=FAKE):
+    p = [FAKE] * 5 if ptrs is None else ptrs
+    return lib.diffattn_fwd(ctypes.byref(desc) if desc is not None else None,
+                            *[ctypes.c_void_p(x) if x else None for x in p],
+                            ctypes.c_void_p(lam) if lam else None, None,
+                            ctypes.c_void_p(out) if out else None, None)
+
+
+def test_null_desc_and_pointers(lib):
+    assert _call(lib, None) == ops.ERR_INVALID_ARG
+    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, True, 1e-5, 0.2)
+    assert _call(lib, d, ptrs=[FAKE, 0, FAKE, FAKE, FAKE]) == ops.ERR_INVALID_ARG
+    assert _call(lib, d, lam=0) == ops.ERR_INVALID_ARG
+    assert _call(lib, d, out=0) == ops.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,value", [("B", -1), ("H", -2), ("N", -5), ("d", 0),
+                                         ("dtype", 7), ("eps", -1.0), ("eps", float("nan")),
+                                         ("lambda_init", float("inf"))])
+def test_invalid_fields(lib, field, value):
+    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, True, 1e-5, 0.2)
+    setattr(d, field, value)
+    assert _call(lib, d) == ops.ERR_INVALID_ARG
+
+
+def test_empty_problem_is_ok_without_launch(lib):
+    for B, H, N in ((0, 4, 128), (2, 0, 128), (1, 4, 0)):
+        d = ops.make_desc(B, H, N, 64, ops.BF16, True, True, 1e-5, 0.2)
+        assert _call(lib, d, ptrs=[0] * 5, lam=0, out=0) == ops.OK
+
+
+def test_bf16_domain(lib):
+    d = ops.make_desc(1, 2, 256, 128, ops.BF16, True, True, 1e-5, 0.2)
+    assert _call(lib, d) == ops.ERR_UNSUPPORTED
+    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, True, 1e-5, 0.2)
+    assert _call(lib, d, ptrs=[FAKE + 8] + [FAKE] * 4) == ops.ERR_INVALID_ARG
+    assert _call(lib, d, out=FAKE + 2) == ops.ERR_INVALID_ARG
+
+
+def test_f32_domain(lib):
+    d = ops.make_desc(1, 1, 5000, 8, ops.F32, False, False, 1e-5, 0.0)
+    assert _call(lib, d) == ops.ERR_UNSUPPORTED
+    d = ops.make_desc(1, 1, 16, 129, ops.F32, False, False, 1e-5, 0.0)
+    assert _call(lib, d) == ops.ERR_UNSUPPORTED
+
+
+def test_headnorm_validation(lib):
+    d = ops.make_desc(1, 1, 16, 200, ops.F32, False, True, 1e-5, 0.0)
+    assert lib.diffattn_headnorm(ctypes.byref(d), ctypes.c_void_p(FAKE), None,
+                                 ctypes.c_void_p(FAKE), None) == ops.ERR_UNSUPPORTED
+    d = ops.make_desc(1, 1, 16, 8, ops.F32, False, True, 1e-5, 0.0)
+    assert lib.diffattn_headnorm(ctypes.byref(d), None, None, ctypes.c_void_p(FAKE),
+                                 None) == ops.ERR_INVALID_ARG
