@@ -41,7 +41,19 @@
 // from one thread execute in order, so S_k of tile j+1 never overwrites P_k
 // of tile j before PV_k of tile j has read it, and the commit that publishes
 // S_k of tile j also certifies that PV_k of tile j-1 is complete (which the
-// softmax needs before it rescales O_k).
+// softmax needs before it rescales O_k).  Operand descriptors are built once
+// and advanced by adding to their start-address field.
+//
+// Softmax (one thread per row, 128 key columns per tile).  Each map keeps a
+// reference maximum m (log2 units) per row and P = 2^(x - m), x = S log2(e) /
+// sqrt(d).  m is only raised when a row's maximum exceeds it by more than 2^8
+// (lazy rescaling), so in steady state a tile needs no maximum at all: the
+// exponentials are computed against the current m, and since every P is at
+// most the row's tile sum, a sum <= 2^8 certifies the tile.  Otherwise (and
+// on the first tile) the warp takes the exact path: the true maximum from S
+// (still intact in TMEM, because P is held in registers until certified), a
+// rescale of O_k and of the running sum when m moves, and the exponentials
+// again.  The causal/ragged mask is compiled only into the tiles that need it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -59,7 +71,7 @@ constexpr int BM = 128;          // query rows per tile (TMEM lanes)
 constexpr int BN = 128;          // keys per key tile
 constexpr int HD = 64;           // query/key half width d
 constexpr int DV = 2 * HD;       // value width 2d
-constexpr int STAGES = 2;        // K/V pipeline depth
+constexpr int STAGES = 3;        // K/V pipeline depth
 constexpr int NUM_THREADS = 384;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
 
@@ -90,6 +102,7 @@ struct Ctrl {
 constexpr uint32_t SMEM_BYTES = OFF_CTRL + sizeof(Ctrl) + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(OFF_STAGES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "SW128 tiles need 1 KB alignment");
+static_assert(SMEM_BYTES + 1024 < (1u << 18), "descriptor start addresses must stay below 256 KB");
 
 constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t tm_s(int k) { return 128u * k; }        // S_k / P_k
@@ -124,16 +137,83 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
-// K-major SW128 operand descriptor of a [rows x 64] bf16 tile, advanced to
-// the 16-element K slice `kk`.
-__device__ __forceinline__ uint64_t desc_kmajor(const uint8_t *tile, int kk) {
-  return smem_desc_sw128(smem_u32(tile) + kk * 32, 16, 1024);
+// One 32-column chunk of a softmax row: mask (key column c0 + i visible iff
+// c0 + i <= lim), x = s * log2(e)/sqrt(d) - m, p = 2^x, accumulate the sum
+// in four packed partial sums and pack p as bf16 pairs into pk[c0/2 ..].
+template <bool kMasked>
+__device__ __forceinline__ void softmax_chunk_exp(const uint32_t (&x)[32], int c0, float m,
+                                                  float sl2, int lim, float2 (&acc)[4],
+                                                  uint32_t (&pk)[BN / 2]) {
+  const float2 scale = make_float2(sl2, sl2), negm = make_float2(-m, -m);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float a = __uint_as_float(x[i]), b = __uint_as_float(x[i + 1]);
+    if (kMasked) {
+      a = (c0 + i <= lim) ? a : -INFINITY;
+      b = (c0 + i + 1 <= lim) ? b : -INFINITY;
+    }
+    float2 e = __ffma2_rn(make_float2(a, b), scale, negm);
+    e.x = ex2_approx(e.x);
+    e.y = ex2_approx(e.y);
+    acc[(i / 2) % 4] = __fadd2_rn(acc[(i / 2) % 4], e);
+    pk[(c0 + i) / 2] = pack_bf16x2(e.x, e.y);
+  }
 }
 
-// MN-major SW128 descriptor of the V tile ([128 keys x 128 values] stored as
-// two [128 x 64] column blocks 16 KB apart), advanced to keys [16 kk, 16 kk + 16).
-__device__ __forceinline__ uint64_t desc_v(const uint8_t *vtile, int kk) {
-  return smem_desc_sw128(smem_u32(vtile) + kk * 16 * 128, TILE_QK_BYTES, 1024);
+// Exponentials of a whole 128-column S row against reference maximum m; the
+// four 32-column TMEM loads are issued two ahead of their use.  Returns the
+// row sum of the (unrounded) exponentials.
+template <bool kMasked>
+__device__ __forceinline__ float softmax_tile_exp(uint32_t t_s, float m, float sl2, int lim,
+                                                  uint32_t (&pk)[BN / 2]) {
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+  uint32_t a[32], b[32];
+  tmem_ld_x32_nowait(t_s, a);
+  tmem_ld_x32_nowait(t_s + 32, b);
+  tmem_ld_wait_x32(a);
+  tmem_ld_wait_x32(b);
+  softmax_chunk_exp<kMasked>(a, 0, m, sl2, lim, acc, pk);
+  tmem_ld_x32_nowait(t_s + 64, a);
+  softmax_chunk_exp<kMasked>(b, 32, m, sl2, lim, acc, pk);
+  tmem_ld_x32_nowait(t_s + 96, b);
+  tmem_ld_wait_x32(a);
+  tmem_ld_wait_x32(b);
+  softmax_chunk_exp<kMasked>(a, 64, m, sl2, lim, acc, pk);
+  softmax_chunk_exp<kMasked>(b, 96, m, sl2, lim, acc, pk);
+  const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
+  return (s01.x + s01.y) + (s23.x + s23.y);
+}
+
+// Maximum of a 128-column S row over its visible columns (tree reduction).
+template <bool kMasked>
+__device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 64) {
+    uint32_t a[32], b[32];
+    tmem_ld_x32_nowait(t_s + c0, a);
+    tmem_ld_x32_nowait(t_s + c0 + 32, b);
+    tmem_ld_wait_x32(a);
+    tmem_ld_wait_x32(b);
+    float v[64];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = __uint_as_float(a[i]);
+      v[32 + i] = __uint_as_float(b[i]);
+    }
+    if (kMasked) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = (c0 + i <= lim) ? v[i] : -INFINITY;
+    }
+#pragma unroll
+    for (int w = 32; w >= 1; w /= 2) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) v[i] = fmaxf(v[i], v[i + w]);
+    }
+    m = fmaxf(m, v[0]);
+  }
+  return m;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -229,51 +309,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
-      const uint8_t *sq[2] = {smem + OFF_Q1, smem + OFF_Q2};
-      auto qk = [&](int k, const uint8_t *st) {
-        const uint8_t *kt = st + (k == 0 ? STAGE_K1 : STAGE_K2);
+      // Operand descriptors are built once.  Every operand is a base tile plus a
+      // byte offset below 256 KB, so advancing it only adds offset >> 4 to the
+      // 14-bit start-address field (no carry into the other fields).
+      const uint64_t dq[2] = {smem_desc_sw128(smem_u32(smem + OFF_Q1), 16, 1024),
+                              smem_desc_sw128(smem_u32(smem + OFF_Q2), 16, 1024)};
+      const uint64_t dk[2] = {smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K1), 16, 1024),
+                              smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K2), 16, 1024)};
+      const uint64_t dvb =
+          smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_V), TILE_QK_BYTES, 1024);
+      auto qk = [&](int k, int s) {  // S_k = Q_k K_k^T, K from stage s; K slices of 32 bytes
+        const uint64_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + tm_s(k), desc_kmajor(sq[k], kk), desc_kmajor(kt, kk), IDESC_QK,
-                       kk > 0);
+          umma_bf16_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK, kk > 0);
       };
-      auto pv = [&](int k, const uint8_t *st, bool accumulate) {
+      auto pv = [&](int k, int s, bool accumulate) {  // O_k += P_k V; 16 keys = 2048 bytes
+        const uint64_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_bf16_ts(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, desc_v(st + STAGE_V, kk),
-                       IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, b + 128 * kk, IDESC_PV,
+                       (accumulate || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag, WAIT_TIMEOUT_NS);
       tc_fence_after_sync();
       for (int j = 0; ok && j < n_kv; ++j) {
         const int s = j % STAGES;
         const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1;
-        const uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
         if (!(ok = mbar_wait(&ctrl->k_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
         tc_fence_after_sync();
-        qk(0, st);
+        qk(0, s);
         umma_commit(&ctrl->s_full[0]);
         if (j > 0) {
           if (!(ok = mbar_wait(&ctrl->p_ready[1], (j - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
             break;
           tc_fence_after_sync();
           const int sp = (j - 1) % STAGES;
-          pv(1, smem + OFF_STAGES + sp * STAGE_BYTES, j - 1 > 0);
+          pv(1, sp, j - 1 > 0);
           umma_commit(&ctrl->kv_empty[sp]);
         }
-        qk(1, st);
+        qk(1, s);
         umma_commit(&ctrl->s_full[1]);
         if (!(ok = mbar_wait(&ctrl->v_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
         if (!(ok = mbar_wait(&ctrl->p_ready[0], j & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
         tc_fence_after_sync();
-        pv(0, st, j > 0);
+        pv(0, s, j > 0);
       }
       if (ok && n_kv > 0) {
         const int jl = n_kv - 1;
         if (mbar_wait(&ctrl->p_ready[1], jl & 1, abort_flag, WAIT_TIMEOUT_NS)) {
           tc_fence_after_sync();
           const int sl = jl % STAGES;
-          pv(1, smem + OFF_STAGES + sl * STAGE_BYTES, jl > 0);
+          pv(1, sl, jl > 0);
           umma_commit(&ctrl->kv_empty[sl]);
           umma_commit(&ctrl->o_done);
         }
@@ -284,7 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax
-    const int k = (warp - 4) / 4;        // which map
+    const int k = (warp - 4) / 4;          // which map
     const int r = (warp % 4) * 32 + lane;  // query row within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + tm_s(k);
@@ -298,59 +385,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t sr[2][64];
-      tmem_ld_x64(t_s, sr[0]);
-      tmem_ld_x64(t_s + 64, sr[1]);
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c / 64][c % 64]);
+      // Key column c of this tile is visible to this row iff c <= lim.
       const int kv0 = j * BN;
-      if (p.causal && kv0 + BN > q0 + r + 1) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (kv0 + c > q0 + r) s[c] = -INFINITY;
+      const int lim = p.causal ? (q0 + r - kv0) : (p.N - 1 - kv0);
+      const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
+      uint32_t pk[BN / 2];
+      float tile_sum = 0.f;
+      // Steady state: exponentials against the current reference maximum; the
+      // row sum bounds every entry, so sum <= 2^8 certifies that no P exceeds
+      // 2^8 and the maximum is never computed.  Otherwise (and on the first
+      // tile) the exact path below recomputes the tile from S, which is still
+      // intact in TMEM because P is only stored once certified.
+      bool exact = (j == 0);
+      if (!exact) {
+        tile_sum = masked ? softmax_tile_exp<true>(t_s, m_run, sl2, lim, pk)
+                          : softmax_tile_exp<false>(t_s, m_run, sl2, lim, pk);
+        exact = __any_sync(0xffffffffu, !(tile_sum <= 256.f));
       }
-      if (!p.causal && kv0 + BN > p.N) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (kv0 + c >= p.N) s[c] = -INFINITY;
-      }
-      float mt = s[0];
-#pragma unroll
-      for (int c = 1; c < BN; ++c) mt = fmaxf(mt, s[c]);
-      const float m_new = fmaxf(m_run, mt * sl2);
-      float alpha = 1.f;
-      if (j == 0) {
-        m_run = m_new;
-      } else if (m_new > m_run + RESCALE_THRESHOLD) {
-        alpha = ex2_approx(m_run - m_new);
-        m_run = m_new;
-      }
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        // O_k of this row is complete up to tile j-1 (certified by s_full).
-#pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(t_o + c0, o);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st_x32(t_o + c0, o);
+      if (exact) {
+        const float mt = masked ? softmax_tile_max<true>(t_s, lim) : softmax_tile_max<false>(t_s, lim);
+        const float m_new = fmaxf(m_run, mt * sl2);
+        float alpha = 1.f;
+        if (j == 0) {
+          m_run = m_new;
+        } else if (m_new > m_run + RESCALE_THRESHOLD) {
+          alpha = ex2_approx(m_run - m_new);
+          m_run = m_new;
         }
-      }
-      l_run *= alpha;
-      const float msub = m_run;
-      float rs = 0.f;
-      uint32_t pk[2][32];
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // O_k of this row is complete up to tile j-1 (certified by s_full).
+#pragma unroll 1
+          for (int c0 = 0; c0 < DV; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(t_o + c0, o);
 #pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float a = ex2_approx(fmaf(s[2 * c], sl2, -msub));
-        const float b = ex2_approx(fmaf(s[2 * c + 1], sl2, -msub));
-        rs += a + b;
-        pk[c / 32][c % 32] = pack_bf16x2(a, b);
+            for (int c = 0; c < 32; c += 2) {
+              const float2 v = __fmul2_rn(
+                  make_float2(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
+                  make_float2(alpha, alpha));
+              o[c] = __float_as_uint(v.x);
+              o[c + 1] = __float_as_uint(v.y);
+            }
+            tmem_st_x32(t_o + c0, o);
+          }
+        }
+        l_run *= alpha;
+        tile_sum = masked ? softmax_tile_exp<true>(t_s, m_run, sl2, lim, pk)
+                          : softmax_tile_exp<false>(t_s, m_run, sl2, lim, pk);
       }
-      l_run += rs;
-      tmem_st_x32(t_s, pk[0]);
-      tmem_st_x32(t_s + 32, pk[1]);
+      l_run += tile_sum;
+      // P_k as packed bf16 pairs over the first 64 columns of S_k.
+#pragma unroll
+      for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+        uint32_t part[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) part[c] = pk[c0 + c];
+        tmem_st_x16(t_s + c0, part);
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&ctrl->p_ready[k]);
@@ -368,15 +459,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float inv1 = xch[r];
       const float c2 = p.lambda[h] * xch[BM + r];
       const int col0 = k * (DV / 2);
-      uint32_t o1r[64], o2r[64];
-      tmem_ld_x64(tmem + lane_addr + tm_o(0) + col0, o1r);
-      tmem_ld_x64(tmem + lane_addr + tm_o(1) + col0, o2r);
       float o[64];
       float ss = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        o[c] = __uint_as_float(o1r[c]) * inv1 - __uint_as_float(o2r[c]) * c2;
-        ss = fmaf(o[c], o[c], ss);
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        uint32_t o1r[16], o2r[16];
+        tmem_ld_x16(tmem + lane_addr + tm_o(0) + col0 + c0, o1r);
+        tmem_ld_x16(tmem + lane_addr + tm_o(1) + col0 + c0, o2r);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          o[c0 + c] = __uint_as_float(o1r[c]) * inv1 - __uint_as_float(o2r[c]) * c2;
+          ss = fmaf(o[c0 + c], o[c0 + c], ss);
+        }
       }
       if (p.headnorm) {
         xch[2 * BM + k * BM + r] = ss;
