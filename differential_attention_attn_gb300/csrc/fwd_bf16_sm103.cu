@@ -304,6 +304,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -369,6 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       umma_commit(&ctrl->drain);
       drain_wait(&ctrl->drain, 0);
     }
+    __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax
     const int k = (warp - 4) / 4;          // which map
