@@ -159,3 +159,13 @@ def test_bf16_rejects_misaligned():
     st = ops.fwd(q1, k, k, k, w.v.cuda(), torch.ones(1, device="cuda"), causal=True,
                  raw_status=True)
     assert st == ops.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_bf16_many_items_per_cta(causal):
+    """More (head, query-tile) work items than SMs (several waves of CTAs, causal and
+    not, both query-tile extents); every output row is compared."""
+    w = W.custom(77, B=8, H=12, N=384 if causal else 320, d=64, causal=causal, headnorm=True,
+                 random_w=True, layer=9)
+    gpu = harness.run_gpu(w).double().cpu().numpy()
+    _cmp_bf16(gpu, harness.run_oracle(w), f"many items causal={causal}")
