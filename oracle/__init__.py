@@ -57,6 +57,9 @@ def _declare(lib):
     lib.oracle_fwd_rows.restype = i
     lib.oracle_fwd_rows.argtypes = [i, i, i64, i, p, p, p, p, p, p, i, i, p, d, d,
                                     i64, p, p, p, i]
+    lib.oracle_fwd_kv_rows.restype = i
+    lib.oracle_fwd_kv_rows.argtypes = [i, i, i64, i64, i, p, p, p, p, p, p, i, i, p, d, d,
+                                       i64, p, p, p, i]
     lib.oracle_diff_map.restype = i
     lib.oracle_diff_map.argtypes = [i64, i, p, p, p, p, d, i, p]
     lib.oracle_headnorm.restype = i
@@ -149,6 +152,48 @@ def fwd_rows(q1, k1, q2, k2, v, lam, bh_idx, row_idx, *, causal: bool, headnorm:
                                          _ptr(out), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_fwd_rows failed with code {rc}")
+    return out
+
+
+def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool, bh_idx=None,
+           row_idx=None, w=None, eps: float = 1e-5, lambda_init_value: float = 0.0,
+           nthreads: int = 0, lib=None) -> np.ndarray:
+    """Key/value-cache form: Nq queries against Nkv keys of the same head.
+
+    q1, q2: [B, H, Nq, d]; k1, k2: [B, H, Nkv, d]; v: [B, H, Nkv, 2d].  Query i is
+    at sequence position Nkv - Nq + i (causal: sees keys j <= Nkv - Nq + i).
+    Returns [B, H, Nq, 2d], or [R, 2d] for the selected (b*H + h, query row) pairs
+    when bh_idx / row_idx are given.
+    """
+    q1, k1, q2, k2, v = map(_f64, (q1, k1, q2, k2, v))
+    if q1.ndim != 4 or k1.ndim != 4:
+        raise ValueError("q and k must be [B, H, N, d]")
+    B, H, Nq, d = q1.shape
+    Nkv = k1.shape[2]
+    if q2.shape != q1.shape or k1.shape != (B, H, Nkv, d) or k2.shape != k1.shape:
+        raise ValueError("q1, q2 must be [B, H, Nq, d] and k1, k2 [B, H, Nkv, d]")
+    if v.shape != (B, H, Nkv, 2 * d):
+        raise ValueError("v must be [B, H, Nkv, 2d]")
+    lam = _f64(lam).reshape(H)
+    wv = None if w is None else _f64(w).reshape(H, 2 * d)
+    if bh_idx is None:
+        bh = ri = None
+        nrows = -1
+        out = np.zeros((B, H, Nq, 2 * d), dtype=np.float64)
+    else:
+        bh = np.ascontiguousarray(np.asarray(bh_idx, dtype=np.int64).reshape(-1))
+        ri = np.ascontiguousarray(np.asarray(row_idx, dtype=np.int64).reshape(-1))
+        if bh.shape != ri.shape:
+            raise ValueError("bh_idx and row_idx must have the same length")
+        nrows = bh.size
+        out = np.zeros((nrows, 2 * d), dtype=np.float64)
+    rc = (lib or load()).oracle_fwd_kv_rows(B, H, Nq, Nkv, d, _ptr(q1), _ptr(k1), _ptr(q2),
+                                            _ptr(k2), _ptr(v), _ptr(lam), int(bool(causal)),
+                                            int(bool(headnorm)), _ptr(wv), float(eps),
+                                            float(lambda_init_value), nrows, _ptr(bh),
+                                            _ptr(ri), _ptr(out), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_fwd_kv_rows failed with code {rc}")
     return out
 
 

@@ -24,7 +24,9 @@
  *   - d in the 1/sqrt(d) scale is the width of one query/key half, as in the
  *     page's worked example (n = 6, d = 8, v of width 2d).
  *   - causal = 1 means key j is visible to query i iff j <= i (square,
- *     top-left aligned); the same mask is applied to both maps.
+ *     top-left aligned); the same mask is applied to both maps.  With fewer
+ *     queries than keys (a key/value cache), the queries are the last
+ *     positions of the sequence, so the mask is aligned bottom-right.
  *   - the per-head normalisation is the RMS form over the 2d output channels
  *     of one (batch, head, token): y = o / sqrt(mean(o^2) + eps) * w[h, c],
  *     then times (1 - lambda_init).  No mean subtraction, no bias.
@@ -37,7 +39,8 @@
  * nothing in any row's arithmetic.
  *
  * Tensor layout: q1, k1, q2, k2 are [B, H, N, d] and v, out are [B, H, N, 2d],
- * all contiguous row-major float64.  lambda is [H]; w is [H, 2d] or NULL
+ * all contiguous row-major float64 (oracle_fwd_kv_rows: Nq query rows, Nkv
+ * key and value rows).  lambda is [H]; w is [H, 2d] or NULL
  * (meaning all ones).
  */
 #include <math.h>
@@ -93,29 +96,31 @@ static void softmax_row(int64_t i, int64_t N, int d, const double *q_row,
         p[j] /= sum;
 }
 
-/* Row i of the differential map of one head: w[j] = map1[i][j] - lambda *
- * map2[i][j].  Scratch p1, p2 hold N doubles each. */
-static void diff_row(int64_t i, int64_t N, int d, const double *q1,
-                     const double *k1, const double *q2, const double *k2,
+/* Row of the differential map for the query at position i (query vectors
+ * q1_row, q2_row) against N keys: w[j] = map1[i][j] - lambda * map2[i][j].
+ * Scratch p1, p2 hold N doubles each. */
+static void diff_row(int64_t i, int64_t N, int d, const double *q1_row,
+                     const double *k1, const double *q2_row, const double *k2,
                      double lam, int causal, double *p1, double *p2, double *w)
 {
-    softmax_row(i, N, d, q1 + i * d, k1, causal, p1);
-    softmax_row(i, N, d, q2 + i * d, k2, causal, p2);
+    softmax_row(i, N, d, q1_row, k1, causal, p1);
+    softmax_row(i, N, d, q2_row, k2, causal, p2);
     for (int64_t j = 0; j < N; ++j)
         w[j] = p1[j] - lam * p2[j];
 }
 
-/* out_row = (map1 - lambda map2)[i, :] V, then optionally the per-head RMS
+/* out_row = (map1 - lambda map2)[i, :] V for the query at position i with
+ * vectors q1_row, q2_row against N keys, then optionally the per-head RMS
  * normalisation and the (1 - lambda_init) scale. */
-static void out_row(int64_t i, int64_t N, int d, const double *q1,
-                    const double *k1, const double *q2, const double *k2,
+static void out_row(int64_t i, int64_t N, int d, const double *q1_row,
+                    const double *k1, const double *q2_row, const double *k2,
                     const double *v, double lam, int causal, int headnorm,
                     const double *w_head, double eps, double lambda_init,
                     double *scratch, double *o)
 {
     double *p1 = scratch, *p2 = scratch + N, *wrow = scratch + 2 * N;
     const int dv = 2 * d;
-    diff_row(i, N, d, q1, k1, q2, k2, lam, causal, p1, p2, wrow);
+    diff_row(i, N, d, q1_row, k1, q2_row, k2, lam, causal, p1, p2, wrow);
     for (int c = 0; c < dv; ++c)
         o[c] = 0.0;
     for (int64_t j = 0; j < N; ++j)
@@ -183,7 +188,7 @@ int oracle_fwd(int B, int H, int64_t N, int d, const double *q1,
             const int64_t bh = r / N, i = r % N;
             const int h = (int)(bh % H);
             const int64_t qk = bh * N * d, vo = bh * N * dv;
-            out_row(i, N, d, q1 + qk, k1 + qk, q2 + qk, k2 + qk, v + vo,
+            out_row(i, N, d, q1 + qk + i * d, k1 + qk, q2 + qk + i * d, k2 + qk, v + vo,
                     lam[h], causal, headnorm, w ? w + (int64_t)h * dv : NULL,
                     eps, lambda_init, scratch, out + vo + i * dv);
         }
@@ -225,9 +230,61 @@ int oracle_fwd_rows(int B, int H, int64_t N, int d, const double *q1,
             const int64_t bh = bh_idx[r], i = row_idx[r];
             const int h = (int)(bh % H);
             const int64_t qk = bh * N * d, vo = bh * N * dv;
-            out_row(i, N, d, q1 + qk, k1 + qk, q2 + qk, k2 + qk, v + vo,
+            out_row(i, N, d, q1 + qk + i * d, k1 + qk, q2 + qk + i * d, k2 + qk, v + vo,
                     lam[h], causal, headnorm, w ? w + (int64_t)h * dv : NULL,
                     eps, lambda_init, scratch, out_rows + r * dv);
+        }
+        free(scratch);
+    }
+    return err;
+}
+
+/* KV-cache form: Nq queries attend to Nkv keys of the same head.  q1, q2 are
+ * [B, H, Nq, d], k1, k2 are [B, H, Nkv, d], v is [B, H, Nkv, 2d] and out is
+ * [B, H, Nq, 2d].  The queries are the last Nq positions of the sequence:
+ * query i sits at position Nkv - Nq + i, so under the causal mask it sees keys
+ * j <= Nkv - Nq + i (with Nq = Nkv this is oracle_fwd).  Rows are selected as
+ * in oracle_fwd_rows (bh_idx[r], row_idx[r] < Nq); nrows < 0 means every row
+ * in order, written to out_rows as a full [B, H, Nq, 2d] tensor. */
+int oracle_fwd_kv_rows(int B, int H, int64_t Nq, int64_t Nkv, int d,
+                       const double *q1, const double *k1, const double *q2,
+                       const double *k2, const double *v, const double *lam,
+                       int causal, int headnorm, const double *w, double eps,
+                       double lambda_init, int64_t nrows, const int64_t *bh_idx,
+                       const int64_t *row_idx, double *out_rows, int nthreads)
+{
+    if (B < 0 || H < 0 || Nq < 0 || Nkv < 0 || d <= 0)
+        return -1;
+    if (causal && Nq > Nkv)
+        return -1;
+    const int64_t BH = (int64_t)B * H;
+    const int all = nrows < 0;
+    const int64_t n = all ? BH * Nq : nrows;
+    for (int64_t r = 0; !all && r < n; ++r)
+        if (bh_idx[r] < 0 || bh_idx[r] >= BH || row_idx[r] < 0 || row_idx[r] >= Nq)
+            return -1;
+    const int dv = 2 * d;
+    int err = 0;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double *scratch = (double *)malloc(sizeof(double) * (size_t)(3 * Nkv + 1));
+        if (!scratch) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n; ++r) {
+            if (!scratch)
+                continue;
+            const int64_t bh = all ? r / Nq : bh_idx[r];
+            const int64_t i = all ? r % Nq : row_idx[r];
+            const int h = (int)(bh % H);
+            const int64_t pos = Nkv - Nq + i;
+            const int64_t qo = bh * Nq * d, ko = bh * Nkv * d, vo = bh * Nkv * dv;
+            out_row(pos, Nkv, d, q1 + qo + i * d, k1 + ko, q2 + qo + i * d, k2 + ko, v + vo,
+                    lam[h], causal, headnorm, w ? w + (int64_t)h * dv : NULL, eps,
+                    lambda_init, scratch, out_rows + r * dv);
         }
         free(scratch);
     }
@@ -247,8 +304,8 @@ int oracle_diff_map(int64_t N, int d, const double *q1, const double *k1,
     if (!scratch)
         return -2;
     for (int64_t i = 0; i < N; ++i)
-        diff_row(i, N, d, q1, k1, q2, k2, lam, causal, scratch, scratch + N,
-                 wmap + i * N);
+        diff_row(i, N, d, q1 + i * d, k1, q2 + i * d, k2, lam, causal, scratch,
+                 scratch + N, wmap + i * N);
     free(scratch);
     return 0;
 }

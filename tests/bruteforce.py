@@ -23,13 +23,20 @@ def _softmax_row(q_row, keys, visible_js, d):
 
 
 def head_forward(q1, k1, q2, k2, v, lam, causal, headnorm, w_head, eps, lambda_init):
-    """One head: lists of rows in, list of output rows out."""
+    """One head: lists of rows in, list of output rows out.
+
+    There may be fewer query rows than key rows (a key/value cache): the queries
+    are then the last positions of the sequence, query i at position
+    len(k1) - len(q1) + i.
+    """
     n = len(q1)
+    n_keys = len(k1)
     d = len(q1[0])
     dv = len(v[0])
     out = []
     for i in range(n):
-        js = [j for j in range(n) if (j <= i or not causal)]
+        pos = n_keys - n + i
+        js = [j for j in range(n_keys) if (j <= pos or not causal)]
         p1 = _softmax_row(q1[i], k1, js, d)
         p2 = _softmax_row(q2[i], k2, js, d)
         o = [0.0] * dv

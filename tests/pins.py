@@ -250,6 +250,77 @@ def pin_rows_match_full(lib):
     return err == 0.0, f"max err {err:.3e}"
 
 
+def _rand_kv(seed, B, H, Nq, Nkv, d):
+    rng = np.random.default_rng(seed)
+    q1, q2 = (rng.standard_normal((B, H, Nq, d)) for _ in range(2))
+    k1, k2 = (rng.standard_normal((B, H, Nkv, d)) for _ in range(2))
+    v = rng.standard_normal((B, H, Nkv, 2 * d))
+    return rng, q1, k1, q2, k2, v
+
+
+def pin_kv_bruteforce(lib):
+    """Key/value-cache form (fewer queries than keys, queries at the last positions)
+    agrees with pure-Python loops to 1e-12, full and selected rows."""
+    worst = 0.0
+    for seed, (B, H, Nq, Nkv, d), causal in [(41, (1, 2, 3, 7, 4), True),
+                                             (42, (2, 1, 5, 9, 3), False),
+                                             (43, (1, 1, 1, 6, 2), True),
+                                             (44, (1, 2, 4, 4, 3), True),
+                                             (45, (2, 2, 2, 11, 4), True)]:
+        rng, q1, k1, q2, k2, v = _rand_kv(seed, B, H, Nq, Nkv, d)
+        lam = rng.uniform(-0.2, 1.2, size=H)
+        w = rng.uniform(0.5, 1.5, size=(H, 2 * d))
+        for headnorm in (False, True):
+            kw = dict(causal=causal, headnorm=headnorm, w=w, eps=1e-3, lambda_init_value=0.45,
+                      lib=lib)
+            o = oracle.fwd_kv(q1, k1, q2, k2, v, lam, **kw)
+            bh = rng.integers(0, B * H, size=7)
+            ri = rng.integers(0, Nq, size=7)
+            rows = oracle.fwd_kv(q1, k1, q2, k2, v, lam, bh_idx=bh, row_idx=ri, **kw)
+            for b in range(B):
+                for h in range(H):
+                    ref = np.array(bruteforce.head_forward(
+                        q1[b, h].tolist(), k1[b, h].tolist(), q2[b, h].tolist(),
+                        k2[b, h].tolist(), v[b, h].tolist(), float(lam[h]), causal, headnorm,
+                        w[h].tolist(), 1e-3, 0.45))
+                    worst = max(worst, float(np.max(np.abs(o[b, h] - ref))))
+                    sel = bh == b * H + h
+                    if sel.any():
+                        worst = max(worst, float(np.max(np.abs(rows[sel] - ref[ri[sel]]))))
+    return worst < 1e-12, f"max err {worst:.3e}"
+
+
+def pin_kv_last_rows(lib):
+    """Attending with the last Nq queries against the whole key/value sequence gives
+    exactly the last Nq rows of the full (square) forward."""
+    worst = 0.0
+    for seed, causal in [(46, True), (47, False)]:
+        rng, q1, k1, q2, k2, v = _rand(seed, 2, 2, 13, 4)
+        lam = rng.uniform(0.1, 0.9, size=2)
+        kw = dict(causal=causal, headnorm=True, eps=1e-5, lambda_init_value=0.3, lib=lib)
+        full = oracle.fwd(q1, k1, q2, k2, v, lam, **kw)
+        for nq in (1, 5, 13):
+            o = oracle.fwd_kv(q1[:, :, -nq:], k1, q2[:, :, -nq:], k2, v, lam, **kw)
+            worst = max(worst, float(np.max(np.abs(o - full[:, :, -nq:]))))
+    return worst == 0.0, f"max err {worst:.3e}"
+
+
+def pin_kv_zero_queries(lib):
+    """Zero queries give uniform maps, so causal query i of Nq against Nkv keys is
+    (1 - lambda) times the mean of v_0 .. v_{Nkv - Nq + i}."""
+    rng = np.random.default_rng(48)
+    Nq, Nkv, d = 4, 10, 3
+    q = np.zeros((1, 2, Nq, d))
+    k1, k2 = rng.standard_normal((2, 1, 2, Nkv, d))
+    v = rng.standard_normal((1, 2, Nkv, 2 * d))
+    lam = np.array([0.25, -0.5])
+    o = oracle.fwd_kv(q, k1, q, k2, v, lam, causal=True, headnorm=False, lib=lib)
+    ref = np.cumsum(v, axis=2)[:, :, Nkv - Nq:] / np.arange(Nkv - Nq + 1, Nkv + 1)[:, None]
+    ref = (1.0 - lam)[None, :, None, None] * ref
+    err = float(np.max(np.abs(o - ref)))
+    return err < 1e-13, f"max err {err:.3e}"
+
+
 PINS = {name[4:]: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
 
 

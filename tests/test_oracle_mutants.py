@@ -24,8 +24,8 @@ MUTANTS = [
     ("reversed_mask", "return causal ? (j <= i) : 1;", "return causal ? (j >= i) : 1;"),
     ("causal_ignored", "return causal ? (j <= i) : 1;", "return 1;"),
     ("transposed_k", "s += q_row[c] * k[j * d + c];", "s += q_row[c] * k[c * N + j];"),
-    ("map2_uses_q1", "softmax_row(i, N, d, q2 + i * d, k2, causal, p2);",
-     "softmax_row(i, N, d, q1 + i * d, k2, causal, p2);"),
+    ("map2_uses_q1", "softmax_row(i, N, d, q2_row, k2, causal, p2);",
+     "softmax_row(i, N, d, q1_row, k2, causal, p2);"),
     ("unnormalised_map", "p[j] /= sum;", "p[j] /= 1.0;"),
     ("v_columns_reversed", "o[c] += wrow[j] * v[j * dv + c];",
      "o[c] += wrow[j] * v[j * dv + (dv - 1 - c)];"),
@@ -44,6 +44,13 @@ MUTANTS = [
      "                    eps, lambda_init, scratch, out + vo + i * dv);",
      "lam[h], causal, headnorm, w ? w : NULL,\n"
      "                    eps, lambda_init, scratch, out + vo + i * dv);"),
+    # key/value-cache form
+    ("kv_top_left_mask", "const int64_t pos = Nkv - Nq + i;", "const int64_t pos = i;"),
+    ("kv_position_off_by_one", "const int64_t pos = Nkv - Nq + i;",
+     "const int64_t pos = Nkv - Nq + i - 1;"),
+    ("kv_key_stride_of_queries", "ko = bh * Nkv * d,", "ko = bh * Nq * d,"),
+    ("kv_value_stride_of_queries", "vo = bh * Nkv * dv;", "vo = bh * Nq * dv;"),
+    ("kv_query_stride_of_keys", "qo = bh * Nq * d,", "qo = bh * Nkv * d,"),
 ]
 
 
