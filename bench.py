@@ -5,6 +5,13 @@ the head-norm epilogue) over one batch of the needle-style causal workload
 B=2, H=16, N=4096, d=64 (value width 128).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload needle_4k|small_causal|mid_causal|long_16k|decode_16k]
+
+--workload picks another measured shape (default needle_4k, the headline).
+decode_16k is one decoding step of 32 heads (B=1, H=32, one query each)
+against a 16384-key cache through diffattn_fwd_kv with the library's split
+count; it is bound by HBM, so its metric is algorithmic GB/s (the cache read
+once, queries in, outputs out).
 
 Metric: algorithmic TFLOP/s with 8*d flops per visible (query, key) pair
 (2*d for each of the two Q K^T maps, 4*d for one combined map times V of
@@ -212,6 +219,21 @@ def run_reference(args):
     from differential_attention_attn_gb300 import workloads as W
     from tests import harness
 
+    if args.workload in DECODE:
+        w = decode_workload(args.workload)
+        base = decode_cpu_baseline(w, 1.0)
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": base["value"],
+                "unit": "GB/s", "n_gpus": world, "steps": 1, "warmup": 0,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "B": w.B, "H": w.H, "Nq": w.N,
+                           "Nkv": w.n_kv, "d": w.d},
+                "cpu_baseline": base,
+                "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    WORKLOAD = args.workload
     w = W.make(WORKLOAD)
     oargs, kw = harness.oracle_args(w)
     rng = np.random.default_rng(11)
@@ -252,9 +274,172 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+DECODE = {"decode_16k": dict(B=1, H=32, Nq=1, Nkv=16384, layer=24)}
+DECODE_METRIC = "diff-attn decode GB/s (1 query per head vs a 16K-key cache, bf16), 1 GPU"
+
+
+def decode_bytes(B, H, Nq, Nkv, d=64, elem=2) -> float:
+    # k1, k2 (2 * d) + v (2d) per cached key; q1, q2 (2 * d) in and out (2d) per query
+    return float(B * H * (Nkv * 4 * d + Nq * 4 * d) * elem)
+
+
+def decode_workload(name, seed_offset=0):
+    from differential_attention_attn_gb300 import workloads as W
+    c = DECODE[name]
+    return W.kv_cache(2000 + seed_offset, B=c["B"], H=c["H"], Nq=c["Nq"], Nkv=c["Nkv"],
+                      causal=True, layer=c["layer"], random_w=False)
+
+
+def run_decode(args):
+    """One decoding step per timed step, through diffattn_fwd_kv (split-KV + combine)."""
+    from differential_attention_attn_gb300 import ops
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ops.load()
+    w = decode_workload(args.workload, seed_offset=rank)
+    B, H, Nq, Nkv, d = w.B, w.H, w.N, w.n_kv, w.d
+    li = float(np.float32(ops.lambda_init(w.layer)))
+    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device=dev)
+    host = [t.contiguous() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    set_bytes = sum(t.numel() * t.element_size() for t in host)
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    sets = [[t.to(dev) for t in host] for _ in range(n_sets)]
+    out = torch.empty((B, H, Nq, 2 * d), dtype=torch.bfloat16, device=dev)
+    splits, ws_bytes = ops.fwd_kv_plan(B, H, Nq, Nkv, causal=True, splits=0)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    kw = dict(causal=True, headnorm=True, eps=float(np.float32(w.eps)), lambda_init=li,
+              splits=splits, workspace=ws, stream=stream)
+
+    def step(ins, o):
+        ops.fwd_kv(*ins, lam, out=o, **kw)
+
+    for i in range(args.warmup):
+        step(sets[i % n_sets], out)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(sets[i % n_sets], out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+
+    # e2e: the step's queries come from pinned host memory and the outputs go back;
+    # the key/value cache is state that stays resident on the device.
+    q_host = [w.q1.contiguous().pin_memory(), w.q2.contiguous().pin_memory()]
+    cache = sets[0]
+    q_dev = [torch.empty_like(t, device=dev) for t in q_host]
+    host_out = torch.empty((B, H, Nq, 2 * d), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        for dst, src in zip(q_dev, q_host):
+            dst.copy_(src, non_blocking=True)
+        step([q_dev[0], cache[1], q_dev[1], cache[3], cache[4]], out)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    times = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_total, e2e_ms = float(times[0]), float(times[1])
+    nbytes = decode_bytes(B, H, Nq, Nkv, d)
+    value = world * nbytes * args.steps / (ms_total * 1e-3) / 1e9
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = read_peaks()
+    peak = float(peaks["hbm_gbs"])
+    launch_ms = ms_total / args.steps
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": launch_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "Nq": Nq, "Nkv": Nkv, "d": d,
+                   "dv": 2 * d, "causal": True, "headnorm": True, "splits": splits,
+                   "workspace_bytes": ws_bytes,
+                   "bytes_convention": "k1, k2, v of the cache once + q1, q2 in + out",
+                   "l2": f"rotating {n_sets} caches of {set_bytes / 1e6:.1f} MB "
+                         f"(> {L2_BYTES / 1e6:.0f} MB L2)",
+                   "parallelism": f"weak x{world} (one full workload per rank)"},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (launch_ms * 1e-3) / 1e9,
+                     "peak": peak, "unit": "GB/s",
+                     "frac": nbytes / (launch_ms * 1e-3) / 1e9 / peak,
+                     "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "kernel": "diffattn_fwd_bf16_sm103_kernel (split-KV partial) + "
+                               "diffattn_splitkv_combine_kernel, timed together per step",
+                     "alg_bytes_per_launch": nbytes, "traffic": None},
+        "e2e": {"value": world * nbytes * args.steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in q_host)),
+                "d2h_bytes_per_step": int(host_out.numel() * host_out.element_size())},
+        "gpu_launches": args.steps * (2 if splits > 1 else 1),
+        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = decode_cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def decode_cpu_baseline(w, seconds: float):
+    """The float64 oracle on whole decoding steps, repeated for about `seconds`."""
+    import oracle
+    from tests import harness
+
+    args, kw = harness.oracle_args(w)
+    cores = oracle.max_threads(0)
+    nbytes = decode_bytes(w.B, w.H, w.N, w.n_kv, w.d)
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds or n == 0:
+        oracle.fwd_kv(*args, **kw)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} whole decoding steps of {w.name}, float64 oracle; {dt:.1f} s"}
+
+
 def run_ours(args):
     from differential_attention_attn_gb300 import ops
     from differential_attention_attn_gb300 import workloads as W
+
+    if args.workload in DECODE:
+        return run_decode(args)
+    WORKLOAD = args.workload
 
     world, rank, local = dist_env()
     if world > 1:
@@ -397,6 +582,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["needle_4k", "small_causal", "mid_causal", "long_16k", *DECODE])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":

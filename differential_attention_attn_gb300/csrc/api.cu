@@ -43,6 +43,51 @@ diffattn_status check_sm103() {
   return cached[dev] == 1 ? DIFFATTN_OK : DIFFATTN_ERR_UNSUPPORTED;
 }
 
+int sm_count() {
+  static int cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Validation shared by diffattn_fwd_kv_plan and diffattn_fwd_kv; on success
+// *splits_out is the split count that will run and *bytes the workspace it needs.
+diffattn_status plan_kv(const diffattn_desc *desc, int64_t n_kv, int splits, int *splits_out,
+                        size_t *bytes) {
+  diffattn_status st = check_desc(desc);
+  if (st != DIFFATTN_OK) return st;
+  if (n_kv < 0 || splits < 0 || splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->causal && n_kv < desc->N) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+  const int64_t BH = desc->B * desc->H;
+  if (BH * desc->N == 0) {
+    *splits_out = 1;
+    *bytes = 0;
+    return DIFFATTN_OK;
+  }
+  if (n_kv == 0) return DIFFATTN_ERR_INVALID_ARG;  // a softmax over no keys
+  const int64_t n_qtiles = (desc->N + kTileRows - 1) / kTileRows;
+  const int64_t n_ktiles = (n_kv + kTileKeys - 1) / kTileKeys;
+  if (splits == 0) {
+    const int sms = sm_count();
+    if (sms <= 0) return DIFFATTN_ERR_CUDA;
+    splits = auto_splits(BH, desc->N, n_kv, desc->causal != 0, sms);
+  }
+  if (splits > n_ktiles) splits = static_cast<int>(n_ktiles);
+  const double elems = static_cast<double>(BH) * static_cast<double>(n_qtiles) * splits *
+                       static_cast<double>(kPartFloats);
+  if (elems * 4.0 > 9.0e18) return DIFFATTN_ERR_UNSUPPORTED;
+  *splits_out = splits;
+  *bytes = splits > 1 ? static_cast<size_t>(BH * n_qtiles * splits * kPartFloats) * sizeof(float)
+                      : 0;
+  return DIFFATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -61,13 +106,49 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
         !aligned16(out))
       return DIFFATTN_ERR_INVALID_ARG;
     if ((st = check_sm103()) != DIFFATTN_OK) return st;
-    return launch_fwd_bf16_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w, out, s);
+    return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out, s, 1,
+                                 nullptr);
   }
   if (desc->d > kF32MaxD || desc->N > kF32MaxN) return DIFFATTN_ERR_UNSUPPORTED;
   return launch_fwd_f32(*desc, static_cast<const float *>(q1), static_cast<const float *>(k1),
                         static_cast<const float *>(q2), static_cast<const float *>(k2),
                         static_cast<const float *>(v), lambda, norm_w, static_cast<float *>(out),
                         s);
+}
+
+diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, int splits,
+                                     int *splits_out, size_t *workspace_bytes) {
+  if (splits_out == nullptr || workspace_bytes == nullptr) return DIFFATTN_ERR_INVALID_ARG;
+  int sp = 1;
+  size_t bytes = 0;
+  const diffattn_status st = plan_kv(desc, n_kv, splits, &sp, &bytes);
+  if (st != DIFFATTN_OK) return st;
+  *splits_out = sp;
+  *workspace_bytes = bytes;
+  return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const void *q1,
+                                const void *k1, const void *q2, const void *k2, const void *v,
+                                const float *lambda, const float *norm_w, void *out, int splits,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+  int sp = 1;
+  size_t need = 0;
+  diffattn_status st = plan_kv(desc, n_kv, splits, &sp, &need);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out) return DIFFATTN_ERR_INVALID_ARG;
+  if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+      !aligned16(out))
+    return DIFFATTN_ERR_INVALID_ARG;
+  if (sp > 1 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need))
+    return DIFFATTN_ERR_INVALID_ARG;
+  if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *part = sp > 1 ? static_cast<float *>(workspace) : nullptr;
+  st = launch_fwd_bf16_sm103(*desc, n_kv, q1, k1, q2, k2, v, lambda, norm_w, out, s, sp, part);
+  if (st != DIFFATTN_OK || sp == 1) return st;
+  return launch_splitkv_combine(*desc, n_kv, sp, part, lambda, norm_w, out, s);
 }
 
 diffattn_status diffattn_headnorm(const diffattn_desc *desc, const float *x, const float *norm_w,

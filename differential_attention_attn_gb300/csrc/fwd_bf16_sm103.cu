@@ -108,13 +108,22 @@ constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t tm_s(int k) { return 128u * k; }        // S_k / P_k
 __host__ __device__ constexpr uint32_t tm_o(int k) { return 256u + 128u * k; }  // O_k
 
+// Split-KV partial blocks (layout in internal.h).
+constexpr int64_t PART_OFF_M = kPartOffM;
+constexpr int64_t PART_OFF_L = kPartOffL;
+constexpr int64_t PART_MAP_FLOATS = kPartMapFloats;
+constexpr int64_t PART_FLOATS = kPartFloats;
+static_assert(BM == kTileRows && BN == kTileKeys && DV == kValueCols, "tile shape");
+
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;   // 2 s per pipeline wait
 constexpr uint64_t DRAIN_TIMEOUT_NS = 200000000ull;   // 0.2 s to drain in-flight copies
 
 struct Params {
   int64_t BH;
   int32_t H;
-  int32_t N;
+  int32_t N;          // query rows per head
+  int32_t N_kv;       // key/value rows per head
+  int32_t q_off;      // sequence position of query row 0 (N_kv - N): causal alignment
   int32_t n_qtiles;
   int32_t n_ktiles;
   int32_t causal;
@@ -126,6 +135,12 @@ struct Params {
   const float *norm_w;
   __nv_bfloat16 *out;
   int32_t *status;
+  // Split-KV partial mode (splits > 1): CTA blockIdx.x handles key tiles
+  // [split * split_tiles, ...) of its query tile and writes unnormalised O_k,
+  // reference maxima and running sums to `part` instead of the output.
+  int32_t splits;
+  int32_t split_tiles;
+  float *part;
 };
 
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -216,6 +231,9 @@ __device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
   return m;
 }
 
+// kPartial: split-KV partial mode (a key range per CTA, partial softmax
+// states to p.part, no epilogue); otherwise the whole forward of a query tile.
+template <bool kPartial>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     diffattn_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
                                    const __grid_constant__ CUtensorMap tm_k1,
@@ -230,14 +248,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // In split-KV mode the combine kernel launched behind this grid may be
+  // scheduled once every CTA has started; it waits for this grid's completion
+  // before reading the partial blocks.
+  if (kPartial) grid_dependents_launch();
 
   // Heaviest tiles first: all heads' last query tiles, then the previous ones.
-  const int64_t item = blockIdx.x;
+  // With split-KV, consecutive CTAs take consecutive key ranges of one item.
+  // (The single-pass instantiation keeps the key range origin a compile-time
+  // zero: a run-time origin measurably slows its loops.)
+  const int64_t item = kPartial ? blockIdx.x / p.splits : blockIdx.x;
+  const int split = kPartial ? static_cast<int>(blockIdx.x % p.splits) : 0;
   const int qt = p.n_qtiles - 1 - static_cast<int>(item / p.BH);
   const int64_t bh = item % p.BH;
   const int h = static_cast<int>(bh % p.H);
   const int q0 = qt * BM;
-  const int n_kv = p.causal ? (qt + 1) : p.n_ktiles;
+  const int n_all = static_cast<int>(key_tiles_seen(qt, p.N, p.N_kv, p.causal != 0));
+  const int kv_lo = split * p.split_tiles;  // first key tile of this CTA
+  const int n_kv = min(n_all, kv_lo + p.split_tiles) - kv_lo;
+  // Early causal query tiles see fewer key tiles than there are splits; the
+  // combine step skips those empty ranges, so the CTA has nothing to do.
+  if (kPartial && n_kv <= 0) return;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
@@ -285,7 +316,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (u > 0 && !mbar_wait(&ctrl->kv_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
           break;
         uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
-        const int32_t y = j * BN;
+        const int32_t y = (kv_lo + j) * BN;
         mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * TILE_QK_BYTES);
         tma_load_3d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, static_cast<int32_t>(bh));
         tma_load_3d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, static_cast<int32_t>(bh));
@@ -388,8 +419,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after_sync();
       // Key column c of this tile is visible to this row iff c <= lim.
-      const int kv0 = j * BN;
-      const int lim = p.causal ? (q0 + r - kv0) : (p.N - 1 - kv0);
+      const int kv0 = (kv_lo + j) * BN;
+      const int lim = p.causal ? (p.q_off + q0 + r - kv0) : (p.N_kv - 1 - kv0);
       const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
       uint32_t pk[BN / 2];
       float tile_sum = 0.f;
@@ -406,6 +437,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (exact) {
         const float mt = masked ? softmax_tile_max<true>(t_s, lim) : softmax_tile_max<false>(t_s, lim);
+        // A row can see no key at all in the first tile of a split key range
+        // (mt = -inf); it then keeps m = -inf, its p are 0 and the next tile
+        // rescales by 2^-inf = 0.
         const float m_new = fmaxf(m_run, mt * sl2);
         float alpha = 1.f;
         if (j == 0) {
@@ -432,8 +466,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         l_run *= alpha;
-        tile_sum = masked ? softmax_tile_exp<true>(t_s, m_run, sl2, lim, pk)
-                          : softmax_tile_exp<false>(t_s, m_run, sl2, lim, pk);
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        tile_sum = masked ? softmax_tile_exp<true>(t_s, m_use, sl2, lim, pk)
+                          : softmax_tile_exp<false>(t_s, m_use, sl2, lim, pk);
       }
       l_run += tile_sum;
       // P_k as packed bf16 pairs over the first 64 columns of S_k.
@@ -453,7 +488,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) ok = mbar_wait(&ctrl->o_done, 0, abort_flag, WAIT_TIMEOUT_NS);
     // Both warpgroups take the same branch: the barrier ORs every thread's view.
     const bool failed = named_barrier_or(1, 256, !ok || *abort_flag != 0);
-    if (!failed) {
+    if (kPartial && !failed) {
+      // Split-KV partial result of this map for real query rows: O_k column-major
+      // (a warp stores 32 consecutive rows of one column), as accumulated against
+      // the reference maximum, then that maximum and the running sum.
+      tc_fence_after_sync();
+      float *blk = p.part + (item * p.splits + split) * PART_FLOATS + k * PART_MAP_FLOATS;
+      const bool real = q0 + r < p.N;
+#pragma unroll 1
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(t_o + c0, v);
+        if (real) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) blk[(c0 + c) * BM + r] = __uint_as_float(v[c]);
+        }
+      }
+      if (real) {
+        blk[PART_OFF_M + r] = m_run;
+        blk[PART_OFF_L + r] = l_run;
+      }
+    } else if (!failed) {
       tc_fence_after_sync();
       float *xch = reinterpret_cast<float *>(smem + OFF_Q1);  // Q tiles are dead now
       xch[k * BM + r] = 1.f / l_run;
@@ -544,22 +599,27 @@ CUresult encode_tile_map(CUtensorMap *map, const void *base, uint64_t inner, uin
 
 }  // namespace
 
-diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
-                                      const void *q2, const void *k2, const void *v,
-                                      const float *lambda, const float *norm_w, void *out,
-                                      cudaStream_t stream) {
+diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
+                                      const void *k1, const void *q2, const void *k2,
+                                      const void *v, const float *lambda, const float *norm_w,
+                                      void *out, cudaStream_t stream, int splits, float *part) {
   const int64_t BH = desc.B * desc.H;
   const int64_t N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
-  if (BH * n_qtiles > INT32_MAX || N > INT32_MAX / 2 || desc.H > INT32_MAX)
+  const int64_t n_ktiles = (n_kv + BN - 1) / BN;
+  if (splits < 1 || (splits > 1 && part == nullptr)) return DIFFATTN_ERR_INVALID_ARG;
+  const int64_t split_tiles = (n_ktiles + splits - 1) / splits;
+  if (BH * n_qtiles * splits > INT32_MAX || N > INT32_MAX / 2 || n_kv > INT32_MAX / 2 ||
+      desc.H > INT32_MAX)
     return DIFFATTN_ERR_UNSUPPORTED;
 
   CUtensorMap maps[5];
   const void *bases[5] = {q1, k1, q2, k2, v};
   for (int i = 0; i < 5; ++i) {
     const uint64_t inner = (i == 4) ? DV : HD;
-    if (encode_tile_map(&maps[i], bases[i], inner, static_cast<uint64_t>(N),
-                        static_cast<uint64_t>(BH)) != CUDA_SUCCESS)
+    const uint64_t rows = (i == 0 || i == 2) ? N : n_kv;
+    if (encode_tile_map(&maps[i], bases[i], inner, rows, static_cast<uint64_t>(BH)) !=
+        CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
 
@@ -568,7 +628,10 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel,
+    if (cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
@@ -579,8 +642,10 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   p.BH = BH;
   p.H = static_cast<int32_t>(desc.H);
   p.N = static_cast<int32_t>(N);
+  p.N_kv = static_cast<int32_t>(n_kv);
+  p.q_off = static_cast<int32_t>(n_kv - N);
   p.n_qtiles = static_cast<int32_t>(n_qtiles);
-  p.n_ktiles = static_cast<int32_t>(n_qtiles);
+  p.n_ktiles = static_cast<int32_t>(n_ktiles);
   p.causal = desc.causal ? 1 : 0;
   p.headnorm = desc.headnorm ? 1 : 0;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
@@ -590,10 +655,17 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   p.norm_w = norm_w;
   p.out = static_cast<__nv_bfloat16 *>(out);
   p.status = desc.status_dev;
+  p.splits = splits;
+  p.split_tiles = static_cast<int32_t>(splits > 1 ? split_tiles : n_ktiles);
+  p.part = splits > 1 ? part : nullptr;
 
-  dim3 grid(static_cast<unsigned>(BH * n_qtiles));
-  diffattn_fwd_bf16_sm103_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  dim3 grid(static_cast<unsigned>(BH * n_qtiles * splits));
+  if (splits > 1)
+    diffattn_fwd_bf16_sm103_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  else
+    diffattn_fwd_bf16_sm103_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 

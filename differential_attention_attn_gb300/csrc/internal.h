@@ -8,11 +8,49 @@
 
 namespace diffattn {
 
-// Fused bf16 forward on tcgen05 / TMEM / TMA (d = 64).
-diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
-                                      const void *q2, const void *k2, const void *v,
-                                      const float *lambda, const float *norm_w, void *out,
-                                      cudaStream_t stream);
+// Tile of the fused bf16 kernel: 128 query rows x 128 keys, d = 64, 2d = 128.
+constexpr int kTileRows = 128;
+constexpr int kTileKeys = 128;
+constexpr int kValueCols = 128;
+
+// Split-KV partial block of one (work item, split), fp32: per map, O
+// column-major [kValueCols][kTileRows] as accumulated against the row's
+// reference maximum, then the reference maxima [kTileRows] (log2 units) and
+// the running sums [kTileRows].  Only real query rows are written.
+constexpr int64_t kPartOffM = int64_t{kValueCols} * kTileRows;
+constexpr int64_t kPartOffL = kPartOffM + kTileRows;
+constexpr int64_t kPartMapFloats = kPartOffL + kTileRows;
+constexpr int64_t kPartFloats = 2 * kPartMapFloats;
+constexpr int kMaxSplits = 256;
+
+// Fused bf16 forward on tcgen05 / TMEM / TMA (d = 64) of N queries against
+// n_kv keys (causal: the queries are the last N positions).  splits == 1
+// writes `out`; splits > 1 writes split-KV partial blocks to `part`, to be
+// merged by launch_splitkv_combine.
+diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
+                                      const void *k1, const void *q2, const void *k2,
+                                      const void *v, const float *lambda, const float *norm_w,
+                                      void *out, cudaStream_t stream, int splits, float *part);
+
+// Merge of the split-KV partial blocks: both maps' softmax states, then
+// o = O1/l1 - lambda O2/l2, the optional head norm and the bf16 store.
+diffattn_status launch_splitkv_combine(const diffattn_desc &desc, int64_t n_kv, int splits,
+                                       const float *part, const float *lambda,
+                                       const float *norm_w, void *out, cudaStream_t stream);
+
+// Key tiles that query tile qt (of N queries against n_kv keys) sees: all of
+// them, or under the causal mask those up to the one holding the position
+// n_kv - N + 128 qt + 127 of its last row.
+__host__ __device__ inline int64_t key_tiles_seen(int64_t qt, int64_t N, int64_t n_kv,
+                                                  bool causal) {
+  const int64_t n_ktiles = (n_kv + kTileKeys - 1) / kTileKeys;
+  if (!causal) return n_ktiles;
+  const int64_t t = ((n_kv - N) + qt * kTileRows + kTileRows - 1) / kTileKeys + 1;
+  return t < n_ktiles ? t : n_ktiles;
+}
+
+// The split count the library picks when the caller asks for 0 (splitkv.cu).
+int auto_splits(int64_t BH, int64_t N, int64_t n_kv, bool causal, int sm_count);
 
 // fp32 forward on CUDA cores (d <= 128, N <= 4096).
 diffattn_status launch_fwd_f32(const diffattn_desc &desc, const float *q1, const float *k1,

@@ -12,6 +12,16 @@ namespace diffattn {
 // ----------------------------------------------------------------------------
 // Shared-memory addresses and timers
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch: let the next kernel on the stream (launched
+// with programmatic stream serialisation) be scheduled, and, in that kernel,
+// wait until the previous grid has completed and its writes are visible.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -57,6 +57,13 @@ def load(path: str = LIB_PATH):
         dp = ctypes.POINTER(Desc)
         lib.diffattn_fwd.restype = ctypes.c_int
         lib.diffattn_fwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp]
+        lib.diffattn_fwd_kv.restype = ctypes.c_int
+        lib.diffattn_fwd_kv.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp, vp,
+                                        ctypes.c_int, vp, ctypes.c_size_t, vp]
+        lib.diffattn_fwd_kv_plan.restype = ctypes.c_int
+        lib.diffattn_fwd_kv_plan.argtypes = [dp, ctypes.c_int64, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_size_t)]
         lib.diffattn_headnorm.restype = ctypes.c_int
         lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
         lib.diffattn_lambda_init.restype = ctypes.c_double
@@ -141,6 +148,73 @@ def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_w=N
     desc = make_desc(B, H, N, d, _DTYPE_CODE[dtype], causal, headnorm, eps, lambda_init, status)
     st = load().diffattn_fwd(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
                              _ptr(lam), _ptr(norm_w), _ptr(out), _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return out
+
+
+def fwd_kv_plan(B, H, N, n_kv, *, causal: bool, splits: int = 0, d: int = 64,
+                headnorm: bool = True, raw_status: bool = False):
+    """`diffattn_fwd_kv_plan`: (split count that will run, workspace bytes)."""
+    desc = make_desc(B, H, N, d, BF16, causal, headnorm, 1e-5, 0.0)
+    sp, nb = ctypes.c_int(0), ctypes.c_size_t(0)
+    st = load().diffattn_fwd_kv_plan(ctypes.byref(desc), int(n_kv), int(splits),
+                                     ctypes.byref(sp), ctypes.byref(nb))
+    if raw_status:
+        return st, sp.value, nb.value
+    _check(st)
+    return sp.value, nb.value
+
+
+def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_w=None,
+           eps: float = 1e-5, lambda_init: float = 0.0, splits: int = 0, workspace=None,
+           out=None, status=None, stream=None, raw_status: bool = False):
+    """Forward of Nq queries against Nkv keys through `diffattn_fwd_kv` (bf16, d = 64).
+
+    q1, q2: [B, H, Nq, 64]; k1, k2: [B, H, Nkv, 64]; v: [B, H, Nkv, 128]; the
+    queries are the last Nq positions.  splits = 0 lets the library choose.
+    workspace: a CUDA tensor of at least the planned bytes, or None (a torch
+    buffer of the planned size is used).  Returns out [B, H, Nq, 128].
+    """
+    if q1.dim() != 4 or k1.dim() != 4:
+        raise ValueError("q1 and k1 must be [B, H, N, d]")
+    B, H, N, d = q1.shape
+    n_kv = k1.shape[2]
+    dtype = q1.dtype
+    for name, t, shape in (("q2", q2, (B, H, N, d)), ("k1", k1, (B, H, n_kv, d)),
+                           ("k2", k2, (B, H, n_kv, d)), ("v", v, (B, H, n_kv, 2 * d))):
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name} must be {shape} {dtype}")
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=dtype, device=q1.device)
+    if tuple(out.shape) != (B, H, N, 2 * d) or out.dtype != dtype:
+        raise ValueError("out must be [B, H, Nq, 2d] of the input dtype")
+    tensors = [q1, k1, q2, k2, v, lam, out] + ([norm_w] if norm_w is not None else [])
+    for t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if lam.dtype != torch.float32 or lam.numel() != H:
+        raise ValueError("lam must be float32 [H]")
+    if norm_w is not None and (norm_w.dtype != torch.float32 or norm_w.numel() != H * 2 * d):
+        raise ValueError("norm_w must be float32 [H, 2d]")
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(dtype, -1), causal, headnorm, eps, lambda_init,
+                     status)
+    lib = load()
+    if workspace is None:
+        sp, nb = ctypes.c_int(0), ctypes.c_size_t(0)
+        st = lib.diffattn_fwd_kv_plan(ctypes.byref(desc), int(n_kv), int(splits),
+                                      ctypes.byref(sp), ctypes.byref(nb))
+        if st != OK:
+            if raw_status:
+                return st
+            _check(st)
+        if nb.value:
+            workspace = torch.empty(nb.value, dtype=torch.uint8, device=q1.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.diffattn_fwd_kv(ctypes.byref(desc), int(n_kv), _ptr(q1), _ptr(k1), _ptr(q2),
+                             _ptr(k2), _ptr(v), _ptr(lam), _ptr(norm_w), _ptr(out), int(splits),
+                             _ptr(workspace), ws_bytes, _stream_handle(stream))
     if raw_status:
         return st
     _check(st)

@@ -64,6 +64,7 @@ class Workload:
     lambda_init_override: float | None  # fixed lambda_init when layer is None
     w: np.ndarray | None              # [H, 2d] float64 or None (ones)
     meta: dict = field(default_factory=dict)
+    n_kv: int | None = None           # key/value rows when they differ from N (k1, k2, v)
 
     @property
     def dv(self) -> int:
@@ -177,3 +178,22 @@ def custom(seed: int, *, B: int, H: int, N: int, d: int, causal: bool, headnorm:
         w = (1.0 + 0.1 * rng.standard_normal(size=(H, 2 * d))).astype(np.float32).astype(np.float64)
     return Workload(f"custom_B{B}H{H}N{N}d{d}", B, H, N, d, dtype, causal, headnorm, eps,
                     q1, k1, q2, k2, v, lam, False, layer, None if layer else 0.0, w)
+
+
+def kv_cache(seed: int, *, B: int, H: int, Nq: int, Nkv: int, d: int = 64, causal: bool = True,
+             headnorm: bool = True, lam_range=(0.1, 0.9), random_w: bool = True,
+             layer: int | None = 4, eps: float = 1e-5) -> Workload:
+    """Queries against a key/value cache: Q1, Q2 [B, H, Nq, d], K1, K2 [B, H, Nkv, d],
+    V [B, H, Nkv, 2d], all N(0,1) in bf16; the queries are the last Nq positions.
+    Draw order: K1, K2, V, Q1, Q2, lambda, w."""
+    rng = np.random.default_rng(seed)
+    k1, k2 = (_to_storage(_normal(rng, (B, H, Nkv, d), 1.0), torch.bfloat16) for _ in range(2))
+    v = _to_storage(_normal(rng, (B, H, Nkv, 2 * d), 1.0), torch.bfloat16)
+    q1, q2 = (_to_storage(_normal(rng, (B, H, Nq, d), 1.0), torch.bfloat16) for _ in range(2))
+    lam = rng.uniform(lam_range[0], lam_range[1], size=H)
+    w = None
+    if random_w:
+        w = (1.0 + 0.1 * rng.standard_normal(size=(H, 2 * d))).astype(np.float32).astype(np.float64)
+    return Workload(f"kv_B{B}H{H}Nq{Nq}Nkv{Nkv}", B, H, Nq, d, torch.bfloat16, causal, headnorm,
+                    eps, q1, k1, q2, k2, v, lam, False, layer, None if layer else 0.0, w,
+                    n_kv=Nkv)

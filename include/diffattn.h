@@ -38,6 +38,7 @@
 #ifndef DIFFATTN_H
 #define DIFFATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -57,11 +58,11 @@ typedef enum diffattn_dtype {
     DIFFATTN_F32 = 1   /* q/k/v/out fp32 throughout */
 } diffattn_dtype;
 
-/* Problem description shared by diffattn_fwd and diffattn_headnorm. */
+/* Problem description shared by every entry point. */
 typedef struct diffattn_desc {
     int64_t B;            /* batch size, >= 0 */
     int64_t H;            /* differential heads, >= 0 */
-    int64_t N;            /* tokens (queries = keys), >= 0 */
+    int64_t N;            /* tokens: queries = keys (diffattn_fwd_kv: queries), >= 0 */
     int32_t d;            /* width of one query/key half; V and out have 2d columns */
     int32_t dtype;        /* diffattn_dtype of q1, k1, q2, k2, v and out */
     int32_t causal;       /* 1: key j visible to query i iff j <= i; 0: all visible */
@@ -102,6 +103,57 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
                              const void *q2, const void *k2, const void *v,
                              const float *lambda, const float *norm_w, void *out,
                              void *stream);
+
+/*
+ * diffattn_fwd_kv — the same forward for N queries against n_kv keys, with
+ * the key range optionally split across CTAs ("split-KV").
+ *
+ * What it computes: exactly diffattn_fwd's formula ("Differential
+ * Transformer", section "How differential attention works": each map is
+ * ordinary softmax attention), with desc->N queries and n_kv keys/values per
+ * head.  The queries are the LAST N positions of the sequence: query i sits at
+ * position n_kv - N + i, so with causal = 1 it sees keys j <= n_kv - N + i
+ * (a key/value cache: N = 1..16 is decoding, N = n_kv is diffattn_fwd).
+ * Because each map is a softmax, its key range can be cut into pieces whose
+ * partial states (unnormalised accumulator, running maximum, running sum)
+ * merge exactly; with splits > 1 the fused kernel writes those states for
+ * every (head, 128-query tile, key range) to `workspace` and a second kernel
+ * merges them, forms map1 - lambda map2 and applies the head norm.  This
+ * fills the GPU when B * H * ceil(N / 128) is small against the SM count.
+ *
+ * Arguments: q1, q2 device bf16 [B, H, N, 64]; k1, k2 device bf16
+ * [B, H, n_kv, 64]; v device bf16 [B, H, n_kv, 128]; out device bf16
+ * [B, H, N, 128], fully overwritten; lambda and norm_w as for diffattn_fwd.
+ * splits: 0 lets the library choose (diffattn_fwd_kv_plan reports the
+ * choice), 1 is the single-pass kernel (no workspace), 2..256 cut each row's
+ * keys into that many ranges of ceil(ceil(n_kv / 128) / splits) 128-key tiles
+ * (requests above ceil(n_kv / 128) are lowered to it).  workspace: device
+ * buffer of at least the bytes diffattn_fwd_kv_plan reports, 16-byte aligned,
+ * caller-owned scratch whose contents on entry do not matter; unused (may be
+ * NULL) when the resolved split count is 1.  Two calls that share a workspace
+ * must be ordered (same stream, or synchronised).
+ *
+ * Errors: DIFFATTN_ERR_INVALID_ARG for a negative n_kv, causal with
+ * n_kv < N, n_kv = 0 with queries present, splits outside 0..256, a missing
+ * or short workspace, or misaligned buffers; DIFFATTN_ERR_UNSUPPORTED unless
+ * dtype is DIFFATTN_BF16 and d == 64, or on a non-sm_103 device.
+ * B * H * N == 0 returns DIFFATTN_OK without launching anything.
+ */
+diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const void *q1,
+                                const void *k1, const void *q2, const void *k2,
+                                const void *v, const float *lambda, const float *norm_w,
+                                void *out, int splits, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * diffattn_fwd_kv_plan — the split count diffattn_fwd_kv runs for this
+ * request (splits = 0: the library's choice for the current device, from its
+ * SM count and a per-CTA cost model) and the workspace bytes it needs (0 when
+ * that count is 1).  Validates exactly as diffattn_fwd_kv does apart from
+ * pointers; host-only apart from reading the device's SM count once.
+ */
+diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, int splits,
+                                     int *splits_out, size_t *workspace_bytes);
 
 /*
  * diffattn_headnorm — the per-head output normalisation on its own

@@ -35,6 +35,25 @@ def run_gpu(w, *, out=None, status=None, device="cuda"):
     return o
 
 
+def run_gpu_kv(w, *, splits=0, workspace=None, out=None, status=None, device="cuda",
+               raw_status=False):
+    """The workload through diffattn_fwd_kv (queries against its key/value rows)."""
+    li = lambda_init_for(w, "gpu")
+    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device=device)
+    nw = None if w.w is None else torch.tensor(w.w, dtype=torch.float32, device=device)
+    dev = [t.to(device) for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    o = ops.fwd_kv(*dev, lam, causal=w.causal, headnorm=w.headnorm, norm_w=nw,
+                   eps=float(np.float32(w.eps)), lambda_init=li, splits=splits,
+                   workspace=workspace, out=out, status=status, raw_status=raw_status)
+    torch.cuda.synchronize()
+    return o
+
+
+def run_oracle_kv(w, bh_idx=None, row_idx=None):
+    args, kw = oracle_args(w)
+    return oracle.fwd_kv(*args, bh_idx=bh_idx, row_idx=row_idx, **kw)
+
+
 def oracle_args(w):
     li = lambda_init_for(w, "oracle")
     f = w.f64

@@ -97,3 +97,53 @@ def test_headnorm_validation(lib):
     d = ops.make_desc(1, 1, 16, 8, ops.F32, False, True, 1e-5, 0.0)
     assert lib.diffattn_headnorm(ctypes.byref(d), None, None, ctypes.c_void_p(FAKE),
                                  None) == ops.ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------------------- fwd_kv
+PART_FLOATS = 2 * (128 * 128 + 2 * 128)  # per (work item, split): two maps' O, m and l
+
+
+def _plan(lib, desc, n_kv, splits):
+    sp, nb = ctypes.c_int(-1), ctypes.c_size_t(0)
+    st = lib.diffattn_fwd_kv_plan(ctypes.byref(desc), n_kv, splits, ctypes.byref(sp),
+                                  ctypes.byref(nb))
+    return st, sp.value, nb.value
+
+
+def _call_kv(lib, desc, n_kv, splits, ws=FAKE, ws_bytes=1 << 40):
+    p = [ctypes.c_void_p(FAKE)] * 5
+    return lib.diffattn_fwd_kv(ctypes.byref(desc), n_kv, *p, ctypes.c_void_p(FAKE), None,
+                               ctypes.c_void_p(FAKE), splits,
+                               ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+
+def test_kv_plan_explicit_splits(lib):
+    d = ops.make_desc(1, 4, 512, 64, ops.BF16, True, True, 1e-5, 0.2)
+    assert _plan(lib, d, 512, 3) == (ops.OK, 3, 16 * 3 * PART_FLOATS * 4)
+    assert _plan(lib, d, 512, 1) == (ops.OK, 1, 0)
+    assert _plan(lib, d, 512, 100) == (ops.OK, 4, 16 * 4 * PART_FLOATS * 4)  # 4 key tiles
+    dec = ops.make_desc(2, 8, 1, 64, ops.BF16, True, True, 1e-5, 0.2)  # decoding: one query
+    assert _plan(lib, dec, 16384, 8) == (ops.OK, 8, 16 * 8 * PART_FLOATS * 4)
+    empty = ops.make_desc(0, 8, 1, 64, ops.BF16, True, True, 1e-5, 0.2)
+    assert _plan(lib, empty, 100, 0) == (ops.OK, 1, 0)
+
+
+def test_kv_validation(lib):
+    d = ops.make_desc(1, 4, 512, 64, ops.BF16, True, True, 1e-5, 0.2)
+    assert _plan(lib, d, 511, 1)[0] == ops.ERR_INVALID_ARG       # causal, fewer keys than queries
+    assert _plan(lib, d, -1, 1)[0] == ops.ERR_INVALID_ARG
+    assert _plan(lib, d, 512, -1)[0] == ops.ERR_INVALID_ARG
+    assert _plan(lib, d, 512, 257)[0] == ops.ERR_INVALID_ARG
+    nc = ops.make_desc(1, 4, 512, 64, ops.BF16, False, True, 1e-5, 0.2)
+    assert _plan(lib, nc, 0, 1)[0] == ops.ERR_INVALID_ARG        # softmax over no keys
+    assert _plan(lib, nc, 100, 1)[0] == ops.OK                    # fewer keys is fine unmasked
+    f32 = ops.make_desc(1, 4, 64, 8, ops.F32, True, True, 1e-5, 0.2)
+    assert _plan(lib, f32, 64, 1)[0] == ops.ERR_UNSUPPORTED
+    wide = ops.make_desc(1, 4, 64, 128, ops.BF16, True, True, 1e-5, 0.2)
+    assert _plan(lib, wide, 64, 1)[0] == ops.ERR_UNSUPPORTED
+    assert lib.diffattn_fwd_kv_plan(ctypes.byref(d), 512, 1, None, None) == ops.ERR_INVALID_ARG
+    # split launches need a large enough, aligned workspace (checked before any launch)
+    assert _call_kv(lib, d, 512, 2, ws=0) == ops.ERR_INVALID_ARG
+    assert _call_kv(lib, d, 512, 2, ws_bytes=16 * 2 * PART_FLOATS * 4 - 4) == ops.ERR_INVALID_ARG
+    assert _call_kv(lib, d, 512, 2, ws=FAKE + 4) == ops.ERR_INVALID_ARG
+    assert _call_kv(lib, d, 511, 1) == ops.ERR_INVALID_ARG
