@@ -64,6 +64,9 @@ def load(path: str = LIB_PATH):
         lib.diffattn_fwd_kv_plan.argtypes = [dp, ctypes.c_int64, ctypes.c_int,
                                              ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_size_t)]
+        lib.diffattn_fwd_kv_noalloc.restype = ctypes.c_int
+        lib.diffattn_fwd_kv_noalloc.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
+                                                vp, ctypes.c_int, vp]
         lib.diffattn_headnorm.restype = ctypes.c_int
         lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
         lib.diffattn_lambda_init.restype = ctypes.c_double
@@ -215,6 +218,40 @@ def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_
     st = lib.diffattn_fwd_kv(ctypes.byref(desc), int(n_kv), _ptr(q1), _ptr(k1), _ptr(q2),
                              _ptr(k2), _ptr(v), _ptr(lam), _ptr(norm_w), _ptr(out), int(splits),
                              _ptr(workspace), ws_bytes, _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def fwd_kv_noalloc(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True,
+                   norm_w=None, eps: float = 1e-5, lambda_init: float = 0.0, splits: int = 0,
+                   out=None, status=None, stream=None, raw_status: bool = False):
+    """`diffattn_fwd_kv_noalloc`: fwd_kv on the library's own 64 MiB scratch area.
+
+    Same arguments and result as :func:`fwd_kv` without the workspace.  Calls
+    that overlap in time race on the shared scratch; the first call on a device
+    must not be inside a CUDA graph capture.
+    """
+    B, H, N, d = q1.shape
+    n_kv = k1.shape[2]
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=q1.device)
+    for t in [q1, k1, q2, k2, v, lam, out] + ([norm_w] if norm_w is not None else []):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if tuple(k2.shape) != tuple(k1.shape) or tuple(q2.shape) != tuple(q1.shape) or \
+            tuple(v.shape) != (B, H, n_kv, 2 * d) or tuple(out.shape) != (B, H, N, 2 * d):
+        raise ValueError("q1, q2 [B, H, Nq, d]; k1, k2 [B, H, Nkv, d]; v [B, H, Nkv, 2d]; "
+                         "out [B, H, Nq, 2d]")
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
+                     lambda_init, status)
+    st = load().diffattn_fwd_kv_noalloc(ctypes.byref(desc), int(n_kv), _ptr(q1), _ptr(k1),
+                                        _ptr(q2), _ptr(k2), _ptr(v), _ptr(lam), _ptr(norm_w),
+                                        _ptr(out), int(splits), _stream_handle(stream))
     if raw_status:
         return st
     _check(st)

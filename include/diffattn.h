@@ -155,6 +155,39 @@ diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const v
 diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, int splits,
                                      int *splits_out, size_t *workspace_bytes);
 
+/* Size of the scratch area diffattn_fwd_kv_noalloc uses: 64 MiB. */
+#define DIFFATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * diffattn_fwd_kv_noalloc — diffattn_fwd_kv without a caller workspace.
+ * The pages have no counterpart to this entry point: it is a convenience of
+ * this library for callers that cannot hand over scratch memory.
+ *
+ * Computes exactly what diffattn_fwd_kv computes, with the same arguments
+ * apart from the workspace: the split-KV partial blocks go to a fixed
+ * DIFFATTN_NOALLOC_SCRATCH_BYTES area that the library owns (a static device
+ * array of its module; nothing is allocated).  Its device address is looked
+ * up once per device with cudaGetSymbolAddress on the first call that needs
+ * it; a failed lookup returns DIFFATTN_ERR_CUDA.  Nothing in the area has to
+ * start at zero, so nothing is cleared.
+ *
+ * Errors: those of diffattn_fwd_kv and diffattn_fwd_kv_plan, plus
+ * DIFFATTN_ERR_UNSUPPORTED when the planned workspace exceeds
+ * DIFFATTN_NOALLOC_SCRATCH_BYTES (checked before anything is launched).
+ *
+ * Caveats: every call on a device shares the one scratch area, so calls
+ * that overlap in time (different streams, or different host threads without
+ * ordering) race on it and give undefined results; order them.  The first
+ * call on each device performs the set-up (the symbol lookup, which can load
+ * the module), so it must come before any CUDA stream capture that records
+ * this entry point.
+ */
+diffattn_status diffattn_fwd_kv_noalloc(const diffattn_desc *desc, int64_t n_kv,
+                                        const void *q1, const void *k1, const void *q2,
+                                        const void *k2, const void *v, const float *lambda,
+                                        const float *norm_w, void *out, int splits,
+                                        void *stream);
+
 /*
  * diffattn_headnorm — the per-head output normalisation on its own
  * ("Differential Transformer", section "How differential attention works":
