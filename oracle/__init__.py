@@ -60,6 +60,9 @@ def _declare(lib):
     lib.oracle_fwd_kv_rows.restype = i
     lib.oracle_fwd_kv_rows.argtypes = [i, i, i64, i64, i, p, p, p, p, p, p, i, i, p, d, d,
                                        i64, p, p, p, i]
+    lib.oracle_bwd.restype = i
+    lib.oracle_bwd.argtypes = [i, i, i64, i, p, p, p, p, p, p, i, i, p, d, d, p, p, p, p, p, p,
+                               p, p, i]
     lib.oracle_diff_map.restype = i
     lib.oracle_diff_map.argtypes = [i64, i, p, p, p, p, d, i, p]
     lib.oracle_headnorm.restype = i
@@ -195,6 +198,34 @@ def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool, bh_idx=None,
     if rc != 0:
         raise RuntimeError(f"oracle_fwd_kv_rows failed with code {rc}")
     return out
+
+
+def bwd(q1, k1, q2, k2, v, lam, dy, *, causal: bool, headnorm: bool, w=None,
+        eps: float = 1e-5, lambda_init_value: float = 0.0, nthreads: int = 0, lib=None):
+    """Gradients of sum(y * dy) for the head forward, float64.
+
+    Returns dict with dq1, dk1, dq2, dk2 [B, H, N, d], dv [B, H, N, 2d], dlam [H]
+    and dw [H, 2d] (zeros without the norm).
+    """
+    q1, k1, q2, k2, v, dy = map(_f64, (q1, k1, q2, k2, v, dy))
+    B, H, N, d = _check_shapes(q1, k1, q2, k2, v)
+    if dy.shape != v.shape:
+        raise ValueError("dy must be [B, H, N, 2d]")
+    lam = _f64(lam).reshape(H)
+    wv = None if w is None else _f64(w).reshape(H, 2 * d)
+    g = {k: np.zeros((B, H, N, d)) for k in ("dq1", "dk1", "dq2", "dk2")}
+    g["dv"] = np.zeros((B, H, N, 2 * d))
+    g["dlam"] = np.zeros(H)
+    g["dw"] = np.zeros((H, 2 * d))
+    rc = (lib or load()).oracle_bwd(B, H, N, d, _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
+                                    _ptr(lam), int(bool(causal)), int(bool(headnorm)), _ptr(wv),
+                                    float(eps), float(lambda_init_value), _ptr(dy),
+                                    _ptr(g["dq1"]), _ptr(g["dk1"]), _ptr(g["dq2"]),
+                                    _ptr(g["dk2"]), _ptr(g["dv"]), _ptr(g["dlam"]),
+                                    _ptr(g["dw"]), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_bwd failed with code {rc}")
+    return g
 
 
 def diff_map(q1, k1, q2, k2, lam: float, *, causal: bool, lib=None) -> np.ndarray:

@@ -335,3 +335,164 @@ int oracle_headnorm(int64_t R, int dv, int H, const double *x,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward pass (gradients of the head forward above).
+ *
+ * The pages give the forward only; its gradient is the plain derivative of
+ * that definition, written out here by the chain rule in float64, one query
+ * row at a time, both maps materialised, nothing blocked or fused:
+ *
+ *   forward (row i):  p1 = softmax(s1), p2 = softmax(s2), s_k[j] = q_k.k_k[j] / sqrt(d)
+ *                     o1 = p1 V, o2 = p2 V, o = o1 - lambda o2
+ *                     y  = o r g,  r = 1 / sqrt(mean(o^2) + eps),  g = w (1 - lambda_init)
+ *   given dy (row i):
+ *     norm:    do = r g dy - (r^3 / 2d) o sum_c(dy_c g_c o_c);   dw += dy o r (1 - lambda_init)
+ *              (without the norm: do = dy)
+ *     lambda:  dlambda += -(do . o2)
+ *     values:  dV[j] += (p1[j] - lambda p2[j]) do
+ *     maps:    dp1[j] = do . v_j,  dp2[j] = -lambda do . v_j
+ *     softmax: ds_k[j] = p_k[j] (dp_k[j] - sum_j' p_k[j'] dp_k[j'])
+ *     logits:  dq_k += ds_k[j] k_k[j] / sqrt(d),  dk_k[j] += ds_k[j] q_k / sqrt(d)
+ *
+ * Layouts as in oracle_fwd; gradients have the shapes of their tensors;
+ * dlam is [H] and dw is [H, 2d] (dw is left untouched without the norm).
+ * All outputs are overwritten.  Returns 0, -1 on bad arguments, -2 if
+ * scratch could not be allocated.
+ */
+static void bwd_head(int64_t N, int d, const double *q1, const double *k1,
+                     const double *q2, const double *k2, const double *v, double lam,
+                     int causal, int headnorm, const double *w_head, double eps,
+                     double lambda_init, const double *dy, double *dq1, double *dk1,
+                     double *dq2, double *dk2, double *dv, double *dlam, double *dw,
+                     double *scratch)
+{
+    const int dv_ = 2 * d;
+    const double scale = 1.0 / sqrt((double)d);
+    double *p1 = scratch, *p2 = scratch + N;
+    double *o1 = scratch + 2 * N, *o2 = o1 + dv_, *o = o2 + dv_, *dout = o + dv_;
+    for (int64_t i = 0; i < N; ++i) {
+        const double *q1i = q1 + i * d, *q2i = q2 + i * d, *dyi = dy + i * dv_;
+        softmax_row(i, N, d, q1i, k1, causal, p1);
+        softmax_row(i, N, d, q2i, k2, causal, p2);
+        for (int c = 0; c < dv_; ++c)
+            o1[c] = o2[c] = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            for (int c = 0; c < dv_; ++c) {
+                o1[c] += p1[j] * v[j * dv_ + c];
+                o2[c] += p2[j] * v[j * dv_ + c];
+            }
+        for (int c = 0; c < dv_; ++c)
+            o[c] = o1[c] - lam * o2[c];
+        /* norm backward */
+        if (headnorm) {
+            double ms = 0.0, t = 0.0;
+            for (int c = 0; c < dv_; ++c)
+                ms += o[c] * o[c];
+            ms /= (double)dv_;
+            const double r = 1.0 / sqrt(ms + eps);
+            for (int c = 0; c < dv_; ++c) {
+                const double g = (w_head ? w_head[c] : 1.0) * (1.0 - lambda_init);
+                t += dyi[c] * g * o[c];
+            }
+            for (int c = 0; c < dv_; ++c) {
+                const double g = (w_head ? w_head[c] : 1.0) * (1.0 - lambda_init);
+                dout[c] = r * g * dyi[c] - r * r * r / (double)dv_ * o[c] * t;
+                dw[c] += dyi[c] * o[c] * r * (1.0 - lambda_init);
+            }
+        } else {
+            for (int c = 0; c < dv_; ++c)
+                dout[c] = dyi[c];
+        }
+        /* lambda */
+        double do_o1 = 0.0, do_o2 = 0.0;
+        for (int c = 0; c < dv_; ++c) {
+            do_o1 += dout[c] * o1[c];
+            do_o2 += dout[c] * o2[c];
+        }
+        *dlam -= do_o2;
+        /* values, maps, softmax, logits */
+        for (int64_t j = 0; j < N; ++j) {
+            if (!visible(i, j, causal))
+                continue;
+            double dvj = 0.0; /* do . v_j */
+            for (int c = 0; c < dv_; ++c) {
+                dv[j * dv_ + c] += (p1[j] - lam * p2[j]) * dout[c];
+                dvj += dout[c] * v[j * dv_ + c];
+            }
+            /* sum_j' p1 dp1 = do . o1 ; sum_j' p2 dp2 = -lambda do . o2 */
+            const double ds1 = p1[j] * (dvj - do_o1);
+            const double ds2 = p2[j] * (-lam * dvj + lam * do_o2);
+            for (int c = 0; c < d; ++c) {
+                dq1[i * d + c] += ds1 * k1[j * d + c] * scale;
+                dk1[j * d + c] += ds1 * q1i[c] * scale;
+                dq2[i * d + c] += ds2 * k2[j * d + c] * scale;
+                dk2[j * d + c] += ds2 * q2i[c] * scale;
+            }
+        }
+    }
+}
+
+int oracle_bwd(int B, int H, int64_t N, int d, const double *q1, const double *k1,
+               const double *q2, const double *k2, const double *v, const double *lam,
+               int causal, int headnorm, const double *w, double eps, double lambda_init,
+               const double *dy, double *dq1, double *dk1, double *dq2, double *dk2,
+               double *dv, double *dlam, double *dw, int nthreads)
+{
+    if (B < 0 || H <= 0 || N < 0 || d <= 0)
+        return -1;
+    const int64_t BH = (int64_t)B * H;
+    const int dv_ = 2 * d;
+    const size_t nqk = (size_t)(BH * N * d), nv = (size_t)(BH * N * dv_);
+    memset(dq1, 0, nqk * sizeof(double));
+    memset(dk1, 0, nqk * sizeof(double));
+    memset(dq2, 0, nqk * sizeof(double));
+    memset(dk2, 0, nqk * sizeof(double));
+    memset(dv, 0, nv * sizeof(double));
+    /* per-(b, h) partial sums of dlambda and dw, added up per head afterwards */
+    double *plam = (double *)calloc((size_t)(BH > 0 ? BH : 1), sizeof(double));
+    double *pw = (double *)calloc((size_t)(BH > 0 ? BH : 1) * dv_, sizeof(double));
+    if (!plam || !pw) {
+        free(plam);
+        free(pw);
+        return -2;
+    }
+    int err = 0;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double *scratch = (double *)malloc(sizeof(double) * (size_t)(2 * N + 4 * dv_ + 1));
+        if (!scratch) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < BH; ++bh) {
+            if (!scratch)
+                continue;
+            const int h = (int)(bh % H);
+            const int64_t qk = bh * N * d, vo = bh * N * dv_;
+            bwd_head(N, d, q1 + qk, k1 + qk, q2 + qk, k2 + qk, v + vo, lam[h], causal,
+                     headnorm, w ? w + (int64_t)h * dv_ : NULL, eps, lambda_init, dy + vo,
+                     dq1 + qk, dk1 + qk, dq2 + qk, dk2 + qk, dv + vo, plam + bh,
+                     pw + bh * dv_, scratch);
+        }
+        free(scratch);
+    }
+    for (int h = 0; h < H; ++h) {
+        dlam[h] = 0.0;
+        if (headnorm)
+            for (int c = 0; c < dv_; ++c)
+                dw[(int64_t)h * dv_ + c] = 0.0;
+    }
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const int h = (int)(bh % H);
+        dlam[h] += plam[bh];
+        if (headnorm)
+            for (int c = 0; c < dv_; ++c)
+                dw[(int64_t)h * dv_ + c] += pw[bh * dv_ + c];
+    }
+    free(plam);
+    free(pw);
+    return err;
+}

@@ -321,6 +321,87 @@ def pin_kv_zero_queries(lib):
     return err < 1e-13, f"max err {err:.3e}"
 
 
+def _fd_grads(lib, tensors, lam, w, dy, causal, headnorm, eps, li, h=1e-6):
+    """Central differences of L = sum(y * dy) through the forward oracle."""
+    names = ["q1", "k1", "q2", "k2", "v"]
+    params = dict(zip(names, [t.copy() for t in tensors]))
+    params["lam"] = lam.copy()
+    params["w"] = w.copy()
+
+    def loss():
+        y = oracle.fwd(*(params[n] for n in names), params["lam"], causal=causal,
+                       headnorm=headnorm, w=params["w"], eps=eps, lambda_init_value=li,
+                       lib=lib)
+        return float(np.sum(y * dy))
+
+    grads = {}
+    for n, arr in params.items():
+        g = np.zeros_like(arr)
+        flat, gflat = arr.reshape(-1), g.reshape(-1)
+        for idx in range(flat.size):
+            keep = flat[idx]
+            flat[idx] = keep + h
+            lp = loss()
+            flat[idx] = keep - h
+            lm = loss()
+            flat[idx] = keep
+            gflat[idx] = (lp - lm) / (2 * h)
+        grads[n] = g
+    return grads
+
+
+def pin_bwd_finite_differences(lib):
+    """Every gradient of the backward oracle matches central differences of the
+    forward oracle (loss sum(y * dy)), causal or not, with and without the norm."""
+    worst = 0.0
+    for seed, causal, headnorm in [(61, True, True), (62, False, True), (63, True, False),
+                                   (64, False, False)]:
+        rng, q1, k1, q2, k2, v = _rand(seed, 1, 2, 5, 3)
+        lam = rng.uniform(-0.3, 1.2, size=2)
+        w = rng.uniform(0.5, 1.5, size=(2, 6))
+        dy = rng.standard_normal(v.shape)
+        eps, li = 1e-2, 0.35
+        g = oracle.bwd(q1, k1, q2, k2, v, lam, dy, causal=causal, headnorm=headnorm, w=w,
+                       eps=eps, lambda_init_value=li, lib=lib)
+        fd = _fd_grads(lib, [q1, k1, q2, k2, v], lam, w, dy, causal, headnorm, eps, li)
+        pairs = [("dq1", "q1"), ("dk1", "k1"), ("dq2", "q2"), ("dk2", "k2"), ("dv", "v"),
+                 ("dlam", "lam"), ("dw", "w")]
+        for gn, pn in pairs:
+            scale = max(1.0, float(np.max(np.abs(fd[pn]))))
+            worst = max(worst, float(np.max(np.abs(g[gn] - fd[pn]))) / scale)
+    return worst < 1e-7, f"max rel err {worst:.3e}"
+
+
+def pin_bwd_lambda_zero_is_sdpa_grad(lib):
+    """lambda = 0, no norm: map 2 gets no gradient and the rest is the float64 autograd
+    gradient of torch scaled_dot_product_attention (an independent implementation)."""
+    worst = 0.0
+    for seed, causal in [(65, True), (66, False)]:
+        rng, q1, k1, q2, k2, v = _rand(seed, 2, 2, 9, 4)
+        dy = rng.standard_normal(v.shape)
+        g = oracle.bwd(q1, k1, q2, k2, v, np.zeros(2), dy, causal=causal, headnorm=False,
+                       lib=lib)
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_() for x in (q1, k1, v))
+        out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal)
+        out.backward(torch.from_numpy(dy))
+        worst = max(worst, float(np.max(np.abs(g["dq1"] - tq.grad.numpy()))),
+                    float(np.max(np.abs(g["dk1"] - tk.grad.numpy()))),
+                    float(np.max(np.abs(g["dv"] - tv.grad.numpy()))),
+                    float(np.max(np.abs(g["dq2"]))), float(np.max(np.abs(g["dk2"]))))
+    return worst < 1e-12, f"max err {worst:.3e}"
+
+
+def pin_bwd_identical_maps_lambda(lib):
+    """q2 = q1, k2 = k1, no norm: y = (1 - lambda) SDPA, so dL/dlambda = -sum(SDPA * dy)."""
+    rng, q1, k1, _, _, v = _rand(67, 2, 3, 7, 4)
+    lam = rng.uniform(0.1, 0.9, size=3)
+    dy = rng.standard_normal(v.shape)
+    g = oracle.bwd(q1, k1, q1, k1, v, lam, dy, causal=True, headnorm=False, lib=lib)
+    ref = -np.sum(_sdpa(q1, k1, v, True) * dy, axis=(0, 2, 3))
+    err = float(np.max(np.abs(g["dlam"] - ref)))
+    return err < 1e-12, f"max err {err:.3e}"
+
+
 PINS = {name[4:]: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
 
 

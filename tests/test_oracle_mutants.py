@@ -51,6 +51,22 @@ MUTANTS = [
     ("kv_key_stride_of_queries", "ko = bh * Nkv * d,", "ko = bh * Nq * d,"),
     ("kv_value_stride_of_queries", "vo = bh * Nkv * dv;", "vo = bh * Nq * dv;"),
     ("kv_query_stride_of_keys", "qo = bh * Nq * d,", "qo = bh * Nkv * d,"),
+    # backward
+    ("bwd_ds2_sign", "const double ds2 = p2[j] * (-lam * dvj + lam * do_o2);",
+     "const double ds2 = p2[j] * (lam * dvj - lam * do_o2);"),
+    ("bwd_softmax_centre_dropped", "const double ds1 = p1[j] * (dvj - do_o1);",
+     "const double ds1 = p1[j] * dvj;"),
+    ("bwd_dk_unscaled", "dk1[j * d + c] += ds1 * q1i[c] * scale;",
+     "dk1[j * d + c] += ds1 * q1i[c];"),
+    ("bwd_dv_plus_lambda", "dv[j * dv_ + c] += (p1[j] - lam * p2[j]) * dout[c];",
+     "dv[j * dv_ + c] += (p1[j] + lam * p2[j]) * dout[c];"),
+    ("bwd_norm_term_halved", "dout[c] = r * g * dyi[c] - r * r * r / (double)dv_ * o[c] * t;",
+     "dout[c] = r * g * dyi[c] - r * r * r / (double)(2 * dv_) * o[c] * t;"),
+    ("bwd_dw_missing_lambda_init", "dw[c] += dyi[c] * o[c] * r * (1.0 - lambda_init);",
+     "dw[c] += dyi[c] * o[c] * r;"),
+    ("bwd_dlambda_of_map1", "*dlam -= do_o2;", "*dlam -= do_o1;"),
+    ("bwd_dq2_uses_k1", "dq2[i * d + c] += ds2 * k2[j * d + c] * scale;",
+     "dq2[i * d + c] += ds2 * k1[j * d + c] * scale;"),
 ]
 
 
