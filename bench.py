@@ -8,6 +8,9 @@ B=2, H=16, N=4096, d=64 (value width 128).  Prints one JSON line.
                   [--workload needle_4k|small_causal|mid_causal|long_16k|decode_16k]
 
 --workload picks another measured shape (default needle_4k, the headline).
+needle_4k_bwd times the backward pass (diffattn_bwd given the saved
+activations of diffattn_fwd_train) on the needle_4k shape, at 20*d
+algorithmic flops per visible pair.
 decode_16k is one decoding step of 32 heads (B=1, H=32, one query each)
 against a 16384-key cache through diffattn_fwd_kv with the library's split
 count; it is bound by HBM, so its metric is algorithmic GB/s (the cache read
@@ -433,12 +436,126 @@ def decode_cpu_baseline(w, seconds: float):
             "sample": f"{n} whole decoding steps of {w.name}, float64 oracle; {dt:.1f} s"}
 
 
+BWD_METRIC = "diff-attn bwd TFLOP/s (causal, bf16), 1 GPU"
+
+
+def run_bwd(args):
+    """One backward pass per step (diffattn_bwd given diffattn_fwd_train's saved
+    activations) on the needle_4k shape; 20*d algorithmic flops per visible pair."""
+    from differential_attention_attn_gb300 import ops
+    from differential_attention_attn_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ops.load()
+    w = W.make("needle_4k", seed_offset=rank)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    li = float(np.float32(w.lambda_init_override))
+    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device=dev)
+    kw = dict(causal=True, headnorm=True, eps=float(np.float32(w.eps)), lambda_init=li)
+    rng = np.random.default_rng(77 + rank)
+    dy_host = torch.from_numpy(rng.standard_normal((B, H, N, 2 * d))).to(torch.bfloat16)
+    host = [t.contiguous() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    saved_bytes, ws_bytes = ops.train_sizes(B, H, N)
+    set_bytes = sum(t.numel() * t.element_size() for t in host) + saved_bytes + \
+        dy_host.numel() * 2
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    sets = []
+    for _ in range(n_sets):
+        ins = [t.to(dev) for t in host]
+        _, saved = ops.fwd_train(*ins, lam, **kw)
+        sets.append((ins, saved, dy_host.to(dev)))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    grads = {k: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+             for k in ("dq1", "dk1", "dq2", "dk2")}
+    grads["dv"] = torch.empty((B, H, N, 2 * d), dtype=torch.bfloat16, device=dev)
+    grads["dlam"] = torch.empty(H, dtype=torch.float32, device=dev)
+    grads["dw"] = torch.empty((H, 2 * d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        ins, saved, dy = sets[i % n_sets]
+        ops.bwd(*ins, lam, saved, dy, workspace=ws, grads=grads, stream=stream, **kw)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    times = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_total = float(times[0])
+    flops_step = alg_flops(B, H, N, d) * 20.0 / 8.0
+    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = read_peaks()
+    peak = float(peaks["bf16_tflops"])
+    launch_ms = ms_total / args.steps
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": launch_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "needle_4k_bwd", "B": B, "H": H, "N": N, "d": d, "dv": 2 * d,
+                   "causal": True, "headnorm": True,
+                   "flops_convention": "20*d per visible pair (S1, S2, dW, dV, dQ, dK), "
+                                       "B*H*N^2/2 pairs",
+                   "l2": f"rotating {n_sets} sets of {set_bytes / 1e6:.1f} MB "
+                         f"(> {L2_BYTES / 1e6:.0f} MB L2)",
+                   "parallelism": f"weak x{world} (one full workload per rank)"},
+        "roofline": {"bound": "tensor", "achieved": flops_step / (launch_ms * 1e-3) / 1e12,
+                     "peak": peak, "unit": UNIT,
+                     "frac": flops_step / (launch_ms * 1e-3) / 1e12 / peak,
+                     "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS bf16 GEMM)",
+                     "kernel": "diffattn_bwd_pre_kernel + diffattn_bwd_bf16_sm103_kernel + "
+                               "diffattn_bwd_finish_kernel (+ 4 memsets), timed together",
+                     "alg_flops_per_launch": flops_step, "traffic": None},
+        "gpu_launches": args.steps * 3,
+        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def run_ours(args):
     from differential_attention_attn_gb300 import ops
     from differential_attention_attn_gb300 import workloads as W
 
     if args.workload in DECODE:
         return run_decode(args)
+    if args.workload == "needle_4k_bwd":
+        return run_bwd(args)
     WORKLOAD = args.workload
 
     world, rank, local = dist_env()
@@ -583,7 +700,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["needle_4k", "small_causal", "mid_causal", "long_16k", *DECODE])
+                    choices=["needle_4k", "small_causal", "mid_causal", "long_16k", *DECODE,
+                             "needle_4k_bwd"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":

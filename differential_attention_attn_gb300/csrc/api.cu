@@ -151,6 +151,58 @@ diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const v
   return launch_splitkv_combine(*desc, n_kv, sp, part, lambda, norm_w, out, s);
 }
 
+diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_bytes,
+                                     size_t *workspace_bytes) {
+  diffattn_status st = check_desc(desc);
+  if (st != DIFFATTN_OK) return st;
+  if (saved_bytes == nullptr || workspace_bytes == nullptr) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+  const int64_t BH = desc->B * desc->H;
+  *saved_bytes = static_cast<size_t>(saved_floats(BH, desc->N)) * sizeof(float);
+  *workspace_bytes = static_cast<size_t>(bwd_workspace_floats(BH, desc->N)) * sizeof(float);
+  return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, const void *k1,
+                                   const void *q2, const void *k2, const void *v,
+                                   const float *lambda, const float *norm_w, void *out,
+                                   void *saved, size_t saved_bytes, void *stream) {
+  size_t need = 0, ws = 0;
+  diffattn_status st = diffattn_train_sizes(desc, &need, &ws);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out || !saved) return DIFFATTN_ERR_INVALID_ARG;
+  if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+      !aligned16(out) || !aligned16(saved) || saved_bytes < need)
+    return DIFFATTN_ERR_INVALID_ARG;
+  if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
+                               static_cast<cudaStream_t>(stream), 1, nullptr,
+                               static_cast<float *>(saved));
+}
+
+diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
+                             const void *q2, const void *k2, const void *v, const float *lambda,
+                             const float *norm_w, const void *saved, const void *dy, void *dq1,
+                             void *dk1, void *dq2, void *dk2, void *dv, float *dlambda,
+                             float *dnorm_w, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+  size_t saved_need = 0, ws_need = 0;
+  diffattn_status st = diffattn_train_sizes(desc, &saved_need, &ws_need);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  const void *ptrs[] = {q1, k1, q2, k2, v, saved, dy, dq1, dk1, dq2, dk2, dv, workspace};
+  for (const void *q : ptrs)
+    if (q == nullptr || !aligned16(q)) return DIFFATTN_ERR_INVALID_ARG;
+  if (!lambda || !dlambda || workspace_bytes < ws_need) return DIFFATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DIFFATTN_ERR_INVALID_ARG;
+  if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  return launch_bwd_bf16_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w,
+                               static_cast<const float *>(saved), dy, dq1, dk1, dq2, dk2, dv,
+                               dlambda, dnorm_w, static_cast<float *>(workspace),
+                               static_cast<cudaStream_t>(stream));
+}
+
 diffattn_status diffattn_headnorm(const diffattn_desc *desc, const float *x, const float *norm_w,
                                   void *out, void *stream) {
   diffattn_status st = check_desc(desc);

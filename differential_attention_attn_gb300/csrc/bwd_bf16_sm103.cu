@@ -1,0 +1,735 @@
+// Backward pass of the differential-attention head on sm_103a.
+//
+// What it computes: the gradient of the head forward ("Differential
+// Transformer", Ultralytics glossary, section "How differential attention
+// works": map_k = softmax(Q_k K_k^T / sqrt(d)), o = (map1 - lambda map2) V,
+// per-head RMS normalisation, times (1 - lambda_init)).  The pages give the
+// forward only; the gradient is its derivative by the chain rule:
+//
+//   norm:    do = r g dy - (r^3 / 2d) o sum_c(dy g o),   r = rsqrt(mean o^2 + eps),
+//            g = w (1 - lambda_init);  dw += dy o r (1 - lambda_init)
+//   lambda:  dlambda = -sum_rows do . o2,  o_k = map_k V (normalised map outputs)
+//   values:  dV = map1^T do - lambda map2^T do
+//   maps:    dW = do V^T,  dS_k = c_k P_k * (dW - D_k),  D_k = do . o_k,
+//            c_1 = 1, c_2 = -lambda
+//   logits:  dQ_k = dS_k K_k / sqrt(d),  dK_k = dS_k^T Q_k / sqrt(d)
+//
+// Kernels:
+//   1. diffattn_bwd_pre_kernel: one warp per row: do (bf16, for the tensor
+//      cores), D_1 and D_2 from the bf16-rounded do, and per-head sums of
+//      dlambda and dw (block reduction, one atomic per head and column).
+//   2. diffattn_bwd_bf16_sm103_kernel: one CTA per (head, 128-key tile, map).
+//      P is recomputed from the forward's saved log2-sum-exp, with keys on the
+//      TMEM lanes (S^T = K Q^T), so dV and dK accumulate in tensor memory over
+//      the query tiles; dQ of each query tile goes to an fp32 accumulator with
+//      vector reductions.  TMEM (512 columns): S^T / P^T 0-127, dW^T 128-255,
+//      dV 256-383, dK 384-447, dQ 448-511.
+//   3. diffattn_bwd_finish_kernel: fp32 accumulators -> bf16 gradients.
+//
+// Roles in kernel 2 (512 threads): warp 0 TMA producer; warp 1 TMEM
+// allocator and single MMA-issuing thread; warps 4-11 two warpgroups (query
+// columns 0-63 and 64-127 of the tile; thread = key row) computing P^T and
+// dS^T; warps 12-15 draining dQ (thread = query row).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace diffattn {
+namespace {
+
+constexpr int BK = 128;  // keys per CTA (TMEM lanes of S^T, dV, dK)
+constexpr int BQ = 128;  // queries per tile
+constexpr int HD = 64;
+constexpr int DV = 128;
+constexpr int NUM_THREADS = 512;
+
+constexpr uint32_t TILE64 = 128 * HD * 2;            // one [128 x 64] bf16 box: 16 KB
+constexpr uint32_t OFF_K = 0;                         // K_k [128 keys x 64]
+constexpr uint32_t OFF_V = OFF_K + TILE64;            // V [128 keys x 128]: two boxes
+constexpr uint32_t OFF_Q = OFF_V + 2 * TILE64;        // 2 stages of Q_k [128 x 64]
+constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE64;       // 2 stages of dO [128 x 128]
+constexpr uint32_t OFF_DS = OFF_DO + 4 * TILE64;      // dS^T [128 keys x 128 queries]
+constexpr uint32_t OFF_VEC = OFF_DS + 2 * TILE64;     // 2 stages of (lse[128], D[128])
+constexpr uint32_t VEC_BYTES = 2 * BQ * 4;
+constexpr uint32_t OFF_CTRL = OFF_VEC + 2 * VEC_BYTES;
+
+struct Ctrl {
+  uint64_t kv_full;
+  uint64_t qd_full[2];
+  uint64_t qd_empty[2];
+  uint64_t s_full;
+  uint64_t ds_ready;
+  uint64_t dq_full;
+  uint64_t dq_free;
+  uint64_t acc_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr uint32_t SMEM_BYTES = OFF_CTRL + sizeof(Ctrl) + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
+static_assert(SMEM_BYTES + 1024 < (1u << 18), "descriptor start addresses must stay below 256 KB");
+
+constexpr uint32_t TM_S = 0, TM_W = 128, TM_DV = 256, TM_DK = 384, TM_DQ = 448;
+constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
+constexpr uint64_t DRAIN_TIMEOUT_NS = 200000000ull;
+
+struct BwdParams {
+  int64_t BH;
+  int32_t H, N, n_qtiles, n_ktiles, causal;
+  float scale_log2;  // log2(e) / sqrt(d)
+  float scale;       // 1 / sqrt(d)
+  const float *lambda;
+  const float *lse;   // [2][BH][n_pad] log2-sum-exp from the forward
+  const float *dvec;  // [2][BH][n_pad] D_k
+  __nv_bfloat16 *dk1, *dk2;  // [BH][N][64]
+  float *dq_acc;             // [2][BH][N][64], zeroed
+  float *dv_acc;             // [BH][N][128], zeroed
+  int32_t *status;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+// Instruction descriptor, kind::f16, bf16 A and B, fp32 D; a_mn / b_mn select
+// MN-major (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_ab(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Plain (non-tensor) bulk copy global -> shared, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > DRAIN_TIMEOUT_NS) return false;
+  }
+  return true;
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled
+// tile of 128-byte rows.
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------- kernel 2
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    diffattn_bwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
+                                   const __grid_constant__ CUtensorMap tm_k1,
+                                   const __grid_constant__ CUtensorMap tm_q2,
+                                   const __grid_constant__ CUtensorMap tm_k2,
+                                   const __grid_constant__ CUtensorMap tm_v,
+                                   const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + OFF_CTRL);
+  volatile int *abort_flag = &ctrl->abort;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // Heaviest key tiles first (under the causal mask key tile 0 sees every query tile).
+  const int map = static_cast<int>(blockIdx.x & 1);
+  const int64_t item = blockIdx.x >> 1;
+  const int kt = static_cast<int>(item / p.BH);
+  const int64_t bh = item % p.BH;
+  const int h = static_cast<int>(bh % p.H);
+  const int k0 = kt * BK;
+  const int qt_first = p.causal ? kt : 0;
+  const int n_q = p.n_qtiles - qt_first;
+  const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BQ;
+  const float *lse_g = p.lse + (map * p.BH + bh) * n_pad;
+  const float *dvec_g = p.dvec + (map * p.BH + bh) * n_pad;
+  const CUtensorMap *tm_q = map ? &tm_q2 : &tm_q1;
+  const CUtensorMap *tm_k = map ? &tm_k2 : &tm_k1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctrl->qd_full[s], 1);
+      mbar_init(&ctrl->qd_empty[s], 1);
+    }
+    mbar_init(&ctrl->s_full, 1);
+    mbar_init(&ctrl->ds_ready, 256);
+    mbar_init(&ctrl->dq_full, 1);
+    mbar_init(&ctrl->dq_free, 128);
+    mbar_init(&ctrl->acc_done, 1);
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(tm_q);
+    tma_prefetch_desc(tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t issued[2] = {0, 0};
+      mbar_arrive_expect_tx(&ctrl->kv_full, 3 * TILE64);
+      tma_load_3d(smem + OFF_K, tm_k, &ctrl->kv_full, 0, k0, static_cast<int32_t>(bh));
+      tma_load_3d(smem + OFF_V, &tm_v, &ctrl->kv_full, 0, k0, static_cast<int32_t>(bh));
+      tma_load_3d(smem + OFF_V + TILE64, &tm_v, &ctrl->kv_full, HD, k0,
+                  static_cast<int32_t>(bh));
+      for (int it = 0; it < n_q; ++it) {
+        const int s = it & 1;
+        const uint32_t u = static_cast<uint32_t>(it >> 1);
+        if (u > 0 && !mbar_wait(&ctrl->qd_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
+          break;
+        const int q0 = (qt_first + it) * BQ;
+        uint64_t *bar = &ctrl->qd_full[s];
+        mbar_arrive_expect_tx(bar, 3 * TILE64 + VEC_BYTES);
+        tma_load_3d(smem + OFF_Q + s * TILE64, tm_q, bar, 0, q0, static_cast<int32_t>(bh));
+        uint8_t *dst = smem + OFF_DO + s * 2 * TILE64;
+        tma_load_3d(dst, &tm_do, bar, 0, q0, static_cast<int32_t>(bh));
+        tma_load_3d(dst + TILE64, &tm_do, bar, HD, q0, static_cast<int32_t>(bh));
+        float *vec = reinterpret_cast<float *>(smem + OFF_VEC + s * VEC_BYTES);
+        bulk_g2s(vec, lse_g + q0, BQ * 4, bar);
+        bulk_g2s(vec + BQ, dvec_g + q0, BQ * 4, bar);
+        issued[s] = u + 1;
+      }
+      drain_wait(&ctrl->kv_full, 0);
+      for (int s = 0; s < 2; ++s)
+        if (issued[s] > 0) drain_wait(&ctrl->qd_full[s], (issued[s] - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);   // S^T = K Q^T
+      constexpr uint32_t ID_W = idesc_ab(BK, BQ, false, false);   // dW^T = V dO^T
+      constexpr uint32_t ID_DV = idesc_ab(BK, DV, false, true);   // dV += P^T dO
+      constexpr uint32_t ID_DK = idesc_ab(BK, HD, false, true);   // dK += dS^T Q
+      constexpr uint32_t ID_DQ = idesc_ab(BQ, HD, true, true);    // dQ = dS K
+      const uint32_t s_k = smem_u32(smem + OFF_K), s_v = smem_u32(smem + OFF_V);
+      const uint32_t s_ds = smem_u32(smem + OFF_DS);
+      // K-major views (rows of 64 bf16): advance 32 bytes per 16 elements.
+      const uint64_t d_k_kmaj = smem_desc_sw128(s_k, 16, 1024);
+      const uint64_t d_v_kmaj = smem_desc_sw128(s_v, 16, 1024);
+      const uint64_t d_ds_kmaj = smem_desc_sw128(s_ds, 16, 1024);
+      // MN-major views (64-wide blocks TILE64 apart): advance 2048 bytes per 16 rows.
+      const uint64_t d_k_mn = smem_desc_sw128(s_k, TILE64, 1024);
+      const uint64_t d_ds_mn = smem_desc_sw128(s_ds, TILE64, 1024);
+      // Adds a byte offset to a descriptor's start address.
+      auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+      bool ok = mbar_wait(&ctrl->kv_full, 0, abort_flag, WAIT_TIMEOUT_NS);
+      tc_fence_after_sync();
+      for (int it = 0; ok && it < n_q; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1;
+        if (!(ok = mbar_wait(&ctrl->qd_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+        tc_fence_after_sync();
+        const uint32_t s_q = smem_u32(smem + OFF_Q + s * TILE64);
+        const uint32_t s_do = smem_u32(smem + OFF_DO + s * 2 * TILE64);
+        const uint64_t d_q_kmaj = smem_desc_sw128(s_q, 16, 1024);
+        const uint64_t d_q_mn = smem_desc_sw128(s_q, TILE64, 1024);
+        const uint64_t d_do_kmaj = smem_desc_sw128(s_do, 16, 1024);
+        const uint64_t d_do_mn = smem_desc_sw128(s_do, TILE64, 1024);
+        // S^T = K Q^T (K = 64) and dW^T = V dO^T (K = 128: two 64-column boxes).
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16_ss(tmem + TM_S, adv(d_k_kmaj, 32 * kk), adv(d_q_kmaj, 32 * kk), ID_S, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * TILE64 + 32 * (kk & 3);
+          umma_bf16_ss(tmem + TM_W, adv(d_v_kmaj, off), adv(d_do_kmaj, off), ID_W, kk > 0);
+        }
+        umma_commit(&ctrl->s_full);
+        if (!(ok = mbar_wait(&ctrl->ds_ready, it & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+        tc_fence_after_sync();
+        // dV += (c P)^T dO: A = packed P^T in TMEM (queries 0-63 at columns 0-31,
+        // 64-127 at 64-95), B = dO MN-major (K = queries).
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
+          umma_bf16_ts(tmem + TM_DV, tmem + TM_S + pcol, adv(d_do_mn, 2048 * kk), ID_DV,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dK += dS^T Q: A = dS^T K-major (K = queries, two 64-query blocks),
+        // B = Q MN-major (N = 64).
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * TILE64 + 32 * (kk & 3);
+          umma_bf16_ss(tmem + TM_DK, adv(d_ds_kmaj, off), adv(d_q_mn, 2048 * kk), ID_DK,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (K = keys).
+        if (it > 0 && !(ok = mbar_wait(&ctrl->dq_free, (it - 1) & 1, abort_flag,
+                                       WAIT_TIMEOUT_NS)))
+          break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_bf16_ss(tmem + TM_DQ, adv(d_ds_mn, 2048 * kk), adv(d_k_mn, 2048 * kk), ID_DQ,
+                       kk > 0);
+        umma_commit(&ctrl->dq_full);
+        umma_commit(&ctrl->qd_empty[s]);
+      }
+      if (ok) umma_commit(&ctrl->acc_done);
+      umma_commit(&ctrl->drain);
+      drain_wait(&ctrl->drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------------------------------------------------------- P^T and dS^T
+    const int g = (warp - 4) / 4;            // query columns 64g .. 64g+63
+    const int kr = (warp % 4) * 32 + lane;   // key row = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + TM_S + 64 * g;
+    const uint32_t t_w = tmem + lane_addr + TM_W + 64 * g;
+    const uint32_t t_p = tmem + lane_addr + TM_S + 64 * g;  // packed P^T over own S columns
+    const float coef = map ? -p.lambda[h] : 1.f;
+    const float sl2 = p.scale_log2;
+    const int kpos = k0 + kr;
+    const bool key_ok = kpos < p.N;
+    uint8_t *ds_tile = smem + OFF_DS + g * TILE64;  // this group's 64 queries
+    bool ok = true;
+    for (int it = 0; it < n_q; ++it) {
+      const int s = it & 1;
+      const int q0 = (qt_first + it) * BQ;
+      ok = mbar_wait(&ctrl->s_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const float *vec = reinterpret_cast<const float *>(smem + OFF_VEC + s * VEC_BYTES);
+      const float *lse = vec + 64 * g;
+      const float *dd = vec + BQ + 64 * g;
+      // Visible iff query position >= key position (causal) and both < N.
+      const int qbase = q0 + 64 * g;
+      const int lim_causal = p.causal ? (kpos - qbase) : -1;  // column c visible iff c >= lim
+      const int lim_n = p.N - qbase;                          // and c < lim_n
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t x[32], w[32];
+        tmem_ld_x32_nowait(t_s + c0, x);
+        tmem_ld_x32_nowait(t_w + c0, w);
+        tmem_ld_wait_x32(x);
+        tmem_ld_wait_x32(w);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float2 l2 = *reinterpret_cast<const float2 *>(lse + c0 + c);
+          const float2 d2 = *reinterpret_cast<const float2 *>(dd + c0 + c);
+          const int ca = c0 + c, cb = c0 + c + 1;
+          const bool va = key_ok && ca >= lim_causal && ca < lim_n;
+          const bool vb = key_ok && cb >= lim_causal && cb < lim_n;
+          float pa = ex2_approx(fmaf(__uint_as_float(x[c]), sl2, -l2.x));
+          float pb = ex2_approx(fmaf(__uint_as_float(x[c + 1]), sl2, -l2.y));
+          pa = va ? pa * coef : 0.f;
+          pb = vb ? pb * coef : 0.f;
+          const float da = pa * (__uint_as_float(w[c]) - d2.x);
+          const float db = pb * (__uint_as_float(w[c + 1]) - d2.y);
+          pk[c / 2] = pack_bf16x2(pa, pb);
+          dk[c / 2] = pack_bf16x2(da, db);
+        }
+        // c P^T as packed bf16 over this group's own S^T columns (already read).
+        tmem_st_x16(t_p + c0 / 2, pk);
+        // dS^T row kr, queries c0 .. c0+31 of this group: four 16-byte chunks.
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 v4 = make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+          *reinterpret_cast<uint4 *>(ds_tile + sw128(kr, c0 / 8 + j)) = v4;
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->ds_ready);
+    }
+    // ---------------------------------------------------------------- dV, dK out
+    if (ok) ok = mbar_wait(&ctrl->acc_done, 0, abort_flag, WAIT_TIMEOUT_NS);
+    // Warp-uniform decision: the TMEM loads below are warp-collective.
+    ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
+    if (ok) {
+      tc_fence_after_sync();
+      // dV columns 64g .. 64g+63 (both maps add into the fp32 accumulator).
+      float *dv_row = p.dv_acc + (bh * p.N + kpos) * DV + 64 * g;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_addr + TM_DV + 64 * g + c0, v);
+        if (key_ok) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            red_add_v4(dv_row + c0 + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                       __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+        }
+      }
+      // dK columns 32g .. 32g+31, scaled by 1/sqrt(d), stored once as bf16.
+      uint32_t v[32];
+      tmem_ld_x32(tmem + lane_addr + TM_DK + 32 * g, v);
+      if (key_ok) {
+        __nv_bfloat16 *dk = (map ? p.dk2 : p.dk1) + (bh * p.N + kpos) * HD + 32 * g;
+        uint4 *dst = reinterpret_cast<uint4 *>(dk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 pkt;
+          pkt.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * p.scale,
+                              __uint_as_float(v[8 * j + 1]) * p.scale);
+          pkt.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * p.scale,
+                              __uint_as_float(v[8 * j + 3]) * p.scale);
+          pkt.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * p.scale,
+                              __uint_as_float(v[8 * j + 5]) * p.scale);
+          pkt.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * p.scale,
+                              __uint_as_float(v[8 * j + 7]) * p.scale);
+          dst[j] = pkt;
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ---------------------------------------------------------------- dQ drain
+    const int qr = (warp % 4) * 32 + lane;  // query row = TMEM lane
+    const uint32_t t_q = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16) + TM_DQ;
+    float *dq_base = p.dq_acc + (map * p.BH + bh) * static_cast<int64_t>(p.N) * HD;
+    for (int it = 0; it < n_q; ++it) {
+      bool ok = mbar_wait(&ctrl->dq_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t a[32], b[32];
+      tmem_ld_x32_nowait(t_q, a);
+      tmem_ld_x32_nowait(t_q + 32, b);
+      tmem_ld_wait_x32(a);
+      tmem_ld_wait_x32(b);
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->dq_free);
+      const int q = (qt_first + it) * BQ + qr;
+      if (q < p.N) {
+        float *row = dq_base + static_cast<int64_t>(q) * HD;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          red_add_v4(row + c, __uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
+                     __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
+          red_add_v4(row + 32 + c, __uint_as_float(b[c]) * p.scale,
+                     __uint_as_float(b[c + 1]) * p.scale, __uint_as_float(b[c + 2]) * p.scale,
+                     __uint_as_float(b[c + 3]) * p.scale);
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag && p.status != nullptr)
+    atomicExch(p.status, static_cast<int32_t>(DIFFATTN_ERR_TIMEOUT));
+}
+
+// ---------------------------------------------------------------- kernel 1
+struct PreParams {
+  int64_t BH;
+  int32_t H, N, n_pad, headnorm;
+  float eps, out_scale;  // out_scale = 1 - lambda_init
+  const float *lambda, *norm_w;
+  const __nv_bfloat16 *dy;  // [BH][N][128]
+  const float *o_n;         // [2][BH][N][128] normalised map outputs
+  __nv_bfloat16 *dout;      // [BH][N][128]
+  float *dvec;              // [2][BH][n_pad]
+  float *dlambda;           // [H], zeroed
+  float *dnorm_w;           // [H][128], zeroed
+};
+
+constexpr int PRE_WARPS = 8;
+constexpr int PRE_ROWS = 64;  // rows per block
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Block (head bh, 64-row chunk); warp w takes rows w, w + 8, ...; lane = 4 columns.
+__global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const PreParams p) {
+  __shared__ float red_w[PRE_WARPS][DV];
+  __shared__ float red_l[PRE_WARPS];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t bh = blockIdx.x;
+  const int h = static_cast<int>(bh % p.H);
+  const int c = 4 * lane;
+  const float lam = p.lambda[h];
+  float g[4] = {p.out_scale, p.out_scale, p.out_scale, p.out_scale};
+  if (p.norm_w)
+    for (int j = 0; j < 4; ++j) g[j] *= p.norm_w[h * DV + c + j];
+  float acc_w[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc_l = 0.f;
+  const int64_t plane = p.BH * static_cast<int64_t>(p.N) * DV;
+  for (int i = blockIdx.y * PRE_ROWS + warp; i < (blockIdx.y + 1) * PRE_ROWS; i += PRE_WARPS) {
+    if (i >= p.n_pad) break;
+    float d1 = 0.f, d2 = 0.f;
+    if (i < p.N) {
+      const int64_t row = (bh * p.N + i) * DV + c;
+      const uint2 yb = *reinterpret_cast<const uint2 *>(p.dy + row);
+      const float2 y01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&yb.x));
+      const float2 y23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&yb.y));
+      const float dy[4] = {y01.x, y01.y, y23.x, y23.y};
+      const float4 a = *reinterpret_cast<const float4 *>(p.o_n + row);
+      const float4 b = *reinterpret_cast<const float4 *>(p.o_n + plane + row);
+      const float o1[4] = {a.x, a.y, a.z, a.w}, o2[4] = {b.x, b.y, b.z, b.w};
+      float o[4], dout[4];
+      for (int j = 0; j < 4; ++j) o[j] = o1[j] - lam * o2[j];
+      if (p.headnorm) {
+        float ms = 0.f, t = 0.f;
+        for (int j = 0; j < 4; ++j) {
+          ms = fmaf(o[j], o[j], ms);
+          t = fmaf(dy[j] * g[j], o[j], t);
+        }
+        ms = warp_sum(ms) * (1.f / DV);
+        t = warp_sum(t);
+        const float r = rsqrtf(ms + p.eps);
+        const float r3 = r * r * r * (1.f / DV);
+        for (int j = 0; j < 4; ++j) {
+          dout[j] = r * g[j] * dy[j] - r3 * o[j] * t;
+          acc_w[j] = fmaf(dy[j] * o[j], r * p.out_scale, acc_w[j]);
+        }
+      } else {
+        for (int j = 0; j < 4; ++j) dout[j] = dy[j];
+      }
+      // dlambda uses do as computed; D_k the bf16 do the tensor cores see.
+      float l2 = 0.f;
+      __nv_bfloat162 b01 = __floats2bfloat162_rn(dout[0], dout[1]);
+      __nv_bfloat162 b23 = __floats2bfloat162_rn(dout[2], dout[3]);
+      const float2 r01 = __bfloat1622float2(b01), r23 = __bfloat1622float2(b23);
+      const float dr[4] = {r01.x, r01.y, r23.x, r23.y};
+      for (int j = 0; j < 4; ++j) {
+        l2 = fmaf(dout[j], o2[j], l2);
+        d1 = fmaf(dr[j], o1[j], d1);
+        d2 = fmaf(dr[j], o2[j], d2);
+      }
+      uint2 ob;
+      ob.x = *reinterpret_cast<uint32_t *>(&b01);
+      ob.y = *reinterpret_cast<uint32_t *>(&b23);
+      *reinterpret_cast<uint2 *>(p.dout + row) = ob;
+      acc_l -= warp_sum(l2);
+      d1 = warp_sum(d1);
+      d2 = warp_sum(d2);
+    }
+    if (lane == 0) {
+      p.dvec[bh * p.n_pad + i] = d1;
+      p.dvec[(p.BH + bh) * p.n_pad + i] = d2;
+    }
+  }
+  for (int j = 0; j < 4; ++j) red_w[warp][c + j] = acc_w[j];
+  if (lane == 0) red_l[warp] = acc_l;
+  __syncthreads();
+  if (p.headnorm && p.dnorm_w != nullptr && threadIdx.x < DV) {
+    float s = 0.f;
+    for (int w = 0; w < PRE_WARPS; ++w) s += red_w[w][threadIdx.x];
+    atomicAdd(p.dnorm_w + h * DV + threadIdx.x, s);
+  }
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < PRE_WARPS; ++w) s += red_l[w];
+    atomicAdd(p.dlambda + h, s);
+  }
+}
+
+// ---------------------------------------------------------------- kernel 3
+// fp32 accumulators -> bf16: dq_acc [2][BH][N][64] -> dq1, dq2; dv_acc -> dv.
+__global__ void diffattn_bwd_finish_kernel(const float *dq_acc, const float *dv_acc,
+                                           __nv_bfloat16 *dq1, __nv_bfloat16 *dq2,
+                                           __nv_bfloat16 *dv, int64_t n_q4, int64_t n_v4) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       i < 2 * n_q4 + n_v4; i += stride) {
+    const float *src;
+    __nv_bfloat16 *dst;
+    int64_t j;
+    if (i < n_q4) {
+      src = dq_acc; dst = dq1; j = i;
+    } else if (i < 2 * n_q4) {
+      src = dq_acc + 4 * n_q4; dst = dq2; j = i - n_q4;
+    } else {
+      src = dv_acc; dst = dv; j = i - 2 * n_q4;
+    }
+    const float4 v = reinterpret_cast<const float4 *>(src)[j];
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2 *>(dst)[j] = o;
+  }
+}
+
+}  // namespace
+
+// cuTensorMapEncodeTiled through the runtime (shared with the forward file's
+// approach: looked up once, no link against the driver library).
+using EncodeTiledFnB = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                    const cuuint32_t *, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                    CUtensorMapFloatOOBfill);
+
+static CUresult encode_map_b(CUtensorMap *map, const void *base, uint64_t inner, uint64_t n,
+                             uint64_t bh) {
+  static EncodeTiledFnB fn = [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<EncodeTiledFnB>(ptr);
+  }();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[3] = {inner, n, bh};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * n};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int64_t bwd_workspace_floats(int64_t BH, int64_t N) {
+  const int64_t n_pad = (N + BQ - 1) / BQ * BQ;
+  // dO bf16 [BH][N][128] (as floats: half), D [2][BH][n_pad], dq_acc [2][BH][N][64],
+  // dv_acc [BH][N][128]; each region rounded to 64 floats (256 bytes).
+  auto r64 = [](int64_t x) { return (x + 63) / 64 * 64; };
+  return r64(BH * N * DV / 2) + r64(2 * BH * n_pad) + r64(2 * BH * N * HD) + r64(BH * N * DV);
+}
+
+diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
+                                      const void *q2, const void *k2, const void *v,
+                                      const float *lambda, const float *norm_w,
+                                      const float *saved, const void *dy, void *dq1, void *dk1,
+                                      void *dq2, void *dk2, void *dv, float *dlambda,
+                                      float *dnorm_w, float *workspace, cudaStream_t stream) {
+  const int64_t BH = desc.B * desc.H, N = desc.N;
+  const int64_t n_qtiles = (N + BQ - 1) / BQ;
+  const int64_t n_pad = n_qtiles * BQ;
+  if (BH * n_qtiles * 2 > INT32_MAX || N > INT32_MAX / 2) return DIFFATTN_ERR_UNSUPPORTED;
+  auto r64 = [](int64_t x) { return (x + 63) / 64 * 64; };
+  float *ws = workspace;
+  __nv_bfloat16 *dout = reinterpret_cast<__nv_bfloat16 *>(ws);
+  ws += r64(BH * N * DV / 2);
+  float *dvec = ws;
+  ws += r64(2 * BH * n_pad);
+  float *dq_acc = ws;
+  ws += r64(2 * BH * N * HD);
+  float *dv_acc = ws;
+  const float *o_n = saved;
+  const float *lse = saved + 2 * BH * N * DV;
+
+  if (cudaMemsetAsync(dq_acc, 0, sizeof(float) * (2 * BH * N * HD), stream) != cudaSuccess ||
+      cudaMemsetAsync(dv_acc, 0, sizeof(float) * (BH * N * DV), stream) != cudaSuccess ||
+      cudaMemsetAsync(dlambda, 0, sizeof(float) * desc.H, stream) != cudaSuccess)
+    return DIFFATTN_ERR_CUDA;
+  if (desc.headnorm && dnorm_w != nullptr &&
+      cudaMemsetAsync(dnorm_w, 0, sizeof(float) * desc.H * DV, stream) != cudaSuccess)
+    return DIFFATTN_ERR_CUDA;
+
+  // 1. do, D_1, D_2, dlambda, dw
+  PreParams pp;
+  pp.BH = BH;
+  pp.H = static_cast<int32_t>(desc.H);
+  pp.N = static_cast<int32_t>(N);
+  pp.n_pad = static_cast<int32_t>(n_pad);
+  pp.headnorm = desc.headnorm ? 1 : 0;
+  pp.eps = desc.eps;
+  pp.out_scale = 1.0f - desc.lambda_init;
+  pp.lambda = lambda;
+  pp.norm_w = norm_w;
+  pp.dy = static_cast<const __nv_bfloat16 *>(dy);
+  pp.o_n = o_n;
+  pp.dout = dout;
+  pp.dvec = dvec;
+  pp.dlambda = dlambda;
+  pp.dnorm_w = desc.headnorm ? dnorm_w : nullptr;
+  dim3 pre_grid(static_cast<unsigned>(BH), static_cast<unsigned>((n_pad + PRE_ROWS - 1) / PRE_ROWS));
+  diffattn_bwd_pre_kernel<<<pre_grid, PRE_WARPS * 32, 0, stream>>>(pp);
+  if (cudaGetLastError() != cudaSuccess) return DIFFATTN_ERR_CUDA;
+
+  // 2. fused gradient kernel
+  CUtensorMap maps[6];
+  const void *bases[6] = {q1, k1, q2, k2, v, dout};
+  for (int i = 0; i < 6; ++i) {
+    const uint64_t inner = (i >= 4) ? DV : HD;
+    if (encode_map_b(&maps[i], bases[i], inner, static_cast<uint64_t>(N),
+                     static_cast<uint64_t>(BH)) != CUDA_SUCCESS)
+      return DIFFATTN_ERR_CUDA;
+  }
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(diffattn_bwd_bf16_sm103_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+      return DIFFATTN_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  BwdParams p;
+  p.BH = BH;
+  p.H = static_cast<int32_t>(desc.H);
+  p.N = static_cast<int32_t>(N);
+  p.n_qtiles = static_cast<int32_t>(n_qtiles);
+  p.n_ktiles = static_cast<int32_t>(n_qtiles);
+  p.causal = desc.causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
+  p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HD)));
+  p.lambda = lambda;
+  p.lse = lse;
+  p.dvec = dvec;
+  p.dk1 = static_cast<__nv_bfloat16 *>(dk1);
+  p.dk2 = static_cast<__nv_bfloat16 *>(dk2);
+  p.dq_acc = dq_acc;
+  p.dv_acc = dv_acc;
+  p.status = desc.status_dev;
+  dim3 grid(static_cast<unsigned>(BH * n_qtiles * 2));
+  diffattn_bwd_bf16_sm103_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  if (cudaGetLastError() != cudaSuccess) return DIFFATTN_ERR_CUDA;
+
+  // 3. bf16 gradients
+  const int64_t n_q4 = BH * N * HD / 4, n_v4 = BH * N * DV / 4;
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  diffattn_bwd_finish_kernel<<<4 * sms, 256, 0, stream>>>(
+      dq_acc, dv_acc, static_cast<__nv_bfloat16 *>(dq1), static_cast<__nv_bfloat16 *>(dq2),
+      static_cast<__nv_bfloat16 *>(dv), n_q4, n_v4);
+  return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+}  // namespace diffattn

@@ -141,6 +141,11 @@ struct Params {
   int32_t splits;
   int32_t split_tiles;
   float *part;
+  // Saved activations for the backward pass (kSave): each map's normalised
+  // output O_k / l_k as fp32 [2][B*H][N][128], and its log2-sum-exp
+  // m_k + log2(l_k) as fp32 [2][B*H][n_pad], n_pad = 128 * n_qtiles.
+  float *save_o;
+  float *save_lse;
 };
 
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -233,7 +238,8 @@ __device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
 
 // kPartial: split-KV partial mode (a key range per CTA, partial softmax
 // states to p.part, no epilogue); otherwise the whole forward of a query tile.
-template <bool kPartial>
+// kSave (with !kPartial): also store the activations the backward pass needs.
+template <bool kPartial, bool kSave>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     diffattn_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
                                    const __grid_constant__ CUtensorMap tm_k1,
@@ -550,6 +556,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           dst[v] = pkt;
         }
       }
+      if (kSave) {
+        // This map's normalised output row and its log2-sum-exp.
+        const float inv = xch[k * BM + r];
+        const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BM;
+        p.save_lse[(k * p.BH + bh) * n_pad + q0 + r] = m_run + __log2f(l_run);
+        const bool real = q0 + r < p.N;
+        float4 *dst = reinterpret_cast<float4 *>(
+            p.save_o + ((k * p.BH + bh) * p.N + (real ? q0 + r : 0)) * DV);
+#pragma unroll 1
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(t_o + c0, v);  // warp-collective: every lane loads, real rows store
+          if (real) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              dst[(c0 + c) / 4] = make_float4(__uint_as_float(v[c]) * inv,
+                                              __uint_as_float(v[c + 1]) * inv,
+                                              __uint_as_float(v[c + 2]) * inv,
+                                              __uint_as_float(v[c + 3]) * inv);
+          }
+        }
+      }
     }
   }
 
@@ -602,12 +630,14 @@ CUresult encode_tile_map(CUtensorMap *map, const void *base, uint64_t inner, uin
 diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
                                       const void *k1, const void *q2, const void *k2,
                                       const void *v, const float *lambda, const float *norm_w,
-                                      void *out, cudaStream_t stream, int splits, float *part) {
+                                      void *out, cudaStream_t stream, int splits, float *part,
+                                      float *save) {
   const int64_t BH = desc.B * desc.H;
   const int64_t N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
   const int64_t n_ktiles = (n_kv + BN - 1) / BN;
-  if (splits < 1 || (splits > 1 && part == nullptr)) return DIFFATTN_ERR_INVALID_ARG;
+  if (splits < 1 || (splits > 1 && part == nullptr) || (splits > 1 && save != nullptr))
+    return DIFFATTN_ERR_INVALID_ARG;
   const int64_t split_tiles = (n_ktiles + splits - 1) / splits;
   if (BH * n_qtiles * splits > INT32_MAX || N > INT32_MAX / 2 || n_kv > INT32_MAX / 2 ||
       desc.H > INT32_MAX)
@@ -628,10 +658,13 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<false>,
+    if (cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
-        cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<true>,
+        cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
@@ -658,13 +691,18 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.splits = splits;
   p.split_tiles = static_cast<int32_t>(splits > 1 ? split_tiles : n_ktiles);
   p.part = splits > 1 ? part : nullptr;
+  p.save_o = save;
+  p.save_lse = save ? save + 2 * BH * N * DV : nullptr;
 
   dim3 grid(static_cast<unsigned>(BH * n_qtiles * splits));
   if (splits > 1)
-    diffattn_fwd_bf16_sm103_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+    diffattn_fwd_bf16_sm103_kernel<true, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  else if (save != nullptr)
+    diffattn_fwd_bf16_sm103_kernel<false, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else
-    diffattn_fwd_bf16_sm103_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+    diffattn_fwd_bf16_sm103_kernel<false, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }

@@ -30,7 +30,26 @@ constexpr int kMaxSplits = 256;
 diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
                                       const void *k1, const void *q2, const void *k2,
                                       const void *v, const float *lambda, const float *norm_w,
-                                      void *out, cudaStream_t stream, int splits, float *part);
+                                      void *out, cudaStream_t stream, int splits, float *part,
+                                      float *save = nullptr);
+
+// Saved activations of diffattn_fwd_train (fp32): the two maps' normalised
+// outputs [2][B*H][N][128], then their log2-sum-exp [2][B*H][n_pad] with
+// n_pad = 128 * ceil(N / 128).
+inline int64_t saved_floats(int64_t BH, int64_t N) {
+  const int64_t n_pad = (N + kTileRows - 1) / kTileRows * kTileRows;
+  return 2 * BH * N * kValueCols + 2 * BH * n_pad;
+}
+
+// Backward pass (bwd_bf16_sm103.cu): workspace size in floats, and the launch
+// of its three kernels (preprocess, fused gradients, bf16 conversion).
+int64_t bwd_workspace_floats(int64_t BH, int64_t N);
+diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
+                                      const void *q2, const void *k2, const void *v,
+                                      const float *lambda, const float *norm_w,
+                                      const float *saved, const void *dy, void *dq1, void *dk1,
+                                      void *dq2, void *dk2, void *dv, float *dlambda,
+                                      float *dnorm_w, float *workspace, cudaStream_t stream);
 
 // Merge of the split-KV partial blocks: both maps' softmax states, then
 // o = O1/l1 - lambda O2/l2, the optional head norm and the bf16 store.

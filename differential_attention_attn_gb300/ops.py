@@ -67,6 +67,15 @@ def load(path: str = LIB_PATH):
         lib.diffattn_fwd_kv_noalloc.restype = ctypes.c_int
         lib.diffattn_fwd_kv_noalloc.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
                                                 vp, ctypes.c_int, vp]
+        lib.diffattn_train_sizes.restype = ctypes.c_int
+        lib.diffattn_train_sizes.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t),
+                                             ctypes.POINTER(ctypes.c_size_t)]
+        lib.diffattn_fwd_train.restype = ctypes.c_int
+        lib.diffattn_fwd_train.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp,
+                                           ctypes.c_size_t, vp]
+        lib.diffattn_bwd.restype = ctypes.c_int
+        lib.diffattn_bwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp, vp,
+                                     fp, fp, vp, ctypes.c_size_t, vp]
         lib.diffattn_headnorm.restype = ctypes.c_int
         lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
         lib.diffattn_lambda_init.restype = ctypes.c_double
@@ -222,6 +231,88 @@ def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_
         return st
     _check(st)
     return out
+
+
+def train_sizes(B, H, N, *, d: int = 64):
+    """`diffattn_train_sizes`: (saved-activation bytes, backward workspace bytes)."""
+    desc = make_desc(B, H, N, d, BF16, True, True, 1e-5, 0.0)
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().diffattn_train_sizes(ctypes.byref(desc), ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def _check_qkv(q1, k1, q2, k2, v):
+    if q1.dim() != 4:
+        raise ValueError("q1 must be [B, H, N, d]")
+    B, H, N, d = q1.shape
+    for name, t, shape in (("k1", k1, (B, H, N, d)), ("q2", q2, (B, H, N, d)),
+                           ("k2", k2, (B, H, N, d)), ("v", v, (B, H, N, 2 * d))):
+        if tuple(t.shape) != shape or t.dtype != q1.dtype:
+            raise ValueError(f"{name} must be {shape} {q1.dtype}")
+    return B, H, N, d
+
+
+def _cuda_contig(ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+
+
+def fwd_train(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_w=None,
+              eps: float = 1e-5, lambda_init: float = 0.0, out=None, saved=None, status=None,
+              stream=None):
+    """`diffattn_fwd_train`: the forward plus the activations the backward needs.
+
+    Returns (out, saved); `saved` is a uint8 CUDA tensor of train_sizes()[0] bytes.
+    """
+    B, H, N, d = _check_qkv(q1, k1, q2, k2, v)
+    saved_bytes, _ = train_sizes(B, H, N, d=d)
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=q1.device)
+    if saved is None:
+        saved = torch.empty(saved_bytes, dtype=torch.uint8, device=q1.device)
+    _cuda_contig([q1, k1, q2, k2, v, lam, norm_w, out, saved])
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
+                     lambda_init, status)
+    _check(load().diffattn_fwd_train(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2),
+                                     _ptr(v), _ptr(lam), _ptr(norm_w), _ptr(out), _ptr(saved),
+                                     saved.numel() * saved.element_size(),
+                                     _stream_handle(stream)))
+    return out, saved
+
+
+def bwd(q1, k1, q2, k2, v, lam, saved, dy, *, causal: bool, headnorm: bool = True,
+        norm_w=None, eps: float = 1e-5, lambda_init: float = 0.0, workspace=None, grads=None,
+        status=None, stream=None, raw_status: bool = False):
+    """`diffattn_bwd`: gradients of sum(out * dy) given fwd_train's `saved`.
+
+    Returns dict dq1, dk1, dq2, dk2 (bf16 [B, H, N, d]), dv (bf16 [B, H, N, 2d]),
+    dlam (fp32 [H]) and dw (fp32 [H, 2d], zeros without the norm).
+    """
+    B, H, N, d = _check_qkv(q1, k1, q2, k2, v)
+    _, ws_bytes = train_sizes(B, H, N, d=d)
+    dev = q1.device
+    if grads is None:
+        grads = {k: torch.empty((B, H, N, d), dtype=q1.dtype, device=dev)
+                 for k in ("dq1", "dk1", "dq2", "dk2")}
+        grads["dv"] = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=dev)
+        grads["dlam"] = torch.empty(H, dtype=torch.float32, device=dev)
+        grads["dw"] = torch.zeros((H, 2 * d), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _cuda_contig([q1, k1, q2, k2, v, lam, norm_w, saved, dy, workspace, *grads.values()])
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
+                     lambda_init, status)
+    st = load().diffattn_bwd(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
+                             _ptr(lam), _ptr(norm_w), _ptr(saved), _ptr(dy), _ptr(grads["dq1"]),
+                             _ptr(grads["dk1"]), _ptr(grads["dq2"]), _ptr(grads["dk2"]),
+                             _ptr(grads["dv"]), _ptr(grads["dlam"]), _ptr(grads["dw"]),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return grads
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

@@ -155,6 +155,63 @@ diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const v
 diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, int splits,
                                      int *splits_out, size_t *workspace_bytes);
 
+/*
+ * Training: diffattn_fwd_train saves what the backward pass needs and
+ * diffattn_bwd returns the gradients of sum(out * dy) with respect to q1, k1,
+ * q2, k2, v, lambda and the norm weight.
+ *
+ * The pages define the forward only ("Differential Transformer", section "How
+ * differential attention works"); the backward is its derivative by the
+ * chain rule: with o_k = map_k V (k = 1, 2), o = o1 - lambda o2 and, with the
+ * norm, y = o r g, r = 1/sqrt(mean(o^2) + eps), g = w (1 - lambda_init):
+ *   do = r g dy - (r^3 / 2d) o sum_c(dy g o)  (do = dy without the norm)
+ *   dw = sum_rows dy o r (1 - lambda_init);  dlambda = -sum_rows do . o2
+ *   dV = map1^T do - lambda map2^T do;  dW = do V^T
+ *   dS_1 = P_1 * (dW - do.o1),  dS_2 = -lambda P_2 * (dW - do.o2)  (per row)
+ *   dQ_k = dS_k K_k / sqrt(d),  dK_k = dS_k^T Q_k / sqrt(d)
+ *
+ * Domain: DIFFATTN_BF16, d == 64, square attention (N queries = N keys),
+ * causal or not, with or without the norm; an sm_103 device.
+ */
+
+/* Bytes of the saved-activation buffer diffattn_fwd_train fills and of the
+ * workspace diffattn_bwd needs (host-only). */
+diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_bytes,
+                                     size_t *workspace_bytes);
+
+/*
+ * diffattn_fwd_train — diffattn_fwd (same arguments, same `out`, bitwise)
+ * that also writes `saved` (caller-owned device buffer of at least
+ * saved_bytes from diffattn_train_sizes, 16-byte aligned): each map's
+ * normalised output o_k (fp32 [2][B*H][N][128]) and log2-sum-exp
+ * (fp32 [2][B*H][128 * ceil(N / 128)]).  Keep it unchanged until the
+ * matching diffattn_bwd has run.
+ */
+diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, const void *k1,
+                                   const void *q2, const void *k2, const void *v,
+                                   const float *lambda, const float *norm_w, void *out,
+                                   void *saved, size_t saved_bytes, void *stream);
+
+/*
+ * diffattn_bwd — gradients given the forward inputs, the same desc, lambda
+ * and norm_w, the `saved` buffer of diffattn_fwd_train and dy (bf16
+ * [B, H, N, 128]).  Outputs (all device, overwritten): dq1, dk1, dq2, dk2
+ * bf16 [B, H, N, 64]; dv bf16 [B, H, N, 128]; dlambda fp32 [H]; dnorm_w fp32
+ * [H, 128] (written only when headnorm = 1; may be NULL to skip it).
+ * workspace: caller-owned scratch of at least workspace_bytes from
+ * diffattn_train_sizes, 256-byte aligned (its contents on entry do not
+ * matter).  dq and dv are summed over key tiles with fp32 atomic adds, so
+ * their last bits can differ between runs; dk, dlambda order is fixed per
+ * key tile.  Errors as for diffattn_fwd; DIFFATTN_ERR_INVALID_ARG also for a
+ * missing or misaligned buffer or a short workspace.
+ */
+diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
+                             const void *q2, const void *k2, const void *v,
+                             const float *lambda, const float *norm_w, const void *saved,
+                             const void *dy, void *dq1, void *dk1, void *dq2, void *dk2,
+                             void *dv, float *dlambda, float *dnorm_w, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
 /* Size of the scratch area diffattn_fwd_kv_noalloc uses: 64 MiB. */
 #define DIFFATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

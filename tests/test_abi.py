@@ -147,3 +147,36 @@ def test_kv_validation(lib):
     assert _call_kv(lib, d, 512, 2, ws_bytes=16 * 2 * PART_FLOATS * 4 - 4) == ops.ERR_INVALID_ARG
     assert _call_kv(lib, d, 512, 2, ws=FAKE + 4) == ops.ERR_INVALID_ARG
     assert _call_kv(lib, d, 511, 1) == ops.ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------------------- training
+def test_train_sizes(lib):
+    B, H, N = 2, 3, 300
+    d = ops.make_desc(B, H, N, 64, ops.BF16, True, True, 1e-5, 0.2)
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.diffattn_train_sizes(ctypes.byref(d), ctypes.byref(a), ctypes.byref(b)) == ops.OK
+    n_pad = 384
+    assert a.value == 4 * (2 * B * H * N * 128 + 2 * B * H * n_pad)
+    assert b.value >= 4 * (B * H * N * 64 + 2 * B * H * n_pad + 2 * B * H * N * 64 + B * H * N * 128)
+    f32 = ops.make_desc(B, H, N, 8, ops.F32, True, True, 1e-5, 0.2)
+    assert lib.diffattn_train_sizes(ctypes.byref(f32), ctypes.byref(a),
+                                    ctypes.byref(b)) == ops.ERR_UNSUPPORTED
+
+
+def test_bwd_validation_before_launch(lib):
+    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, True, 1e-5, 0.2)
+    f = ctypes.c_void_p(FAKE)
+    # q1 k1 q2 k2 v | lambda norm_w saved dy | dq1 dk1 dq2 dk2 dv | dlambda dnorm_w
+    args = [f] * 5 + [f, None, f, f] + [f] * 5 + [f, None]
+    # workspace too small
+    assert lib.diffattn_bwd(ctypes.byref(d), *args, f, 16, None) == ops.ERR_INVALID_ARG
+    # workspace not 256-byte aligned
+    assert lib.diffattn_bwd(ctypes.byref(d), *args, ctypes.c_void_p(FAKE + 16), 1 << 40,
+                            None) == ops.ERR_INVALID_ARG
+    # missing dy
+    bad = list(args)
+    bad[8] = None
+    assert lib.diffattn_bwd(ctypes.byref(d), *bad, f, 1 << 40, None) == ops.ERR_INVALID_ARG
+    # fwd_train needs the saved buffer
+    assert lib.diffattn_fwd_train(ctypes.byref(d), *[f] * 5, f, None, f, None, 1 << 40,
+                                  None) == ops.ERR_INVALID_ARG
