@@ -54,8 +54,9 @@ constexpr uint32_t OFF_K = 0;                         // K_k [128 keys x 64]
 constexpr uint32_t OFF_V = OFF_K + TILE64;            // V [128 keys x 128]: two boxes
 constexpr uint32_t OFF_Q = OFF_V + 2 * TILE64;        // 2 stages of Q_k [128 x 64]
 constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE64;       // 2 stages of dO [128 x 128]
-constexpr uint32_t OFF_DS = OFF_DO + 4 * TILE64;      // dS^T [128 keys x 128 queries]
-constexpr uint32_t OFF_VEC = OFF_DS + 2 * TILE64;     // 2 stages of (lse[128], D[128])
+constexpr uint32_t OFF_DS = OFF_DO + 4 * TILE64;      // 2 buffers of dS^T [128 keys x 128 queries]
+constexpr uint32_t DS_BYTES = 2 * TILE64;
+constexpr uint32_t OFF_VEC = OFF_DS + 2 * DS_BYTES;   // 2 stages of (lse[128], D[128])
 constexpr uint32_t VEC_BYTES = 2 * BQ * 4;
 constexpr uint32_t OFF_CTRL = OFF_VEC + 2 * VEC_BYTES;
 
@@ -65,6 +66,7 @@ struct Ctrl {
   uint64_t qd_empty[2];
   uint64_t s_full;
   uint64_t ds_ready;
+  uint64_t ds_free[2];
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t acc_done;
@@ -88,7 +90,7 @@ struct BwdParams {
   float scale;       // 1 / sqrt(d)
   const float *lambda;
   const float *lse;   // [2][BH][n_pad] log2-sum-exp from the forward
-  const float *dvec;  // [2][BH][n_pad] D_k
+  const float *dvec;  // [2][BH][n_pad] c_k D_k
   __nv_bfloat16 *dk1, *dk2;  // [BH][N][64]
   float *dq_acc;             // [2][BH][N][64], zeroed
   float *dv_acc;             // [BH][N][128], zeroed
@@ -139,6 +141,78 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// TMEM loads of 16 columns without waiting, and a wait that passes the
+// registers through (so no use is scheduled before it).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait16x4(uint32_t (&a)[16], uint32_t (&b)[16],
+                                              uint32_t (&c)[16], uint32_t (&d)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
+                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]),
+                 "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
+                 "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]),
+                 "+r"(b[14]), "+r"(b[15])
+               :
+               : "memory");
+  asm volatile("" : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3]), "+r"(c[4]), "+r"(c[5]),
+                    "+r"(c[6]), "+r"(c[7]), "+r"(c[8]), "+r"(c[9]), "+r"(c[10]), "+r"(c[11]),
+                    "+r"(c[12]), "+r"(c[13]), "+r"(c[14]), "+r"(c[15]), "+r"(d[0]), "+r"(d[1]),
+                    "+r"(d[2]), "+r"(d[3]), "+r"(d[4]), "+r"(d[5]), "+r"(d[6]), "+r"(d[7]),
+                    "+r"(d[8]), "+r"(d[9]), "+r"(d[10]), "+r"(d[11]), "+r"(d[12]), "+r"(d[13]),
+                    "+r"(d[14]), "+r"(d[15]) : : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
+// One chunk of a key row: P^T = 2^(S^T log2e/sqrt(d) - lse) and
+// dS^T = P^T (c dW^T - c D); lse and c D are the tile's per-query vectors.
+// kMasked: query column c0 + i is visible iff lo <= c0 + i < hi (and the key
+// row is real); otherwise every column is visible.
+template <bool kMasked, int W>
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&x)[W], const uint32_t (&w)[W],
+                                          const float *lse, const float *cd, int c0, float sl2,
+                                          float coef, int lo, int hi, uint32_t (&pk)[W / 2],
+                                          uint32_t (&dk)[W / 2]) {
+  const float2 scale = make_float2(sl2, sl2), cc = make_float2(coef, coef);
+#pragma unroll
+  for (int c = 0; c < W; c += 4) {
+    const float4 l4 = *reinterpret_cast<const float4 *>(lse + c0 + c);
+    const float4 d4 = *reinterpret_cast<const float4 *>(cd + c0 + c);
+#pragma unroll
+    for (int h2 = 0; h2 < 4; h2 += 2) {
+      const int i = c + h2;
+      const float2 l2 = h2 ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+      const float2 d2 = h2 ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+      float2 e = __ffma2_rn(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), scale,
+                            make_float2(-l2.x, -l2.y));
+      float pa = ex2_approx(e.x), pb = ex2_approx(e.y);
+      if (kMasked) {
+        pa = (c0 + i >= lo && c0 + i < hi) ? pa : 0.f;
+        pb = (c0 + i + 1 >= lo && c0 + i + 1 < hi) ? pb : 0.f;
+      }
+      const float2 t = __ffma2_rn(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])),
+                                  cc, make_float2(-d2.x, -d2.y));
+      const float2 ds = __fmul2_rn(make_float2(pa, pb), t);
+      pk[i / 2] = pack_bf16x2(pa, pb);
+      dk[i / 2] = pack_bf16x2(ds.x, ds.y);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel 2
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     diffattn_bwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
@@ -178,6 +252,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(&ctrl->s_full, 1);
     mbar_init(&ctrl->ds_ready, 256);
+    mbar_init(&ctrl->ds_free[0], 1);
+    mbar_init(&ctrl->ds_free[1], 1);
     mbar_init(&ctrl->dq_full, 1);
     mbar_init(&ctrl->dq_free, 128);
     mbar_init(&ctrl->acc_done, 1);
@@ -244,53 +320,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // K-major views (rows of 64 bf16): advance 32 bytes per 16 elements.
       const uint64_t d_k_kmaj = smem_desc_sw128(s_k, 16, 1024);
       const uint64_t d_v_kmaj = smem_desc_sw128(s_v, 16, 1024);
-      const uint64_t d_ds_kmaj = smem_desc_sw128(s_ds, 16, 1024);
       // MN-major views (64-wide blocks TILE64 apart): advance 2048 bytes per 16 rows.
       const uint64_t d_k_mn = smem_desc_sw128(s_k, TILE64, 1024);
       const uint64_t d_ds_mn = smem_desc_sw128(s_ds, TILE64, 1024);
       // Adds a byte offset to a descriptor's start address.
       auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-      bool ok = mbar_wait(&ctrl->kv_full, 0, abort_flag, WAIT_TIMEOUT_NS);
-      tc_fence_after_sync();
-      for (int it = 0; ok && it < n_q; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1;
-        if (!(ok = mbar_wait(&ctrl->qd_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
-        tc_fence_after_sync();
-        const uint32_t s_q = smem_u32(smem + OFF_Q + s * TILE64);
-        const uint32_t s_do = smem_u32(smem + OFF_DO + s * 2 * TILE64);
-        const uint64_t d_q_kmaj = smem_desc_sw128(s_q, 16, 1024);
-        const uint64_t d_q_mn = smem_desc_sw128(s_q, TILE64, 1024);
-        const uint64_t d_do_kmaj = smem_desc_sw128(s_do, 16, 1024);
-        const uint64_t d_do_mn = smem_desc_sw128(s_do, TILE64, 1024);
-        // S^T = K Q^T (K = 64) and dW^T = V dO^T (K = 128: two 64-column boxes).
+      auto stage_desc = [&](int st, bool k_major, bool is_do) {
+        const uint32_t base = is_do ? smem_u32(smem + OFF_DO + st * 2 * TILE64)
+                                    : smem_u32(smem + OFF_Q + st * TILE64);
+        return k_major ? smem_desc_sw128(base, 16, 1024) : smem_desc_sw128(base, TILE64, 1024);
+      };
+      // S^T = K Q^T (K = 64) and dW^T = V dO^T (K = 128: two 64-column boxes) of
+      // the query tile held in stage st.
+      auto issue_s_w = [&](int st) {
+        const uint64_t d_q = stage_desc(st, true, false), d_do = stage_desc(st, true, true);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + TM_S, adv(d_k_kmaj, 32 * kk), adv(d_q_kmaj, 32 * kk), ID_S, kk > 0);
+          umma_bf16_ss(tmem + TM_S, adv(d_k_kmaj, 32 * kk), adv(d_q, 32 * kk), ID_S, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = (kk >> 2) * TILE64 + 32 * (kk & 3);
-          umma_bf16_ss(tmem + TM_W, adv(d_v_kmaj, off), adv(d_do_kmaj, off), ID_W, kk > 0);
+          umma_bf16_ss(tmem + TM_W, adv(d_v_kmaj, off), adv(d_do, off), ID_W, kk > 0);
         }
         umma_commit(&ctrl->s_full);
+      };
+      // Order per query tile i: dV_i and dK_i (A operands from TMEM), dQ_i
+      // (from shared memory), then S and dW of tile i+1.  Issuing tile i+1's S
+      // and dW before dQ_i lets its P^T / dS^T work overlap dQ_i, but measured
+      // slower: that work then shares shared-memory bandwidth with the SS MMA.
+      bool ok = mbar_wait(&ctrl->kv_full, 0, abort_flag, WAIT_TIMEOUT_NS) &&
+                mbar_wait(&ctrl->qd_full[0], 0, abort_flag, WAIT_TIMEOUT_NS);
+      tc_fence_after_sync();
+      if (ok) issue_s_w(0);
+      for (int it = 0; ok && it < n_q; ++it) {
+        const int s = it & 1;  // Q / dO stage and dS^T buffer of tile it
         if (!(ok = mbar_wait(&ctrl->ds_ready, it & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
         tc_fence_after_sync();
-        // dV += (c P)^T dO: A = packed P^T in TMEM (queries 0-63 at columns 0-31,
-        // 64-127 at 64-95), B = dO MN-major (K = queries).
+        // dV += P^T dO (c applied at the end): A = packed P^T in TMEM (queries
+        // 0-63 at columns 0-31, 64-127 at 64-95), B = dO MN-major (K = queries).
+        const uint64_t d_do_mn = stage_desc(s, false, true);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
           umma_bf16_ts(tmem + TM_DV, tmem + TM_S + pcol, adv(d_do_mn, 2048 * kk), ID_DV,
                        (it > 0 || kk > 0) ? 1u : 0u);
         }
-        // dK += dS^T Q: A = dS^T K-major (K = queries, two 64-query blocks),
-        // B = Q MN-major (N = 64).
+        // dK += dS^T Q: A = packed dS^T in TMEM over the dW^T columns (same column
+        // map as P^T), B = Q MN-major (N = 64).
+        const uint64_t d_q_mn = stage_desc(s, false, false);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * TILE64 + 32 * (kk & 3);
-          umma_bf16_ss(tmem + TM_DK, adv(d_ds_kmaj, off), adv(d_q_mn, 2048 * kk), ID_DK,
+          const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
+          umma_bf16_ts(tmem + TM_DK, tmem + TM_W + pcol, adv(d_q_mn, 2048 * kk), ID_DK,
                        (it > 0 || kk > 0) ? 1u : 0u);
         }
+        const uint64_t d_ds_m = adv(d_ds_mn, s * DS_BYTES);
         // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (K = keys).
         if (it > 0 && !(ok = mbar_wait(&ctrl->dq_free, (it - 1) & 1, abort_flag,
                                        WAIT_TIMEOUT_NS)))
@@ -298,10 +382,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          umma_bf16_ss(tmem + TM_DQ, adv(d_ds_mn, 2048 * kk), adv(d_k_mn, 2048 * kk), ID_DQ,
+          umma_bf16_ss(tmem + TM_DQ, adv(d_ds_m, 2048 * kk), adv(d_k_mn, 2048 * kk), ID_DQ,
                        kk > 0);
         umma_commit(&ctrl->dq_full);
         umma_commit(&ctrl->qd_empty[s]);
+        umma_commit(&ctrl->ds_free[s]);
+        if (it + 1 < n_q) {
+          const int s1 = (it + 1) & 1;
+          if (!(ok = mbar_wait(&ctrl->qd_full[s1], ((it + 1) >> 1) & 1, abort_flag,
+                               WAIT_TIMEOUT_NS)))
+            break;
+          tc_fence_after_sync();
+          issue_s_w(s1);  // overwrites P^T_i and dS^T_i after dV_i, dK_i (in-order)
+        }
       }
       if (ok) umma_commit(&ctrl->acc_done);
       umma_commit(&ctrl->drain);
@@ -320,55 +413,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float sl2 = p.scale_log2;
     const int kpos = k0 + kr;
     const bool key_ok = kpos < p.N;
-    uint8_t *ds_tile = smem + OFF_DS + g * TILE64;  // this group's 64 queries
+    const bool key_tile_ragged = k0 + BK > p.N;
     bool ok = true;
     for (int it = 0; it < n_q; ++it) {
       const int s = it & 1;
       const int q0 = (qt_first + it) * BQ;
       ok = mbar_wait(&ctrl->s_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
+      // dS^T buffer s was last read by the dK / dQ MMAs of tile it - 2.
+      if (ok && it >= 2)
+        ok = mbar_wait(&ctrl->ds_free[s], ((it >> 1) - 1) & 1, abort_flag, WAIT_TIMEOUT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
+      uint8_t *ds_tile = smem + OFF_DS + s * DS_BYTES + g * TILE64;  // this group's 64 queries
       const float *vec = reinterpret_cast<const float *>(smem + OFF_VEC + s * VEC_BYTES);
       const float *lse = vec + 64 * g;
-      const float *dd = vec + BQ + 64 * g;
-      // Visible iff query position >= key position (causal) and both < N.
+      const float *cd = vec + BQ + 64 * g;
+      // Column c of this group (query q0 + 64 g + c) is visible iff lo <= c < hi.
       const int qbase = q0 + 64 * g;
-      const int lim_causal = p.causal ? (kpos - qbase) : -1;  // column c visible iff c >= lim
-      const int lim_n = p.N - qbase;                          // and c < lim_n
-#pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t x[32], w[32];
-        tmem_ld_x32_nowait(t_s + c0, x);
-        tmem_ld_x32_nowait(t_w + c0, w);
-        tmem_ld_wait_x32(x);
-        tmem_ld_wait_x32(w);
-        uint32_t pk[16], dk[16];
+      const int lo = p.causal ? (kpos - qbase) : 0;
+      const int hi = key_ok ? (p.N - qbase) : 0;
+      const bool masked = key_tile_ragged || q0 + BQ > p.N || (p.causal && q0 == k0);
+      // Four 16-column chunks; the loads of chunks 2 and 3 overlap the work on
+      // chunks 0 and 1.  Chunk c writes its packed P^T over S^T columns 8c .. 8c+7
+      // and its packed dS^T over dW^T columns 8c .. 8c+7 of this group, all
+      // already read; dS^T also goes to shared memory for the dQ product.
+      uint32_t xa[16], wa[16], xb[16], wb[16];
+      auto work = [&](const uint32_t (&x)[16], const uint32_t (&w)[16], int c0) {
+        uint32_t pk[8], dk[8];
+        if (masked)
+          bwd_chunk<true, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
+        else
+          bwd_chunk<false, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
+        tmem_st8(t_p + c0 / 2, pk);
+        tmem_st8(t_w + c0 / 2, dk);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 l2 = *reinterpret_cast<const float2 *>(lse + c0 + c);
-          const float2 d2 = *reinterpret_cast<const float2 *>(dd + c0 + c);
-          const int ca = c0 + c, cb = c0 + c + 1;
-          const bool va = key_ok && ca >= lim_causal && ca < lim_n;
-          const bool vb = key_ok && cb >= lim_causal && cb < lim_n;
-          float pa = ex2_approx(fmaf(__uint_as_float(x[c]), sl2, -l2.x));
-          float pb = ex2_approx(fmaf(__uint_as_float(x[c + 1]), sl2, -l2.y));
-          pa = va ? pa * coef : 0.f;
-          pb = vb ? pb * coef : 0.f;
-          const float da = pa * (__uint_as_float(w[c]) - d2.x);
-          const float db = pb * (__uint_as_float(w[c + 1]) - d2.y);
-          pk[c / 2] = pack_bf16x2(pa, pb);
-          dk[c / 2] = pack_bf16x2(da, db);
-        }
-        // c P^T as packed bf16 over this group's own S^T columns (already read).
-        tmem_st_x16(t_p + c0 / 2, pk);
-        // dS^T row kr, queries c0 .. c0+31 of this group: four 16-byte chunks.
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
           uint4 v4 = make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
           *reinterpret_cast<uint4 *>(ds_tile + sw128(kr, c0 / 8 + j)) = v4;
         }
-      }
+      };
+      tmem_ld16(t_s, xa);
+      tmem_ld16(t_w, wa);
+      tmem_ld16(t_s + 16, xb);
+      tmem_ld16(t_w + 16, wb);
+      tmem_wait16x4(xa, wa, xb, wb);
+      work(xa, wa, 0);
+      tmem_ld16(t_s + 32, xa);
+      tmem_ld16(t_w + 32, wa);
+      work(xb, wb, 16);
+      tmem_ld16(t_s + 48, xb);
+      tmem_ld16(t_w + 48, wb);
+      tmem_wait16x4(xa, wa, xb, wb);
+      work(xa, wa, 32);
+      work(xb, wb, 48);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before_sync();
@@ -380,7 +478,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
     if (ok) {
       tc_fence_after_sync();
-      // dV columns 64g .. 64g+63 (both maps add into the fp32 accumulator).
+      // dV columns 64g .. 64g+63, times c (both maps add into the fp32 accumulator).
       float *dv_row = p.dv_acc + (bh * p.N + kpos) * DV + 64 * g;
 #pragma unroll 1
       for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -389,8 +487,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (key_ok) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4)
-            red_add_v4(dv_row + c0 + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                       __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            red_add_v4(dv_row + c0 + c, coef * __uint_as_float(v[c]),
+                       coef * __uint_as_float(v[c + 1]), coef * __uint_as_float(v[c + 2]),
+                       coef * __uint_as_float(v[c + 3]));
         }
       }
       // dK columns 32g .. 32g+31, scaled by 1/sqrt(d), stored once as bf16.
@@ -465,7 +564,7 @@ struct PreParams {
   const __nv_bfloat16 *dy;  // [BH][N][128]
   const float *o_n;         // [2][BH][N][128] normalised map outputs
   __nv_bfloat16 *dout;      // [BH][N][128]
-  float *dvec;              // [2][BH][n_pad]
+  float *dvec;              // [2][BH][n_pad] c_k D_k
   float *dlambda;           // [H], zeroed
   float *dnorm_w;           // [H][128], zeroed
 };
@@ -544,9 +643,9 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
       d1 = warp_sum(d1);
       d2 = warp_sum(d2);
     }
-    if (lane == 0) {
+    if (lane == 0) {  // c_k D_k: c_1 = 1, c_2 = -lambda
       p.dvec[bh * p.n_pad + i] = d1;
-      p.dvec[(p.BH + bh) * p.n_pad + i] = d2;
+      p.dvec[(p.BH + bh) * p.n_pad + i] = -lam * d2;
     }
   }
   for (int j = 0; j < 4; ++j) red_w[warp][c + j] = acc_w[j];
