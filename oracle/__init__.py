@@ -65,6 +65,8 @@ def _declare(lib):
                                p, p, i]
     lib.oracle_diff_map.restype = i
     lib.oracle_diff_map.argtypes = [i64, i, p, p, p, p, d, i, p]
+    lib.oracle_groupnorm.restype = i
+    lib.oracle_groupnorm.argtypes = [i64, i, i, p, p, p, d, d, p]
     lib.oracle_headnorm.restype = i
     lib.oracle_headnorm.argtypes = [i64, i, i, p, p, p, d, d, p]
     return lib
@@ -124,7 +126,7 @@ def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool,
     wv = None if w is None else _f64(w).reshape(H, 2 * d)
     out = np.zeros((B, H, N, 2 * d), dtype=np.float64)
     rc = (lib or load()).oracle_fwd(B, H, N, d, _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2),
-                                    _ptr(v), _ptr(lam), int(bool(causal)), int(bool(headnorm)),
+                                    _ptr(v), _ptr(lam), int(bool(causal)), int(headnorm),
                                     _ptr(wv), float(eps), float(lambda_init_value), _ptr(out),
                                     int(nthreads))
     if rc != 0:
@@ -150,7 +152,7 @@ def fwd_rows(q1, k1, q2, k2, v, lam, bh_idx, row_idx, *, causal: bool, headnorm:
     out = np.zeros((bh.size, 2 * d), dtype=np.float64)
     rc = (lib or load()).oracle_fwd_rows(B, H, N, d, _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2),
                                          _ptr(v), _ptr(lam), int(bool(causal)),
-                                         int(bool(headnorm)), _ptr(wv), float(eps),
+                                         int(headnorm), _ptr(wv), float(eps),
                                          float(lambda_init_value), bh.size, _ptr(bh), _ptr(ri),
                                          _ptr(out), int(nthreads))
     if rc != 0:
@@ -192,7 +194,7 @@ def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool, bh_idx=None,
         out = np.zeros((nrows, 2 * d), dtype=np.float64)
     rc = (lib or load()).oracle_fwd_kv_rows(B, H, Nq, Nkv, d, _ptr(q1), _ptr(k1), _ptr(q2),
                                             _ptr(k2), _ptr(v), _ptr(lam), int(bool(causal)),
-                                            int(bool(headnorm)), _ptr(wv), float(eps),
+                                            int(headnorm), _ptr(wv), float(eps),
                                             float(lambda_init_value), nrows, _ptr(bh),
                                             _ptr(ri), _ptr(out), int(nthreads))
     if rc != 0:
@@ -218,7 +220,7 @@ def bwd(q1, k1, q2, k2, v, lam, dy, *, causal: bool, headnorm: bool, w=None,
     g["dlam"] = np.zeros(H)
     g["dw"] = np.zeros((H, 2 * d))
     rc = (lib or load()).oracle_bwd(B, H, N, d, _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
-                                    _ptr(lam), int(bool(causal)), int(bool(headnorm)), _ptr(wv),
+                                    _ptr(lam), int(bool(causal)), int(headnorm), _ptr(wv),
                                     float(eps), float(lambda_init_value), _ptr(dy),
                                     _ptr(g["dq1"]), _ptr(g["dk1"]), _ptr(g["dq2"]),
                                     _ptr(g["dk2"]), _ptr(g["dv"]), _ptr(g["dlam"]),
@@ -252,4 +254,19 @@ def headnorm(x, h_idx, w=None, *, H: int, eps: float, lambda_init_value: float,
                                          float(lambda_init_value), _ptr(y))
     if rc != 0:
         raise RuntimeError(f"oracle_headnorm failed with code {rc}")
+    return y
+
+
+def groupnorm(x, h_idx, w=None, *, H: int, eps: float, lambda_init_value: float,
+              lib=None) -> np.ndarray:
+    """Per-head group normalisation (mean-subtracting) of rows x[R, dv], times (1 - lambda_init)."""
+    x = _f64(x)
+    R, dv = x.shape
+    hi = np.ascontiguousarray(np.asarray(h_idx, dtype=np.int64).reshape(R))
+    wv = None if w is None else _f64(w).reshape(H, dv)
+    y = np.zeros_like(x)
+    rc = (lib or load()).oracle_groupnorm(R, dv, H, _ptr(x), _ptr(hi), _ptr(wv), float(eps),
+                                          float(lambda_init_value), _ptr(y))
+    if rc != 0:
+        raise RuntimeError(f"oracle_groupnorm failed with code {rc}")
     return y

@@ -27,9 +27,11 @@
  *     top-left aligned); the same mask is applied to both maps.  With fewer
  *     queries than keys (a key/value cache), the queries are the last
  *     positions of the sequence, so the mask is aligned bottom-right.
- *   - the per-head normalisation is the RMS form over the 2d output channels
- *     of one (batch, head, token): y = o / sqrt(mean(o^2) + eps) * w[h, c],
- *     then times (1 - lambda_init).  No mean subtraction, no bias.
+ *   - the per-head normalisation (headnorm = 1) is the RMS form over the 2d
+ *     output channels of one (batch, head, token): y = o / sqrt(mean(o^2) +
+ *     eps) * w[h, c], then times (1 - lambda_init).  No mean subtraction, no
+ *     bias.  headnorm = 2 is the mean-subtracting form the page names
+ *     (GroupNorm, one group per head), also without bias.
  *   - layers are numbered from 1 (the formula uses l - 1; l = 1 gives 0.2).
  *
  * The code is deliberately plain: one query row at a time, both maps
@@ -109,6 +111,28 @@ static void diff_row(int64_t i, int64_t N, int d, const double *q1_row,
         w[j] = p1[j] - lam * p2[j];
 }
 
+/* The page's own wording for the per-head normalisation is GroupNorm with one
+ * group per head: subtract the row mean over the 2d channels, divide by the
+ * square root of the (biased) variance plus eps, multiply by the per-channel
+ * weight, then by (1 - lambda_init).  No bias (headnorm = 2). */
+static void group_norm_row(double *o, int dv, const double *w_head, double eps,
+                           double lambda_init)
+{
+    double mu = 0.0;
+    for (int c = 0; c < dv; ++c)
+        mu += o[c];
+    mu /= (double)dv;
+    double var = 0.0;
+    for (int c = 0; c < dv; ++c)
+        var += (o[c] - mu) * (o[c] - mu);
+    var /= (double)dv;
+    const double rg = 1.0 / sqrt(var + eps);
+    for (int c = 0; c < dv; ++c) {
+        const double g = w_head ? w_head[c] : 1.0;
+        o[c] = (o[c] - mu) * rg * g * (1.0 - lambda_init);
+    }
+}
+
 /* out_row = (map1 - lambda map2)[i, :] V for the query at position i with
  * vectors q1_row, q2_row against N keys, then optionally the per-head RMS
  * normalisation and the (1 - lambda_init) scale. */
@@ -128,6 +152,10 @@ static void out_row(int64_t i, int64_t N, int d, const double *q1_row,
             o[c] += wrow[j] * v[j * dv + c];
     if (!headnorm)
         return;
+    if (headnorm == 2) {
+        group_norm_row(o, dv, w_head, eps, lambda_init);
+        return;
+    }
     double ms = 0.0;
     for (int c = 0; c < dv; ++c)
         ms += o[c] * o[c];
@@ -310,6 +338,23 @@ int oracle_diff_map(int64_t N, int d, const double *q1, const double *k1,
     return 0;
 }
 
+/* Per-head group normalisation alone (the headnorm = 2 form), rows x[R, dv]
+ * of head h_idx[r]; the same steps out_row takes for it. */
+int oracle_groupnorm(int64_t R, int dv, int H, const double *x, const int64_t *h_idx,
+                     const double *w, double eps, double lambda_init, double *y)
+{
+    if (R < 0 || dv <= 0 || H <= 0)
+        return -1;
+    for (int64_t r = 0; r < R; ++r) {
+        if (h_idx[r] < 0 || h_idx[r] >= H)
+            return -1;
+        for (int c = 0; c < dv; ++c)
+            y[r * dv + c] = x[r * dv + c];
+        group_norm_row(y + r * dv, dv, w ? w + h_idx[r] * dv : NULL, eps, lambda_init);
+    }
+    return 0;
+}
+
 /* Per-head RMS normalisation alone, applied to given rows x[R, dv] of head
  * h_idx[r]: y = x / sqrt(mean(x^2) + eps) * w[h, c] * (1 - lambda_init).
  * The same steps out_row takes after the weighted value sum. */
@@ -439,8 +484,8 @@ int oracle_bwd(int B, int H, int64_t N, int d, const double *q1, const double *k
                const double *dy, double *dq1, double *dk1, double *dq2, double *dk2,
                double *dv, double *dlam, double *dw, int nthreads)
 {
-    if (B < 0 || H <= 0 || N < 0 || d <= 0)
-        return -1;
+    if (B < 0 || H <= 0 || N < 0 || d <= 0 || headnorm < 0 || headnorm > 1)
+        return -1;  /* the backward covers the RMS form (headnorm = 1) only */
     const int64_t BH = (int64_t)B * H;
     const int dv_ = 2 * d;
     const size_t nqk = (size_t)(BH * N * d), nv = (size_t)(BH * N * dv_);

@@ -402,6 +402,62 @@ def pin_bwd_identical_maps_lambda(lib):
     return err < 1e-12, f"max err {err:.3e}"
 
 
+def pin_groupnorm_is_torch_group_norm(lib):
+    """headnorm = 2 equals torch group_norm with one group over the 2d channels of each
+    (batch, head, token) and the head's weight, times (1 - lambda_init); also through the
+    standalone entry."""
+    rng, q1, k1, q2, k2, v = _rand(71, 2, 3, 10, 4)
+    lam = rng.uniform(0.1, 0.9, size=3)
+    w = rng.uniform(0.5, 1.5, size=(3, 8))
+    eps, li = 1e-3, 0.4
+    raw = oracle.fwd(q1, k1, q2, k2, v, lam, causal=True, headnorm=0, lib=lib)
+    got = oracle.fwd(q1, k1, q2, k2, v, lam, causal=True, headnorm=2, w=w, eps=eps,
+                     lambda_init_value=li, lib=lib)
+    worst = 0.0
+    for h in range(3):
+        x = torch.from_numpy(raw[:, h].reshape(-1, 8, 1).copy())
+        ref = F.group_norm(x, 1, weight=torch.from_numpy(w[h].copy()), eps=eps).numpy()
+        ref = ref.reshape(raw[:, h].shape) * (1 - li)
+        worst = max(worst, float(np.max(np.abs(got[:, h] - ref))))
+    hidx = np.tile(np.repeat(np.arange(3), 10), 2)
+    alone = oracle.groupnorm(raw.reshape(-1, 8), hidx, w, H=3, eps=eps, lambda_init_value=li,
+                             lib=lib)
+    worst = max(worst, float(np.max(np.abs(alone - got.reshape(-1, 8)))))
+    return worst < 1e-12, f"max err {worst:.3e}"
+
+
+def pin_groupnorm_shift_invariance(lib):
+    """Adding the same constant to every entry of V shifts each o channel by
+    (1 - lambda) times it (rows of map1 - lambda map2 sum to 1 - lambda), which the
+    mean-subtracting norm removes; the RMS norm does not."""
+    rng, q1, k1, q2, k2, v = _rand(72, 1, 2, 9, 4)
+    lam = np.array([0.3, 0.6])
+    w = rng.uniform(0.5, 1.5, size=(2, 8))
+    kw = dict(causal=True, w=w, eps=1e-4, lambda_init_value=0.25, lib=lib)
+    a = oracle.fwd(q1, k1, q2, k2, v, lam, headnorm=2, **kw)
+    b = oracle.fwd(q1, k1, q2, k2, v + 3.0, lam, headnorm=2, **kw)
+    r1 = oracle.fwd(q1, k1, q2, k2, v, lam, headnorm=1, **kw)
+    r2 = oracle.fwd(q1, k1, q2, k2, v + 3.0, lam, headnorm=1, **kw)
+    err = float(np.max(np.abs(a - b)))
+    rms_moves = float(np.max(np.abs(r1 - r2)))
+    return err < 1e-10 and rms_moves > 1e-3, f"group shift err {err:.3e}, rms moves {rms_moves:.3e}"
+
+
+def pin_groupnorm_closed_form(lib):
+    """With weight 1, each output row has mean 0 and mean square
+    (1 - lambda_init)^2 var / (var + eps), var = the row's variance of o."""
+    rng, q1, k1, q2, k2, v = _rand(73, 1, 2, 12, 4)
+    lam = np.array([0.5, 0.7])
+    eps, li = 1e-2, 0.3
+    raw = oracle.fwd(q1, k1, q2, k2, v, lam, causal=False, headnorm=0, lib=lib)
+    y = oracle.fwd(q1, k1, q2, k2, v, lam, causal=False, headnorm=2, eps=eps,
+                   lambda_init_value=li, lib=lib)
+    var = raw.var(axis=-1)
+    e1 = float(np.max(np.abs(y.mean(axis=-1))))
+    e2 = float(np.max(np.abs((y ** 2).mean(axis=-1) - (1 - li) ** 2 * var / (var + eps))))
+    return max(e1, e2) < 1e-13, f"mean err {e1:.3e}, ms err {e2:.3e}"
+
+
 PINS = {name[4:]: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
 
 

@@ -65,6 +65,10 @@ MUTANTS = [
     ("bwd_dw_missing_lambda_init", "dw[c] += dyi[c] * o[c] * r * (1.0 - lambda_init);",
      "dw[c] += dyi[c] * o[c] * r;"),
     ("bwd_dlambda_of_map1", "*dlam -= do_o2;", "*dlam -= do_o1;"),
+    ("groupnorm_variance_uncentred", "var += (o[c] - mu) * (o[c] - mu);", "var += o[c] * o[c];"),
+    ("groupnorm_output_uncentred", "o[c] = (o[c] - mu) * rg * g * (1.0 - lambda_init);",
+     "o[c] = o[c] * rg * g * (1.0 - lambda_init);"),
+    ("groupnorm_mean_over_d", "    mu /= (double)dv;\n", "    mu /= (double)(dv / 2);\n"),
     ("bwd_dq2_uses_k1", "dq2[i * d + c] += ds2 * k2[j * d + c] * scale;",
      "dq2[i * d + c] += ds2 * k1[j * d + c] * scale;"),
 ]
