@@ -20,6 +20,7 @@ diffattn_status check_desc(const diffattn_desc *desc) {
   if (desc->dtype != DIFFATTN_BF16 && desc->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID_ARG;
   if (!(desc->eps >= 0.f) || !std::isfinite(desc->eps) || !std::isfinite(desc->lambda_init))
     return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->headnorm < 0 || desc->headnorm > 2) return DIFFATTN_ERR_INVALID_ARG;
   // B * H * N * 2d elements must be addressable with 64-bit offsets.
   const double elems = static_cast<double>(desc->B) * static_cast<double>(desc->H) *
                        static_cast<double>(desc->N) * 2.0 * static_cast<double>(desc->d);
@@ -157,6 +158,7 @@ diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_by
   if (st != DIFFATTN_OK) return st;
   if (saved_bytes == nullptr || workspace_bytes == nullptr) return DIFFATTN_ERR_INVALID_ARG;
   if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (desc->headnorm == 2) return DIFFATTN_ERR_UNSUPPORTED;  // backward: RMS form only
   const int64_t BH = desc->B * desc->H;
   *saved_bytes = static_cast<size_t>(saved_floats(BH, desc->N)) * sizeof(float);
   *workspace_bytes = static_cast<size_t>(bwd_workspace_floats(BH, desc->N)) * sizeof(float);

@@ -239,7 +239,8 @@ __device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
 // kPartial: split-KV partial mode (a key range per CTA, partial softmax
 // states to p.part, no epilogue); otherwise the whole forward of a query tile.
 // kSave (with !kPartial): also store the activations the backward pass needs.
-template <bool kPartial, bool kSave>
+// kGroup (with !kPartial): the head norm is the mean-subtracting form.
+template <bool kPartial, bool kSave, bool kGroup>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     diffattn_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
                                    const __grid_constant__ CUtensorMap tm_k1,
@@ -536,6 +537,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (p.headnorm) {
+        if (kGroup) {  // mean-subtracting (group) form: centre the row first
+          float sm = 0.f;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sm += o[c];
+          xch[4 * BM + k * BM + r] = sm;
+          named_barrier_sync(1, 256);
+          const float mu = (xch[4 * BM + r] + xch[5 * BM + r]) * (1.f / DV);
+          ss = 0.f;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            o[c] -= mu;
+            ss = fmaf(o[c], o[c], ss);
+          }
+        }
         xch[2 * BM + k * BM + r] = ss;
         named_barrier_sync(1, 256);
         const float tot = xch[2 * BM + r] + xch[3 * BM + r];
@@ -658,14 +673,17 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto *k0 = diffattn_fwd_bf16_sm103_kernel<false, false, false>;
+    auto *k1 = diffattn_fwd_bf16_sm103_kernel<true, false, false>;
+    auto *k2 = diffattn_fwd_bf16_sm103_kernel<false, true, false>;
+    auto *k3 = diffattn_fwd_bf16_sm103_kernel<false, false, true>;
+    if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
-        cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<true, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
-        cudaFuncSetAttribute(diffattn_fwd_bf16_sm103_kernel<false, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
     attr_set[dev] = true;
@@ -680,7 +698,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.n_qtiles = static_cast<int32_t>(n_qtiles);
   p.n_ktiles = static_cast<int32_t>(n_ktiles);
   p.causal = desc.causal ? 1 : 0;
-  p.headnorm = desc.headnorm ? 1 : 0;
+  p.headnorm = desc.headnorm ? 1 : 0;  // the form is the kGroup instantiation
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   p.eps = desc.eps;
   p.out_scale = 1.0f - desc.lambda_init;
@@ -696,14 +714,17 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
 
   dim3 grid(static_cast<unsigned>(BH * n_qtiles * splits));
   if (splits > 1)
-    diffattn_fwd_bf16_sm103_kernel<true, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    diffattn_fwd_bf16_sm103_kernel<true, false, false>
+        <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else if (save != nullptr)
-    diffattn_fwd_bf16_sm103_kernel<false, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    diffattn_fwd_bf16_sm103_kernel<false, true, false>
+        <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  else if (desc.headnorm == 2)
+    diffattn_fwd_bf16_sm103_kernel<false, false, true>
+        <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else
-    diffattn_fwd_bf16_sm103_kernel<false, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    diffattn_fwd_bf16_sm103_kernel<false, false, false>
+        <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 

@@ -103,6 +103,15 @@ __global__ void __launch_bounds__(WARPS * 32) diffattn_fwd_f32_kernel(const F32P
     }
   }
   if (p.headnorm) {
+    if (p.headnorm == 2) {  // mean-subtracting form: centre the row first
+      float sm = 0.f;
+#pragma unroll
+      for (int t = 0; t < MAX_COLS_PER_LANE; ++t) sm += o[t];
+      const float mu = warp_sum(sm) / static_cast<float>(dv);
+#pragma unroll
+      for (int t = 0; t < MAX_COLS_PER_LANE; ++t)
+        if (lane + 32 * t < dv) o[t] -= mu;
+    }
     float ss = 0.f;
 #pragma unroll
     for (int t = 0; t < MAX_COLS_PER_LANE; ++t) ss += o[t] * o[t];
@@ -137,7 +146,7 @@ diffattn_status launch_fwd_f32(const diffattn_desc &desc, const float *q1, const
   p.N = static_cast<int32_t>(desc.N);
   p.d = desc.d;
   p.causal = desc.causal ? 1 : 0;
-  p.headnorm = desc.headnorm ? 1 : 0;
+  p.headnorm = desc.headnorm;
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc.d)));
   p.eps = desc.eps;
   p.out_scale = 1.0f - desc.lambda_init;

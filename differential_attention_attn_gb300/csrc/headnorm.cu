@@ -23,20 +23,31 @@ template <bool kBf16Out>
 __global__ void __launch_bounds__(WARPS * 32)
     diffattn_headnorm_kernel(const float *__restrict__ x, const float *__restrict__ w,
                              void *__restrict__ out, int64_t rows, int32_t N, int32_t H,
-                             int32_t dv, float eps, float out_scale) {
+                             int32_t dv, float eps, float out_scale, int32_t centre) {
   const int lane = threadIdx.x % 32;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * WARPS;
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * WARPS + threadIdx.x / 32; row < rows;
        row += warps_total) {
     const float *xr = x + row * dv;
     float v[MAX_PER_LANE];
-    float ss = 0.f;
+    float sm = 0.f;
 #pragma unroll
     for (int t = 0; t < MAX_PER_LANE; ++t) {
       const int c = lane + 32 * t;
       v[t] = c < dv ? __ldg(xr + c) : 0.f;
-      ss = fmaf(v[t], v[t], ss);
+      sm += v[t];
     }
+    if (centre) {  // mean-subtracting (group) form
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      const float mu = sm / static_cast<float>(dv);
+#pragma unroll
+      for (int t = 0; t < MAX_PER_LANE; ++t)
+        if (lane + 32 * t < dv) v[t] -= mu;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int t = 0; t < MAX_PER_LANE; ++t) ss = fmaf(v[t], v[t], ss);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float r = rsqrtf(ss / static_cast<float>(dv) + eps) * out_scale;
@@ -73,11 +84,11 @@ diffattn_status launch_headnorm(const diffattn_desc &desc, const float *x, const
   if (desc.dtype == DIFFATTN_BF16)
     diffattn_headnorm_kernel<true><<<blocks, WARPS * 32, 0, stream>>>(
         x, norm_w, out, rows, static_cast<int32_t>(desc.N), static_cast<int32_t>(desc.H), dv,
-        desc.eps, out_scale);
+        desc.eps, out_scale, desc.headnorm == 2 ? 1 : 0);
   else
     diffattn_headnorm_kernel<false><<<blocks, WARPS * 32, 0, stream>>>(
         x, norm_w, out, rows, static_cast<int32_t>(desc.N), static_cast<int32_t>(desc.H), dv,
-        desc.eps, out_scale);
+        desc.eps, out_scale, desc.headnorm == 2 ? 1 : 0);
   return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 

@@ -181,12 +181,24 @@ __global__ void __launch_bounds__(kCombineThreads)
   const float c1 = real ? 1.f / L1 : 0.f;
   const float c2 = real ? -lam / L2 : 0.f;
   float ov[kColsPerThread];
-  float ss = 0.f;
+  float ss = 0.f, sm = 0.f;
 #pragma unroll
   for (int c = 0; c < kColsPerThread; ++c) {
     ov[c] = fmaf(acc1[c], c1, acc2[c] * c2);
-    ss = fmaf(ov[c], ov[c], ss);
+    sm += ov[c];
   }
+  if (p.headnorm == 2) {  // mean-subtracting (group) form: centre the row first
+    ss_warp[warp][lane] = sm;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) tot += ss_warp[w][lane];
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < kColsPerThread; ++c) ov[c] -= tot * (1.f / kValueCols);
+  }
+#pragma unroll
+  for (int c = 0; c < kColsPerThread; ++c) ss = fmaf(ov[c], ov[c], ss);
   if (p.headnorm) {
     ss_warp[warp][lane] = ss;
     __syncthreads();
@@ -225,7 +237,7 @@ diffattn_status launch_splitkv_combine(const diffattn_desc &desc, int64_t n_kv, 
   p.n_qtiles = static_cast<int32_t>(n_qtiles);
   p.split_tiles = static_cast<int32_t>((n_ktiles + splits - 1) / splits);
   p.splits = splits;
-  p.headnorm = desc.headnorm ? 1 : 0;
+  p.headnorm = desc.headnorm;
   p.n_kv = n_kv;
   p.causal = desc.causal ? 1 : 0;
   p.eps = desc.eps;

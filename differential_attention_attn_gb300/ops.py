@@ -120,17 +120,18 @@ def _stream_handle(stream):
 
 def make_desc(B, H, N, d, dtype_code, causal, headnorm, eps, lambda_init_value, status=None):
     return Desc(int(B), int(H), int(N), int(d), int(dtype_code), int(bool(causal)),
-                int(bool(headnorm)), float(eps), float(lambda_init_value),
+                int(headnorm), float(eps), float(lambda_init_value),
                 None if status is None else status.data_ptr())
 
 
-def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_w=None,
+def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm_w=None,
         eps: float = 1e-5, lambda_init: float = 0.0, out=None, status=None, stream=None,
         raw_status: bool = False):
     """Differential-attention head forward through `diffattn_fwd`.
 
     q1, k1, q2, k2: [B, H, N, d]; v: [B, H, N, 2d] (all bf16 or all fp32, CUDA,
-    contiguous); lam: float32 [H]; norm_w: float32 [H, 2d] or None.  Returns
+    contiguous); lam: float32 [H]; norm_w: float32 [H, 2d] or None.  headnorm:
+    0 none, 1 (or True) RMS form, 2 mean-subtracting group form.  Returns
     `out` [B, H, N, 2d] (allocated by torch when not given).  With
     raw_status=True the status code is returned instead of raising.
     """
@@ -350,8 +351,9 @@ def fwd_kv_noalloc(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = Tru
 
 
 def headnorm(x, *, H: int, norm_w=None, eps: float = 1e-5, lambda_init: float = 0.0,
-             out_dtype=torch.bfloat16, out=None, stream=None):
-    """Per-head RMS normalisation through `diffattn_headnorm`.
+             out_dtype=torch.bfloat16, out=None, stream=None, mode: int = 1):
+    """Per-head normalisation through `diffattn_headnorm` (mode 1: RMS; mode 2:
+    mean-subtracting group form).
 
     x: float32 [B, H, N, 2d] CUDA; returns [B, H, N, 2d] in out_dtype.
     """
@@ -365,7 +367,7 @@ def headnorm(x, *, H: int, norm_w=None, eps: float = 1e-5, lambda_init: float = 
     for t in [x, out] + ([norm_w] if norm_w is not None else []):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all tensors must be contiguous CUDA tensors")
-    desc = make_desc(B, H, N, dv // 2, _DTYPE_CODE[out.dtype], False, True, eps, lambda_init)
+    desc = make_desc(B, H, N, dv // 2, _DTYPE_CODE[out.dtype], False, mode, eps, lambda_init)
     _check(load().diffattn_headnorm(ctypes.byref(desc), _ptr(x), _ptr(norm_w), _ptr(out),
                                     _stream_handle(stream)))
     return out

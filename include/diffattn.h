@@ -17,6 +17,11 @@
  *
  *   y[c] = o[c] / sqrt(mean_c(o^2) + eps) * w[h, c] * (1 - lambda_init)
  *
+ * (headnorm = 1), or, with headnorm = 2, the mean-subtracting form the page
+ * names (GroupNorm with one group per head, no bias):
+ *
+ *   y[c] = (o[c] - mean_c o) / sqrt(var_c(o) + eps) * w[h, c] * (1 - lambda_init)
+ *
  * Conventions shared by every entry point:
  *   - All tensors are caller-owned, contiguous, row-major device buffers.
  *     The library allocates no device memory, never frees a caller buffer,
@@ -66,7 +71,9 @@ typedef struct diffattn_desc {
     int32_t d;            /* width of one query/key half; V and out have 2d columns */
     int32_t dtype;        /* diffattn_dtype of q1, k1, q2, k2, v and out */
     int32_t causal;       /* 1: key j visible to query i iff j <= i; 0: all visible */
-    int32_t headnorm;     /* 1: apply RMS head norm, w and (1 - lambda_init); 0: raw o */
+    int32_t headnorm;     /* 0: raw o; 1: RMS head norm, w and (1 - lambda_init);
+                             2: mean-subtracting head norm (the page's GroupNorm, one
+                             group per head, no bias), w and (1 - lambda_init) */
     float eps;            /* RMS norm epsilon (inside the square root), >= 0 */
     float lambda_init;    /* the (1 - lambda_init) output scale uses this value */
     int32_t *status_dev;  /* optional device int32 (NULL = none).  Kernels never clear
@@ -171,7 +178,8 @@ diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, in
  *   dQ_k = dS_k K_k / sqrt(d),  dK_k = dS_k^T Q_k / sqrt(d)
  *
  * Domain: DIFFATTN_BF16, d == 64, square attention (N queries = N keys),
- * causal or not, with or without the norm; an sm_103 device.
+ * causal or not, headnorm 0 or 1 (2 is DIFFATTN_ERR_UNSUPPORTED); an sm_103
+ * device.
  */
 
 /* Bytes of the saved-activation buffer diffattn_fwd_train fills and of the
@@ -253,7 +261,8 @@ diffattn_status diffattn_fwd_kv_noalloc(const diffattn_desc *desc, int64_t n_kv,
  *
  * x is device float32 [B, H, N, 2d]; norm_w device float32 [H, 2d] or NULL;
  * out device [B, H, N, 2d] in desc->dtype (bf16 rounded to nearest even, or
- * fp32).  desc->causal and desc->headnorm are ignored.  Supported: 1 <= d <= 128.
+ * fp32).  desc->headnorm = 2 selects the mean-subtracting form, 0 or 1 the RMS
+ * form; desc->causal is ignored.  Supported: 1 <= d <= 128.
  */
 diffattn_status diffattn_headnorm(const diffattn_desc *desc, const float *x,
                                   const float *norm_w, void *out, void *stream);

@@ -180,3 +180,12 @@ def test_bwd_validation_before_launch(lib):
     # fwd_train needs the saved buffer
     assert lib.diffattn_fwd_train(ctypes.byref(d), *[f] * 5, f, None, f, None, 1 << 40,
                                   None) == ops.ERR_INVALID_ARG
+
+
+def test_headnorm_mode_validation(lib):
+    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, 3, 1e-5, 0.2)
+    assert _call(lib, d) == ops.ERR_INVALID_ARG
+    g = ops.make_desc(1, 2, 256, 64, ops.BF16, True, 2, 1e-5, 0.2)
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.diffattn_train_sizes(ctypes.byref(g), ctypes.byref(a),
+                                    ctypes.byref(b)) == ops.ERR_UNSUPPORTED

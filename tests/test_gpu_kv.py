@@ -131,3 +131,11 @@ def test_kv_rejects_short_workspace_on_device():
     sp, nbytes = ops.fwd_kv_plan(1, 2, 64, 2048, causal=True, splits=4)
     ws = torch.empty(nbytes - 16, dtype=torch.uint8, device="cuda")
     assert harness.run_gpu_kv(w, splits=4, workspace=ws, raw_status=True) == ops.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_kv_group_norm(splits):
+    """headnorm = 2 through the split-KV combine kernel and the single-pass kernel."""
+    w = W.kv_cache(495, B=1, H=3, Nq=40, Nkv=1500, causal=True)
+    w.headnorm = 2
+    _cmp(harness.run_gpu_kv(w, splits=splits), harness.run_oracle_kv(w), f"group splits={splits}")

@@ -169,3 +169,42 @@ def test_bf16_many_items_per_cta(causal):
                  random_w=True, layer=9)
     gpu = harness.run_gpu(w).double().cpu().numpy()
     _cmp_bf16(gpu, harness.run_oracle(w), f"many items causal={causal}")
+
+
+# ----------------------------------------------------------------------------- group-norm form
+@pytest.mark.parametrize("N", [7, 128, 200, 640])
+@pytest.mark.parametrize("causal", [True, False])
+def test_bf16_group_norm(N, causal):
+    """headnorm = 2 (mean-subtracting, the page's GroupNorm wording) in the fused epilogue."""
+    w = W.custom(700 + N, B=2, H=3, N=N, d=64, causal=causal, headnorm=2, random_w=True,
+                 layer=6)
+    gpu = harness.run_gpu(w).double().cpu().numpy()
+    _cmp_bf16(gpu, harness.run_oracle(w), f"group N={N} causal={causal}")
+
+
+@pytest.mark.parametrize("N,d", [(6, 8), (100, 64), (257, 128)])
+def test_f32_group_norm(N, d):
+    w = W.custom(710 + N, B=2, H=2, N=N, d=d, causal=True, headnorm=2, dtype=torch.float32,
+                 random_w=True, layer=3)
+    gpu = harness.run_gpu(w).double().cpu().numpy()
+    assert np.max(np.abs(gpu - harness.run_oracle(w))) <= 1e-5
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_group_norm_kernel(out_dtype):
+    rng = np.random.default_rng(5)
+    B, H, N, dv = 2, 3, 77, 128
+    x = (rng.standard_normal((B, H, N, dv)) + 2.0).astype(np.float32)  # non-zero mean
+    wgt = (1 + 0.1 * rng.standard_normal((H, dv))).astype(np.float32)
+    eps, li = np.float32(1e-5), np.float32(0.35)
+    y = ops.headnorm(torch.from_numpy(x).cuda(), H=H, norm_w=torch.from_numpy(wgt).cuda(),
+                     eps=float(eps), lambda_init=float(li), out_dtype=out_dtype, mode=2)
+    torch.cuda.synchronize()
+    hidx = np.tile(np.repeat(np.arange(H), N), B)
+    ref = oracle.groupnorm(x.reshape(-1, dv).astype(np.float64), hidx, wgt.astype(np.float64),
+                           H=H, eps=float(eps), lambda_init_value=float(li))
+    got = y.double().cpu().numpy().reshape(-1, dv)
+    if out_dtype == torch.float32:
+        assert np.max(np.abs(got - ref)) <= 1e-5 * max(1.0, np.max(np.abs(ref)))
+    else:
+        assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5)
