@@ -117,6 +117,30 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
                         s);
 }
 
+diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, const void *k1,
+                                     const void *q2, const void *k2, const void *v,
+                                     const float *lambda, const float *norm_w, void *out,
+                                     const diffattn_strides *strides, void *stream) {
+  diffattn_status st = check_desc(desc);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out || !strides)
+    return DIFFATTN_ERR_INVALID_ARG;
+  if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+      !aligned16(out))
+    return DIFFATTN_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i) {
+    const int64_t s3[3] = {strides[i].b, strides[i].h, strides[i].n};
+    for (int64_t x : s3)
+      if (x <= 0 || (x & 7) != 0 || x >= (int64_t{1} << 39)) return DIFFATTN_ERR_INVALID_ARG;
+  }
+  if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
+  if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
+                               static_cast<cudaStream_t>(stream), 1, nullptr, nullptr, strides);
+}
+
 diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, int splits,
                                      int *splits_out, size_t *workspace_bytes) {
   if (splits_out == nullptr || workspace_bytes == nullptr) return DIFFATTN_ERR_INVALID_ARG;

@@ -146,6 +146,8 @@ struct Params {
   // m_k + log2(l_k) as fp32 [2][B*H][n_pad], n_pad = 128 * n_qtiles.
   float *save_o;
   float *save_lse;
+  // Element strides of `out` (batch, head, row); rows of 128 are contiguous.
+  int64_t out_sb, out_sh, out_sn;
 };
 
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -264,11 +266,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // With split-KV, consecutive CTAs take consecutive key ranges of one item.
   // (The single-pass instantiation keeps the key range origin a compile-time
   // zero: a run-time origin measurably slows its loops.)
-  const int64_t item = kPartial ? blockIdx.x / p.splits : blockIdx.x;
-  const int split = kPartial ? static_cast<int>(blockIdx.x % p.splits) : 0;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(item / p.BH);
-  const int64_t bh = item % p.BH;
-  const int h = static_cast<int>(bh % p.H);
+  // The grid has fewer than 2^31 CTAs (checked at launch), so the decode uses
+  // 32-bit division: a 64-bit one is a long software sequence that every CTA
+  // would run before its first load.
+  const uint32_t BH32 = static_cast<uint32_t>(p.BH), H32 = static_cast<uint32_t>(p.H);
+  const uint32_t item32 = kPartial ? blockIdx.x / static_cast<uint32_t>(p.splits) : blockIdx.x;
+  const int64_t item = item32;
+  const int split = kPartial ? static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.splits)) : 0;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(item32 / BH32);
+  const uint32_t bh32 = item32 % BH32;
+  const int64_t bh = bh32;
+  const int h = static_cast<int>(bh32 % H32);
+  const int b_idx = static_cast<int>(bh32 / H32);
   const int q0 = qt * BM;
   const int n_all = static_cast<int>(key_tiles_seen(qt, p.N, p.N_kv, p.causal != 0));
   const int kv_lo = split * p.split_tiles;  // first key tile of this CTA
@@ -315,8 +324,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = 0;
       mbar_arrive_expect_tx(&ctrl->q_full, 2 * TILE_QK_BYTES);
-      tma_load_3d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, q0, static_cast<int32_t>(bh));
-      tma_load_3d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, q0, static_cast<int32_t>(bh));
+      tma_load_4d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, q0, h, b_idx);
+      tma_load_4d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, q0, h, b_idx);
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % STAGES;
         const uint32_t u = static_cast<uint32_t>(j / STAGES);
@@ -325,12 +334,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
         const int32_t y = (kv_lo + j) * BN;
         mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * TILE_QK_BYTES);
-        tma_load_3d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, static_cast<int32_t>(bh));
-        tma_load_3d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, static_cast<int32_t>(bh));
+        tma_load_4d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, h, b_idx);
+        tma_load_4d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, h, b_idx);
         mbar_arrive_expect_tx(&ctrl->v_full[s], TILE_V_BYTES);
-        tma_load_3d(st + STAGE_V, &tm_v, &ctrl->v_full[s], 0, y, static_cast<int32_t>(bh));
-        tma_load_3d(st + STAGE_V + TILE_QK_BYTES, &tm_v, &ctrl->v_full[s], HD, y,
-                    static_cast<int32_t>(bh));
+        tma_load_4d(st + STAGE_V, &tm_v, &ctrl->v_full[s], 0, y, h, b_idx);
+        tma_load_4d(st + STAGE_V + TILE_QK_BYTES, &tm_v, &ctrl->v_full[s], HD, y, h, b_idx);
         issued[s] = u + 1;
       }
       // Never leave with a copy in flight: wait (bounded) for every issued load.
@@ -560,7 +568,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? __ldg(w + c) : 1.f);
       }
       if (q0 + r < p.N) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (bh * p.N + q0 + r) * DV + col0);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + b_idx * p.out_sb + h * p.out_sh +
+                                               (q0 + r) * p.out_sn + col0);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           uint4 pkt;
@@ -626,18 +635,20 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
+// 4-D view {inner, rows, H, B} of a bf16 tensor with element strides (sn, sh,
+// sb) and contiguous rows; 128-row x 64-column boxes with 128-byte swizzle.
 CUresult encode_tile_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t n,
-                         uint64_t bh) {
+                         uint64_t H, uint64_t B, const diffattn_strides &st) {
   EncodeTiledFn encode = encode_tiled_fn();
   if (encode == nullptr) return CUDA_ERROR_NOT_FOUND;
-  cuuint64_t dims[3] = {inner, n, bh};
-  cuuint64_t strides[2] = {inner * 2, inner * 2 * n};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t dims[4] = {inner, n, H, B};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                           static_cast<cuuint64_t>(st.b) * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 }  // namespace
@@ -646,7 +657,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
                                       const void *k1, const void *q2, const void *k2,
                                       const void *v, const float *lambda, const float *norm_w,
                                       void *out, cudaStream_t stream, int splits, float *part,
-                                      float *save) {
+                                      float *save, const diffattn_strides *strides) {
   const int64_t BH = desc.B * desc.H;
   const int64_t N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
@@ -658,13 +669,20 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
       desc.H > INT32_MAX)
     return DIFFATTN_ERR_UNSUPPORTED;
 
+  // Element strides of q1, k1, q2, k2, v, out: given, or contiguous [B, H, rows, width].
+  diffattn_strides st[6];
+  for (int i = 0; i < 6; ++i) {
+    const int64_t width = (i >= 4) ? DV : HD;
+    const int64_t rows = (i == 0 || i == 2 || i == 5) ? N : n_kv;
+    st[i] = strides ? strides[i] : diffattn_strides{desc.H * rows * width, rows * width, width};
+  }
   CUtensorMap maps[5];
   const void *bases[5] = {q1, k1, q2, k2, v};
   for (int i = 0; i < 5; ++i) {
     const uint64_t inner = (i == 4) ? DV : HD;
     const uint64_t rows = (i == 0 || i == 2) ? N : n_kv;
-    if (encode_tile_map(&maps[i], bases[i], inner, rows, static_cast<uint64_t>(BH)) !=
-        CUDA_SUCCESS)
+    if (encode_tile_map(&maps[i], bases[i], inner, rows, static_cast<uint64_t>(desc.H),
+                        static_cast<uint64_t>(desc.B), st[i]) != CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
 
@@ -710,6 +728,9 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.split_tiles = static_cast<int32_t>(splits > 1 ? split_tiles : n_ktiles);
   p.part = splits > 1 ? part : nullptr;
   p.save_o = save;
+  p.out_sb = st[5].b;
+  p.out_sh = st[5].h;
+  p.out_sn = st[5].n;
   p.save_lse = save ? save + 2 * BH * N * DV : nullptr;
 
   dim3 grid(static_cast<unsigned>(BH * n_qtiles * splits));

@@ -31,7 +31,8 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
                                       const void *k1, const void *q2, const void *k2,
                                       const void *v, const float *lambda, const float *norm_w,
                                       void *out, cudaStream_t stream, int splits, float *part,
-                                      float *save = nullptr);
+                                      float *save = nullptr,
+                                      const diffattn_strides *strides = nullptr);
 
 // Saved activations of diffattn_fwd_train (fp32): the two maps' normalised
 // outputs [2][B*H][N][128], then their log2-sum-exp [2][B*H][n_pad] with

@@ -39,6 +39,11 @@ class Desc(ctypes.Structure):
     ]
 
 
+class Strides(ctypes.Structure):
+    """Mirror of `diffattn_strides` (element strides of batch, head, row)."""
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("n", ctypes.c_int64)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -76,6 +81,9 @@ def load(path: str = LIB_PATH):
         lib.diffattn_bwd.restype = ctypes.c_int
         lib.diffattn_bwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp, vp,
                                      fp, fp, vp, ctypes.c_size_t, vp]
+        lib.diffattn_fwd_strided.restype = ctypes.c_int
+        lib.diffattn_fwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp,
+                                             ctypes.POINTER(Strides), vp]
         lib.diffattn_headnorm.restype = ctypes.c_int
         lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
         lib.diffattn_lambda_init.restype = ctypes.c_double
@@ -161,6 +169,35 @@ def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm_w=None,
     desc = make_desc(B, H, N, d, _DTYPE_CODE[dtype], causal, headnorm, eps, lambda_init, status)
     st = load().diffattn_fwd(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
                              _ptr(lam), _ptr(norm_w), _ptr(out), _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return out
+
+
+def fwd_strided(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm_w=None,
+                eps: float = 1e-5, lambda_init: float = 0.0, out=None, status=None,
+                stream=None, raw_status: bool = False):
+    """`diffattn_fwd_strided`: the bf16 forward on [B, H, N, d]-shaped views of any
+    layout whose rows are contiguous (e.g. x.permute(0, 2, 1, 3) of [B, N, H, d]
+    storage); `out` may be such a view too (default: a contiguous tensor)."""
+    B, H, N, d = q1.shape
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=q1.device)
+    ts = [q1, k1, q2, k2, v, out]
+    shapes = [(B, H, N, d)] * 4 + [(B, H, N, 2 * d)] * 2
+    for t, shape in zip(ts, shapes):
+        if tuple(t.shape) != shape or t.dtype != q1.dtype or not t.is_cuda:
+            raise ValueError(f"expected a CUDA {q1.dtype} tensor of shape {shape}")
+        if t.stride(-1) != 1:
+            raise ValueError("rows must be contiguous (last stride 1)")
+    _cuda_contig([lam, norm_w])
+    arr = (Strides * 6)(*[Strides(t.stride(0), t.stride(1), t.stride(2)) for t in ts])
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
+                     lambda_init, status)
+    st = load().diffattn_fwd_strided(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2),
+                                     _ptr(v), _ptr(lam), _ptr(norm_w), _ptr(out), arr,
+                                     _stream_handle(stream))
     if raw_status:
         return st
     _check(st)

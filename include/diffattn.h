@@ -111,6 +111,31 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
                              const float *lambda, const float *norm_w, void *out,
                              void *stream);
 
+/* Element strides of one [B, H, rows, width] tensor whose rows (width
+ * elements) are contiguous: element (b, h, i, c) sits at b*b + h*h + i*n + c. */
+typedef struct diffattn_strides {
+    int64_t b; /* batch stride */
+    int64_t h; /* head stride */
+    int64_t n; /* row (token) stride */
+} diffattn_strides;
+
+/*
+ * diffattn_fwd_strided — diffattn_fwd with caller-given strides, so that
+ * q1, k1, q2, k2, v and out may be views of other layouts (for example
+ * [B, N, H, d] storage, strides {N*H*d, d, H*d}) without copies.  Same
+ * computation and output values as diffattn_fwd on contiguous copies.
+ *
+ * strides[0..5] are those of q1, k1, q2, k2, v, out, in elements.  Rows must
+ * be contiguous; every stride must be a positive multiple of 8 elements (16
+ * bytes, the tensor-copy engine's rule) and below 2^39.  Domain: DIFFATTN_BF16,
+ * d == 64, any N >= 1, headnorm 0, 1 or 2, 16-byte aligned bases, an sm_103
+ * device; anything else returns an error before launching.
+ */
+diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, const void *k1,
+                                     const void *q2, const void *k2, const void *v,
+                                     const float *lambda, const float *norm_w, void *out,
+                                     const diffattn_strides *strides, void *stream);
+
 /*
  * diffattn_fwd_kv — the same forward for N queries against n_kv keys, with
  * the key range optionally split across CTAs ("split-KV").

@@ -189,3 +189,19 @@ def test_headnorm_mode_validation(lib):
     a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
     assert lib.diffattn_train_sizes(ctypes.byref(g), ctypes.byref(a),
                                     ctypes.byref(b)) == ops.ERR_UNSUPPORTED
+
+
+def test_strided_validation_before_launch(lib):
+    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, 1, 1e-5, 0.2)
+    f = ctypes.c_void_p(FAKE)
+    good = [ops.Strides(2 * 256 * 64, 256 * 64, 64)] * 4 + [ops.Strides(2 * 256 * 128, 256 * 128, 128)] * 2
+    for bad in (ops.Strides(0, 64, 64), ops.Strides(8, 12, 64), ops.Strides(8, 8, 1 << 40)):
+        arr = (ops.Strides * 6)(*(good[:2] + [bad] + good[3:]))
+        assert lib.diffattn_fwd_strided(ctypes.byref(d), f, f, f, f, f, f, None, f, arr,
+                                        None) == ops.ERR_INVALID_ARG
+    assert lib.diffattn_fwd_strided(ctypes.byref(d), f, f, f, f, f, f, None, f, None,
+                                    None) == ops.ERR_INVALID_ARG
+    f32 = ops.make_desc(1, 2, 256, 64, ops.F32, True, 1, 1e-5, 0.2)
+    arr = (ops.Strides * 6)(*good)
+    assert lib.diffattn_fwd_strided(ctypes.byref(f32), f, f, f, f, f, f, None, f, arr,
+                                    None) == ops.ERR_UNSUPPORTED
