@@ -27,9 +27,9 @@
 //   3. diffattn_bwd_finish_kernel: fp32 accumulators -> bf16 gradients.
 //
 // Roles in kernel 2 (512 threads): warp 0 TMA producer; warp 1 TMEM
-// allocator and single MMA-issuing thread; warps 4-11 two warpgroups (query
-// columns 0-63 and 64-127 of the tile; thread = key row) computing P^T and
-// dS^T; warps 12-15 draining dQ (thread = query row).
+// allocator and single MMA-issuing thread; warps 4-15 three warpgroups
+// (thread = key row) sharing the P^T / dS^T work of each tile by 16-query
+// chunks, the one with fewer chunks then draining dQ (thread = query row).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -171,6 +171,14 @@ __device__ __forceinline__ void tmem_wait16x4(uint32_t (&a)[16], uint32_t (&b)[1
                     "+r"(d[8]), "+r"(d[9]), "+r"(d[10]), "+r"(d[11]), "+r"(d[12]), "+r"(d[13]),
                     "+r"(d[14]), "+r"(d[15]) : : "memory");
 }
+__device__ __forceinline__ void tmem_wait16(uint32_t (&a)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
+                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
+               :
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&ctrl->qd_empty[s], 1);
     }
     mbar_init(&ctrl->s_full, 1);
-    mbar_init(&ctrl->ds_ready, 256);
+    mbar_init(&ctrl->ds_ready, 384);
     mbar_init(&ctrl->ds_free[0], 1);
     mbar_init(&ctrl->ds_free[1], 1);
     mbar_init(&ctrl->dq_full, 1);
@@ -357,11 +365,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!(ok = mbar_wait(&ctrl->ds_ready, it & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
         tc_fence_after_sync();
         // dV += P^T dO (c applied at the end): A = packed P^T in TMEM (queries
-        // 0-63 at columns 0-31, 64-127 at 64-95), B = dO MN-major (K = queries).
+        // 16c .. 16c+15 at columns 16c .. 16c+7), B = dO MN-major (K = queries).
         const uint64_t d_do_mn = stage_desc(s, false, true);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
+          const uint32_t pcol = 16 * kk;  // chunk kk's packed columns
           umma_bf16_ts(tmem + TM_DV, tmem + TM_S + pcol, adv(d_do_mn, 2048 * kk), ID_DV,
                        (it > 0 || kk > 0) ? 1u : 0u);
         }
@@ -370,7 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t d_q_mn = stage_desc(s, false, false);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
+          const uint32_t pcol = 16 * kk;  // chunk kk's packed columns
           umma_bf16_ts(tmem + TM_DK, tmem + TM_W + pcol, adv(d_q_mn, 2048 * kk), ID_DK,
                        (it > 0 || kk > 0) ? 1u : 0u);
         }
@@ -401,19 +409,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       drain_wait(&ctrl->drain, 0);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 12) {
-    // ---------------------------------------------------------------- P^T and dS^T
-    const int g = (warp - 4) / 4;            // query columns 64g .. 64g+63
-    const int kr = (warp % 4) * 32 + lane;   // key row = TMEM lane
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- P^T, dS^T, dQ drain
+    // Three warpgroups share the eight 16-query chunks of a tile: group g takes
+    // chunks [c_lo, c_hi) = [0, 3), [3, 6), [6, 8).  Chunk c leaves its packed
+    // P^T over S^T columns 16c .. 16c+7 and its packed dS^T over dW^T columns
+    // 16c .. 16c+7 (both already read), and dS^T in shared memory for dQ.
+    // Group 2 (two chunks) then drains dQ while the next tile's S^T and dW^T run.
+    const int g = (warp - 4) / 4;
+    const int c_lo = 3 * g, c_hi = (g == 2) ? 8 : 3 * g + 3;
+    const int kr = (warp % 4) * 32 + lane;  // key row (dQ: query row) = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t t_s = tmem + lane_addr + TM_S + 64 * g;
-    const uint32_t t_w = tmem + lane_addr + TM_W + 64 * g;
-    const uint32_t t_p = tmem + lane_addr + TM_S + 64 * g;  // packed P^T over own S columns
+    const uint32_t t_s = tmem + lane_addr + TM_S;
+    const uint32_t t_w = tmem + lane_addr + TM_W;
     const float coef = map ? -p.lambda[h] : 1.f;
     const float sl2 = p.scale_log2;
     const int kpos = k0 + kr;
     const bool key_ok = kpos < p.N;
     const bool key_tile_ragged = k0 + BK > p.N;
+    float *dq_base = p.dq_acc + (map * p.BH + bh) * static_cast<int64_t>(p.N) * HD;
     bool ok = true;
     for (int it = 0; it < n_q; ++it) {
       const int s = it & 1;
@@ -425,52 +439,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      uint8_t *ds_tile = smem + OFF_DS + s * DS_BYTES + g * TILE64;  // this group's 64 queries
+      uint8_t *ds_buf = smem + OFF_DS + s * DS_BYTES;
       const float *vec = reinterpret_cast<const float *>(smem + OFF_VEC + s * VEC_BYTES);
-      const float *lse = vec + 64 * g;
-      const float *cd = vec + BQ + 64 * g;
-      // Column c of this group (query q0 + 64 g + c) is visible iff lo <= c < hi.
-      const int qbase = q0 + 64 * g;
-      const int lo = p.causal ? (kpos - qbase) : 0;
-      const int hi = key_ok ? (p.N - qbase) : 0;
+      const float *lse = vec;
+      const float *cd = vec + BQ;
+      // Query column c of the tile (query q0 + c) is visible iff lo <= c < hi.
+      const int lo = p.causal ? (kpos - q0) : 0;
+      const int hi = key_ok ? (p.N - q0) : 0;
       const bool masked = key_tile_ragged || q0 + BQ > p.N || (p.causal && q0 == k0);
-      // Four 16-column chunks; the loads of chunks 2 and 3 overlap the work on
-      // chunks 0 and 1.  Chunk c writes its packed P^T over S^T columns 8c .. 8c+7
-      // and its packed dS^T over dW^T columns 8c .. 8c+7 of this group, all
-      // already read; dS^T also goes to shared memory for the dQ product.
-      uint32_t xa[16], wa[16], xb[16], wb[16];
-      auto work = [&](const uint32_t (&x)[16], const uint32_t (&w)[16], int c0) {
+      auto work = [&](const uint32_t (&x)[16], const uint32_t (&w)[16], int c) {
+        const int c0 = 16 * c;
         uint32_t pk[8], dk[8];
         if (masked)
           bwd_chunk<true, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
         else
           bwd_chunk<false, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
-        tmem_st8(t_p + c0 / 2, pk);
-        tmem_st8(t_w + c0 / 2, dk);
+        tmem_st8(t_s + c0, pk);
+        tmem_st8(t_w + c0, dk);
+        uint8_t *sub = ds_buf + (c >> 2) * TILE64;  // 64-query half of the dS^T tile
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint4 v4 = make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
-          *reinterpret_cast<uint4 *>(ds_tile + sw128(kr, c0 / 8 + j)) = v4;
+          *reinterpret_cast<uint4 *>(sub + sw128(kr, (c & 3) * 2 + j)) = v4;
         }
       };
-      tmem_ld16(t_s, xa);
-      tmem_ld16(t_w, wa);
-      tmem_ld16(t_s + 16, xb);
-      tmem_ld16(t_w + 16, wb);
+      // Loads of the third chunk overlap the work on the second.
+      uint32_t xa[16], wa[16], xb[16], wb[16];
+      tmem_ld16(t_s + 16 * c_lo, xa);
+      tmem_ld16(t_w + 16 * c_lo, wa);
+      tmem_ld16(t_s + 16 * (c_lo + 1), xb);
+      tmem_ld16(t_w + 16 * (c_lo + 1), wb);
       tmem_wait16x4(xa, wa, xb, wb);
-      work(xa, wa, 0);
-      tmem_ld16(t_s + 32, xa);
-      tmem_ld16(t_w + 32, wa);
-      work(xb, wb, 16);
-      tmem_ld16(t_s + 48, xb);
-      tmem_ld16(t_w + 48, wb);
-      tmem_wait16x4(xa, wa, xb, wb);
-      work(xa, wa, 32);
-      work(xb, wb, 48);
+      work(xa, wa, c_lo);
+      const bool third = c_lo + 2 < c_hi;  // uniform per warp
+      if (third) {
+        tmem_ld16(t_s + 16 * (c_lo + 2), xa);
+        tmem_ld16(t_w + 16 * (c_lo + 2), wa);
+      }
+      work(xb, wb, c_lo + 1);
+      if (third) {
+        tmem_wait16x4(xa, wa, xb, wb);
+        work(xa, wa, c_lo + 2);
+      }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(&ctrl->ds_ready);
+      if (g == 2) {
+        // dQ of this tile into the fp32 accumulator, by the group with the
+        // fewest chunks, while the next tile's S^T and dW^T run.
+        ok = mbar_wait(&ctrl->dq_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        uint32_t a[32], b[32];
+        tmem_ld_x32_nowait(tmem + lane_addr + TM_DQ, a);
+        tmem_ld_x32_nowait(tmem + lane_addr + TM_DQ + 32, b);
+        tmem_ld_wait_x32(a);
+        tmem_ld_wait_x32(b);
+        tc_fence_before_sync();
+        mbar_arrive(&ctrl->dq_free);
+        const int q = q0 + kr;
+        if (q < p.N) {
+          float *row = dq_base + static_cast<int64_t>(q) * HD;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            red_add_v4(row + c, __uint_as_float(a[c]) * p.scale,
+                       __uint_as_float(a[c + 1]) * p.scale, __uint_as_float(a[c + 2]) * p.scale,
+                       __uint_as_float(a[c + 3]) * p.scale);
+            red_add_v4(row + 32 + c, __uint_as_float(b[c]) * p.scale,
+                       __uint_as_float(b[c + 1]) * p.scale, __uint_as_float(b[c + 2]) * p.scale,
+                       __uint_as_float(b[c + 3]) * p.scale);
+          }
+        }
+      }
     }
     // ---------------------------------------------------------------- dV, dK out
     if (ok) ok = mbar_wait(&ctrl->acc_done, 0, abort_flag, WAIT_TIMEOUT_NS);
@@ -478,68 +520,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
     if (ok) {
       tc_fence_after_sync();
-      // dV columns 64g .. 64g+63, times c (both maps add into the fp32 accumulator).
-      float *dv_row = p.dv_acc + (bh * p.N + kpos) * DV + 64 * g;
+      // dV columns of this group's chunks, times c (both maps add into the
+      // fp32 accumulator).
+      float *dv_row = p.dv_acc + (bh * p.N + kpos) * DV;
 #pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_addr + TM_DV + 64 * g + c0, v);
+      for (int c = c_lo; c < c_hi; ++c) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_addr + TM_DV + 16 * c, v);
+        tmem_wait16(v);
         if (key_ok) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            red_add_v4(dv_row + c0 + c, coef * __uint_as_float(v[c]),
-                       coef * __uint_as_float(v[c + 1]), coef * __uint_as_float(v[c + 2]),
-                       coef * __uint_as_float(v[c + 3]));
+          for (int j = 0; j < 16; j += 4)
+            red_add_v4(dv_row + 16 * c + j, coef * __uint_as_float(v[j]),
+                       coef * __uint_as_float(v[j + 1]), coef * __uint_as_float(v[j + 2]),
+                       coef * __uint_as_float(v[j + 3]));
         }
       }
-      // dK columns 32g .. 32g+31, scaled by 1/sqrt(d), stored once as bf16.
-      uint32_t v[32];
-      tmem_ld_x32(tmem + lane_addr + TM_DK + 32 * g, v);
-      if (key_ok) {
-        __nv_bfloat16 *dk = (map ? p.dk2 : p.dk1) + (bh * p.N + kpos) * HD + 32 * g;
-        uint4 *dst = reinterpret_cast<uint4 *>(dk);
+      // dK 16-column chunks g and g + 3, scaled by 1/sqrt(d), stored once as bf16.
+#pragma unroll 1
+      for (int c = g; c < HD / 16; c += 3) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_addr + TM_DK + 16 * c, v);
+        tmem_wait16(v);
+        if (key_ok) {
+          uint4 *dst = reinterpret_cast<uint4 *>((map ? p.dk2 : p.dk1) + (bh * p.N + kpos) * HD +
+                                                 16 * c);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint4 pkt;
-          pkt.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * p.scale,
-                              __uint_as_float(v[8 * j + 1]) * p.scale);
-          pkt.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * p.scale,
-                              __uint_as_float(v[8 * j + 3]) * p.scale);
-          pkt.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * p.scale,
-                              __uint_as_float(v[8 * j + 5]) * p.scale);
-          pkt.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * p.scale,
-                              __uint_as_float(v[8 * j + 7]) * p.scale);
-          dst[j] = pkt;
-        }
-      }
-    }
-  } else if (warp >= 12) {
-    // ---------------------------------------------------------------- dQ drain
-    const int qr = (warp % 4) * 32 + lane;  // query row = TMEM lane
-    const uint32_t t_q = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16) + TM_DQ;
-    float *dq_base = p.dq_acc + (map * p.BH + bh) * static_cast<int64_t>(p.N) * HD;
-    for (int it = 0; it < n_q; ++it) {
-      bool ok = mbar_wait(&ctrl->dq_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
-      uint32_t a[32], b[32];
-      tmem_ld_x32_nowait(t_q, a);
-      tmem_ld_x32_nowait(t_q + 32, b);
-      tmem_ld_wait_x32(a);
-      tmem_ld_wait_x32(b);
-      tc_fence_before_sync();
-      mbar_arrive(&ctrl->dq_free);
-      const int q = (qt_first + it) * BQ + qr;
-      if (q < p.N) {
-        float *row = dq_base + static_cast<int64_t>(q) * HD;
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          red_add_v4(row + c, __uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
-                     __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
-          red_add_v4(row + 32 + c, __uint_as_float(b[c]) * p.scale,
-                     __uint_as_float(b[c + 1]) * p.scale, __uint_as_float(b[c + 2]) * p.scale,
-                     __uint_as_float(b[c + 3]) * p.scale);
+          for (int j = 0; j < 2; ++j) {
+            uint4 pkt;
+            pkt.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * p.scale,
+                                __uint_as_float(v[8 * j + 1]) * p.scale);
+            pkt.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * p.scale,
+                                __uint_as_float(v[8 * j + 3]) * p.scale);
+            pkt.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * p.scale,
+                                __uint_as_float(v[8 * j + 5]) * p.scale);
+            pkt.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * p.scale,
+                                __uint_as_float(v[8 * j + 7]) * p.scale);
+            dst[j] = pkt;
+          }
         }
       }
     }
