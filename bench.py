@@ -8,6 +8,8 @@ B=2, H=16, N=4096, d=64 (value width 128).  Prints one JSON line.
                   [--workload needle_4k|small_causal|mid_causal|long_16k|decode_16k]
 
 --workload picks another measured shape (default needle_4k, the headline).
+wide_4k is the forward with query/key halves of width d = 128 (B=2, H=8,
+N=4096, causal; value width 256).
 needle_4k_bwd times the backward pass (diffattn_bwd given the saved
 activations of diffattn_fwd_train) on the needle_4k shape, at 20*d
 algorithmic flops per visible pair.
@@ -569,7 +571,11 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     ops.load()
 
-    w = W.make(WORKLOAD, seed_offset=rank)
+    if WORKLOAD == "wide_4k":  # d = 128 per half (value width 256)
+        w = W.custom(3000 + rank, B=2, H=8, N=4096, d=128, causal=True, headnorm=True,
+                     random_w=True, layer=12)
+    else:
+        w = W.make(WORKLOAD, seed_offset=rank)
     B, H, N, d = w.B, w.H, w.N, w.d
     li = float(np.float32(w.lambda_init_override if w.layer is None
                           else ops.lambda_init(w.layer)))
@@ -673,11 +679,12 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
                      "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS bf16 GEMM)",
-                     "kernel": "diffattn_fwd_bf16_sm103_kernel",
+                     "kernel": ("diffattn_fwd_d128_sm103_kernel" if d == 128
+                                else "diffattn_fwd_bf16_sm103_kernel"),
                      "alg_flops_per_launch": flops_step,
                      "alg_bytes_per_launch": alg_bytes(B, H, N, d),
                      "achieved_gbs": alg_bytes(B, H, N, d) / (launch_ms * 1e-3) / 1e9,
-                     "traffic": read_traffic(WORKLOAD)},
+                     "traffic": read_traffic(WORKLOAD) if d == 64 else None},
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
                 "d2h_bytes_per_step": int(host_out.numel() * host_out.element_size())},
@@ -701,7 +708,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["needle_4k", "small_causal", "mid_causal", "long_16k", *DECODE,
-                             "needle_4k_bwd"])
+                             "needle_4k_bwd", "wide_4k"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":

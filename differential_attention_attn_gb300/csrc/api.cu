@@ -102,11 +102,13 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
   if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out) return DIFFATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (desc->dtype == DIFFATTN_BF16) {
-    if (desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+    if (desc->d != 64 && desc->d != 128) return DIFFATTN_ERR_UNSUPPORTED;
     if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
         !aligned16(out))
       return DIFFATTN_ERR_INVALID_ARG;
     if ((st = check_sm103()) != DIFFATTN_OK) return st;
+    if (desc->d == 128)
+      return launch_fwd_d128_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w, out, s);
     return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out, s, 1,
                                  nullptr);
   }

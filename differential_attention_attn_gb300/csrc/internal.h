@@ -72,6 +72,13 @@ __host__ __device__ inline int64_t key_tiles_seen(int64_t qt, int64_t N, int64_t
 // The split count the library picks when the caller asks for 0 (splitkv.cu).
 int auto_splits(int64_t BH, int64_t N, int64_t n_kv, bool causal, int sm_count);
 
+// Fused bf16 forward for d = 128 (value width 256): two passes per query tile
+// (statistics, then one normalised accumulator); contiguous [B, H, N, width].
+diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
+                                      const void *q2, const void *k2, const void *v,
+                                      const float *lambda, const float *norm_w, void *out,
+                                      cudaStream_t stream);
+
 // fp32 forward on CUDA cores (d <= 128, N <= 4096).
 diffattn_status launch_fwd_f32(const diffattn_desc &desc, const float *q1, const float *k1,
                                const float *q2, const float *k2, const float *v,

@@ -98,10 +98,12 @@ typedef struct diffattn_desc {
  * cudaStream_t or NULL.
  *
  * Supported domain (anything else is DIFFATTN_ERR_UNSUPPORTED):
- *   - DIFFATTN_BF16: d == 64 (2d = 128); any N >= 1 (a ragged last tile is
- *     masked); B * H * ceil(N / 128) <= 2^31 - 1.  q1, k1, q2, k2, v must be
- *     16-byte aligned (DIFFATTN_ERR_INVALID_ARG otherwise).  Runs the fused
- *     tcgen05/TMEM/TMA kernel; needs an sm_103 device.
+ *   - DIFFATTN_BF16: d == 64 (2d = 128) or d == 128 (2d = 256); any N >= 1
+ *     (a ragged last tile is masked); B * H * ceil(N / 128) <= 2^31 - 1.  q1,
+ *     k1, q2, k2, v must be 16-byte aligned (DIFFATTN_ERR_INVALID_ARG
+ *     otherwise).  Runs a fused tcgen05/TMEM/TMA kernel (for d == 128 a
+ *     two-pass one: row statistics, then a single normalised accumulator);
+ *     needs an sm_103 device.  The other entry points take d == 64 only.
  *   - DIFFATTN_F32: 1 <= d <= 128, N <= 4096.  Plain CUDA-core kernel
  *     (accurate expf, fp32 accumulation).
  * B * H * N == 0 returns DIFFATTN_OK without launching anything.
