@@ -9,25 +9,30 @@
 // columns) would fill tensor memory, so this kernel makes two passes over the
 // keys of a 128-row query tile and keeps a single accumulator:
 //
-//   pass 1, per 64-key tile:  S1 = Q1 K1^T, S2 = Q2 K2^T  (tcgen05, K = 128)
+//   pass 1, per 128-key tile:  S1 = Q1 K1^T, S2 = Q2 K2^T  (tcgen05, K = 128)
 //            exact online row maxima m_k and sums l_k of 2^(S_k log2e/sqrt(d))
-//   pass 2, per 64-key tile:  S1, S2 again;
+//   pass 2, per 128-key tile:  S1, S2 again;
 //            P = 2^(x1 - m1) / l1 - lambda 2^(x2 - m2) / l2   (final weights)
-//            O += P V   (one TS MMA, N = 256, P read from TMEM)
+//            O += P V   (one TS MMA per 16 keys, N = 256, P read from TMEM)
 //
 // Each map is an ordinary softmax, so after pass 1 the normalisers are final
 // and pass 2 needs no rescaling: O is the raw output o directly.  The price is
-// the second S and the second set of exponentials.
+// the second S and the second set of exponentials.  Tiles are 128 keys wide
+// because an MMA with N = 64 takes nearly as long to issue as one with N = 128.
 //
-// Tensor memory (512 columns): S1 double-buffered at 0 and 64, S2 at 128 and
-// 192 (64 fp32 columns each), O at 256-511.  P of tile j is written as packed
-// bf16 over the S1 buffer of tile j (keys 0-31 at its columns 0-15, keys 32-63
-// at 32-47, each over columns its writers have already read).
+// Tensor memory (512 columns) changes layout between the passes:
+//   pass 1: S1 / S2 double-buffered, buffer b at 256 b (S1) and 256 b + 128 (S2)
+//   pass 2: S1 at 0, S2 at 128 (single), O at 256-511
+// P of a pass-2 tile is written as packed bf16 over S1 (keys 0-63 at columns
+// 0-31, keys 64-127 at 64-95, each over columns its writers have just read).
+// Shared memory holds Q1, Q2 (64 KB) and two 64 KB halves: in pass 1 each
+// half is a stage of K1, K2; in pass 2 half 0 holds K1, K2 and half 1 holds V,
+// each released as soon as its MMA has read it.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
 // MMA issuer, warps 4-7 and 8-11 two warpgroups (thread = query row = TMEM
 // lane).  Pass 1: group g keeps the statistics of map g + 1.  Pass 2: group g
-// forms P for keys 32g .. 32g+31 of both maps.  Epilogue: group g normalises
+// forms P for keys 64g .. 64g+63 of both maps.  Epilogue: group g normalises
 // and stores output columns 128g .. 128g+127.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -43,27 +48,22 @@ namespace diffattn {
 namespace {
 
 constexpr int BM = 128;   // query rows per tile
-constexpr int BN = 64;    // keys per key tile
+constexpr int BN = 128;   // keys per key tile
 constexpr int HD = 128;   // query/key half width d
 constexpr int DV = 256;   // value width 2d
 constexpr int NUM_THREADS = 384;
-constexpr int STAGES = 2;
 
-constexpr uint32_t BOX_Q = BM * 64 * 2;  // [128 rows x 64 columns] bf16: 16 KB
-constexpr uint32_t BOX_K = BN * 64 * 2;  // [64 rows x 64 columns] bf16: 8 KB
-constexpr uint32_t OFF_Q1 = 0;           // two 64-column boxes
-constexpr uint32_t OFF_Q2 = 2 * BOX_Q;
-constexpr uint32_t OFF_ST = 4 * BOX_Q;
-constexpr uint32_t ST_K1 = 0;            // two boxes
-constexpr uint32_t ST_K2 = 2 * BOX_K;    // two boxes
-constexpr uint32_t ST_V = 4 * BOX_K;     // four boxes (256 value columns)
-constexpr uint32_t STAGE_BYTES = 8 * BOX_K;
-constexpr uint32_t OFF_CTRL = OFF_ST + STAGES * STAGE_BYTES;
+constexpr uint32_t BOX = 128 * 64 * 2;   // one [128 rows x 64 columns] bf16 box: 16 KB
+constexpr uint32_t OFF_Q1 = 0;           // two boxes
+constexpr uint32_t OFF_Q2 = 2 * BOX;
+constexpr uint32_t OFF_HALF = 4 * BOX;   // two halves of HALF_BYTES
+constexpr uint32_t HALF_BYTES = 4 * BOX; // K1 + K2 (two boxes each), or V (four boxes)
+constexpr uint32_t OFF_CTRL = OFF_HALF + 2 * HALF_BYTES;
 
 struct Ctrl {
   uint64_t q_full;
-  uint64_t kv_full[STAGES];
-  uint64_t kv_empty[STAGES];
+  uint64_t kv_full[2];   // per shared-memory half
+  uint64_t kv_empty[2];
   uint64_t s_full[2];
   uint64_t s_done[2];
   uint64_t o_done;
@@ -77,8 +77,10 @@ constexpr uint32_t SMEM_BYTES = OFF_CTRL + sizeof(Ctrl) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(SMEM_BYTES + 1024 < (1u << 18), "descriptor start addresses must stay below 256 KB");
 
-__host__ __device__ constexpr uint32_t tm_s1(int b) { return 64u * b; }
-__host__ __device__ constexpr uint32_t tm_s2(int b) { return 128u + 64u * b; }
+// S_k (k = 0, 1) of tile t: pass 1 double-buffers, pass 2 has one buffer at 0.
+__host__ __device__ constexpr uint32_t tm_s(int k, bool pass2, int t) {
+  return (pass2 ? 0u : 256u * static_cast<uint32_t>(t & 1)) + 128u * static_cast<uint32_t>(k);
+}
 constexpr uint32_t TM_O = 256;
 
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
@@ -132,9 +134,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&ctrl->kv_full[s], 1);
-      mbar_init(&ctrl->kv_empty[s], 1);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(&ctrl->kv_full[hf], 1);
+      mbar_init(&ctrl->kv_empty[hf], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctrl->s_full[b], 1);
@@ -163,35 +165,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
+    // Shared-memory half hf is filled once per use: pass-1 tile t uses half
+    // t & 1 (K1, K2); a pass-2 tile uses half 0 (K1, K2) and half 1 (V).
     if (lane == 0) {
-      uint32_t issued[STAGES] = {0, 0};
-      mbar_arrive_expect_tx(&ctrl->q_full, 4 * BOX_Q);
+      uint32_t uses[2] = {0, 0};
+      mbar_arrive_expect_tx(&ctrl->q_full, 4 * BOX);
       for (int c = 0; c < 2; ++c) {
-        tma_load_4d(smem + OFF_Q1 + c * BOX_Q, &tm_q1, &ctrl->q_full, 64 * c, q0, h, b_idx);
-        tma_load_4d(smem + OFF_Q2 + c * BOX_Q, &tm_q2, &ctrl->q_full, 64 * c, q0, h, b_idx);
+        tma_load_4d(smem + OFF_Q1 + c * BOX, &tm_q1, &ctrl->q_full, 64 * c, q0, h, b_idx);
+        tma_load_4d(smem + OFF_Q2 + c * BOX, &tm_q2, &ctrl->q_full, 64 * c, q0, h, b_idx);
       }
-      for (int t = 0; t < T; ++t) {
-        const int s = t & 1;
-        const uint32_t u = static_cast<uint32_t>(t >> 1);
-        if (u > 0 && !mbar_wait(&ctrl->kv_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
-          break;
+      auto acquire = [&](int hf) {  // wait until half hf is free, then arm its barrier
+        if (uses[hf] > 0 && !mbar_wait(&ctrl->kv_empty[hf], (uses[hf] - 1) & 1, abort_flag,
+                                       WAIT_TIMEOUT_NS))
+          return false;
+        mbar_arrive_expect_tx(&ctrl->kv_full[hf], HALF_BYTES);
+        ++uses[hf];
+        return true;
+      };
+      bool ok = true;
+      for (int t = 0; ok && t < T; ++t) {
         const bool pass2 = t >= n_kv;
         const int y = (pass2 ? t - n_kv : t) * BN;
-        uint8_t *st = smem + OFF_ST + s * STAGE_BYTES;
-        uint64_t *bar = &ctrl->kv_full[s];
-        mbar_arrive_expect_tx(bar, (pass2 ? 8 : 4) * BOX_K);
+        const int hk = pass2 ? 0 : (t & 1);
+        if (!(ok = acquire(hk))) break;
+        uint8_t *st = smem + OFF_HALF + hk * HALF_BYTES;
         for (int c = 0; c < 2; ++c) {
-          tma_load_4d(st + ST_K1 + c * BOX_K, &tm_k1, bar, 64 * c, y, h, b_idx);
-          tma_load_4d(st + ST_K2 + c * BOX_K, &tm_k2, bar, 64 * c, y, h, b_idx);
+          tma_load_4d(st + c * BOX, &tm_k1, &ctrl->kv_full[hk], 64 * c, y, h, b_idx);
+          tma_load_4d(st + (2 + c) * BOX, &tm_k2, &ctrl->kv_full[hk], 64 * c, y, h, b_idx);
         }
-        if (pass2)
+        if (pass2) {
+          if (!(ok = acquire(1))) break;
+          uint8_t *sv = smem + OFF_HALF + HALF_BYTES;
           for (int c = 0; c < 4; ++c)
-            tma_load_4d(st + ST_V + c * BOX_K, &tm_v, bar, 64 * c, y, h, b_idx);
-        issued[s] = u + 1;
+            tma_load_4d(sv + c * BOX, &tm_v, &ctrl->kv_full[1], 64 * c, y, h, b_idx);
+        }
       }
       drain_wait(&ctrl->q_full, 0);
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s] > 0) drain_wait(&ctrl->kv_full[s], (issued[s] - 1) & 1);
+      for (int hf = 0; hf < 2; ++hf)
+        if (uses[hf] > 0) drain_wait(&ctrl->kv_full[hf], (uses[hf] - 1) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -201,58 +212,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
       const uint64_t dq[2] = {smem_desc_sw128(smem_u32(smem + OFF_Q1), 16, 1024),
                               smem_desc_sw128(smem_u32(smem + OFF_Q2), 16, 1024)};
-      const uint64_t dk[2] = {smem_desc_sw128(smem_u32(smem + OFF_ST + ST_K1), 16, 1024),
-                              smem_desc_sw128(smem_u32(smem + OFF_ST + ST_K2), 16, 1024)};
-      // V [64 keys x 256 columns] as four 64-column boxes BOX_K apart (MN-major B).
-      const uint64_t dvb = smem_desc_sw128(smem_u32(smem + OFF_ST + ST_V), BOX_K, 1024);
+      // K-major views of half hf: K1 at box 0-1, K2 at box 2-3.
+      const uint64_t dh = smem_desc_sw128(smem_u32(smem + OFF_HALF), 16, 1024);
+      // V [128 keys x 256 columns] in half 1 as four 64-column boxes (MN-major B).
+      const uint64_t dvb = smem_desc_sw128(smem_u32(smem + OFF_HALF + HALF_BYTES), BOX, 1024);
       auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-      // S_k of tile t into buffer b: K = 128 as two 64-column boxes of Q and K.
+      uint32_t uses[2] = {0, 0};  // consumed uses of each half
+      // S_k of tile t from the K tiles in half hk (K = 128 as two 64-column boxes).
       auto issue_qk = [&](int t) {
-        const int s = t & 1, b = t & 1;
+        const bool pass2 = t >= n_kv;
+        const int hk = pass2 ? 0 : (t & 1);
+        if (!mbar_wait(&ctrl->kv_full[hk], uses[hk] & 1, abort_flag, WAIT_TIMEOUT_NS))
+          return false;
+        ++uses[hk];
+        tc_fence_after_sync();
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const uint32_t d_tm = tmem + (k == 0 ? tm_s1(b) : tm_s2(b));
+          const uint32_t d_tm = tmem + tm_s(k, pass2, t);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t qoff = (kk >> 2) * BOX_Q + 32 * (kk & 3);
-            const uint32_t koff = s * STAGE_BYTES + (kk >> 2) * BOX_K + 32 * (kk & 3);
-            umma_bf16_ss(d_tm, adv(dq[k], qoff), adv(dk[k], koff), IDESC_QK, kk > 0);
+            const uint32_t off = (kk >> 2) * BOX + 32 * (kk & 3);
+            umma_bf16_ss(d_tm, adv(dq[k], off),
+                         adv(dh, hk * HALF_BYTES + 2 * k * BOX + off), IDESC_QK, kk > 0);
           }
         }
-        umma_commit(&ctrl->s_full[b]);
-        if (t < n_kv) umma_commit(&ctrl->kv_empty[s]);  // pass 1 reads only K
+        umma_commit(&ctrl->s_full[t & 1]);
+        umma_commit(&ctrl->kv_empty[hk]);  // K read once the S MMAs are done
+        return true;
       };
       bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag, WAIT_TIMEOUT_NS);
       tc_fence_after_sync();
-      for (int t = 0; ok && t < 2 && t < T; ++t) {
-        if (!(ok = mbar_wait(&ctrl->kv_full[t & 1], 0, abort_flag, WAIT_TIMEOUT_NS))) break;
-        tc_fence_after_sync();
-        issue_qk(t);
-      }
+      // Pass 1 runs two tiles ahead (double-buffered S); pass 2 one tile ahead.
+      if (ok) ok = issue_qk(0);
+      if (ok && n_kv > 1) ok = issue_qk(1);
       for (int t = 0; ok && t < T; ++t) {
-        const int s = t & 1, b = t & 1;
+        const int b = t & 1;
         if (!(ok = mbar_wait(&ctrl->s_done[b], (t >> 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
           break;
         tc_fence_after_sync();
         if (t >= n_kv) {
-          // O += P V: P packed over S1[b] (keys 0-31 at columns 0-15, 32-63 at
-          // 32-47), V MN-major (16 keys = 2048 bytes per step), N = 256.
+          // O += P V: P packed over S1 (keys 0-63 at columns 0-31, 64-127 at
+          // 64-95), V MN-major (16 keys = 2048 bytes per step), N = 256.
+          if (!(ok = mbar_wait(&ctrl->kv_full[1], uses[1] & 1, abort_flag, WAIT_TIMEOUT_NS)))
+            break;
+          ++uses[1];
+          tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t pcol = (kk < 2) ? 8 * kk : 32 + 8 * (kk - 2);
-            umma_bf16_ts(tmem + TM_O, tmem + tm_s1(b) + pcol,
-                         adv(dvb, s * STAGE_BYTES + 2048 * kk), IDESC_PV,
-                         (t > n_kv || kk > 0) ? 1u : 0u);
+            const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
+            umma_bf16_ts(tmem + TM_O, tmem + tm_s(0, true, t) + pcol, adv(dvb, 2048 * kk),
+                         IDESC_PV, (t > n_kv || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&ctrl->kv_empty[s]);
+          umma_commit(&ctrl->kv_empty[1]);
         }
-        if (t + 2 < T) {  // S of tile t+2 into buffer b, after PV of tile t (in order)
-          if (!(ok = mbar_wait(&ctrl->kv_full[s], ((t + 2) >> 1) & 1, abort_flag,
-                               WAIT_TIMEOUT_NS)))
-            break;
-          tc_fence_after_sync();
-          issue_qk(t + 2);
-        }
+        // Next S: pass-1 tile t + 2 into this buffer, or (from the last pass-1
+        // tile on) the next pass-2 tile, after PV of this one (in order).
+        const int nxt = (t + 2 < n_kv) ? t + 2 : (t + 1 >= n_kv && t + 1 < T) ? t + 1 : -1;
+        if (nxt >= 0 && !(ok = issue_qk(nxt))) break;
       }
       if (ok) umma_commit(&ctrl->o_done);
       umma_commit(&ctrl->drain);
@@ -267,7 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float sl2 = p.scale_log2;
     const int qpos = q0 + r;
     float m = -INFINITY, l = 0.f;               // pass 1: statistics of map g + 1
-    float m1 = 0.f, m2 = 0.f, c1 = 0.f, c2 = 0.f;  // pass 2: 2^(x - m_k) scaled by c_k
+    float m1 = 0.f, m2 = 0.f, c1 = 0.f, c2 = 0.f;  // pass 2
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int b = t & 1;
@@ -281,34 +297,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int lim = p.causal ? (qpos - kv0) : (p.N - 1 - kv0);
       const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
       if (!pass2) {
-        uint32_t a[32], bb[32];
-        const uint32_t t_s = tmem + lane_addr + (g == 0 ? tm_s1(b) : tm_s2(b));
-        tmem_ld_x32_nowait(t_s, a);
-        tmem_ld_x32_nowait(t_s + 32, bb);
-        tmem_ld_wait_x32(a);
-        tmem_ld_wait_x32(bb);
-        tc_fence_before_sync();
-        mbar_arrive(&ctrl->s_done[b]);  // S read: the buffer may be refilled
-        float x[64];
+        // Online statistics over four 32-column chunks; the buffer is released
+        // once the last chunk has been read.
+        const uint32_t t_s = tmem + lane_addr + tm_s(g, false, t);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld_x32(t_s + c0, a);
+          if (c0 == BN - 32) {
+            tc_fence_before_sync();
+            mbar_arrive(&ctrl->s_done[b]);
+          }
+          float x[32];
+          float mt = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(a[i]) * sl2;
-          x[32 + i] = __uint_as_float(bb[i]) * sl2;
-        }
-        if (masked) {
+          for (int i = 0; i < 32; ++i) {
+            x[i] = __uint_as_float(a[i]) * sl2;
+            if (masked) x[i] = (c0 + i <= lim) ? x[i] : -INFINITY;
+            mt = fmaxf(mt, x[i]);
+          }
+          const float m_new = fmaxf(m, mt);
+          if (m_new != -INFINITY) {
+            float sum = 0.f;
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = (i <= lim) ? x[i] : -INFINITY;
-        }
-        float mt = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mt = fmaxf(mt, x[i]);
-        const float m_new = fmaxf(m, mt);
-        if (m_new != -INFINITY) {
-          float sum = 0.f;
-#pragma unroll
-          for (int i = 0; i < 64; ++i) sum += ex2_approx(x[i] - m_new);
-          l = l * ex2_approx(m - m_new) + sum;
-          m = m_new;
+            for (int i = 0; i < 32; ++i) sum += ex2_approx(x[i] - m_new);
+            l = l * ex2_approx(m - m_new) + sum;
+            m = m_new;
+          }
         }
         if (t == n_kv - 1) {
           // Final statistics of both maps for every row.
@@ -321,27 +336,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           c2 = p.lambda[h] / ctrl->xch[3][r];
         }
       } else {
-        // Keys 32g .. 32g+31 of both maps: P = 2^(x1 - m1) / l1 - lambda 2^(x2 - m2) / l2.
-        uint32_t a[32], bb[32];
-        tmem_ld_x32_nowait(tmem + lane_addr + tm_s1(b) + 32 * g, a);
-        tmem_ld_x32_nowait(tmem + lane_addr + tm_s2(b) + 32 * g, bb);
-        tmem_ld_wait_x32(a);
-        tmem_ld_wait_x32(bb);
-        uint32_t pk[16];
+        // Keys 64g .. 64g+63 of both maps in two 32-key chunks:
+        // P = 2^(x1 - m1) / l1 - lambda 2^(x2 - m2) / l2, packed over S1.
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          const int kc = 64 * g + c0;  // first key column of the chunk
+          uint32_t a[32], bb[32];
+          tmem_ld_x32_nowait(tmem + lane_addr + tm_s(0, true, t) + kc, a);
+          tmem_ld_x32_nowait(tmem + lane_addr + tm_s(1, true, t) + kc, bb);
+          tmem_ld_wait_x32(a);
+          tmem_ld_wait_x32(bb);
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float pa = ex2_approx(fmaf(__uint_as_float(a[i]), sl2, -m1)) * c1 -
-                     ex2_approx(fmaf(__uint_as_float(bb[i]), sl2, -m2)) * c2;
-          float pb = ex2_approx(fmaf(__uint_as_float(a[i + 1]), sl2, -m1)) * c1 -
-                     ex2_approx(fmaf(__uint_as_float(bb[i + 1]), sl2, -m2)) * c2;
-          if (masked) {
-            pa = (32 * g + i <= lim) ? pa : 0.f;
-            pb = (32 * g + i + 1 <= lim) ? pb : 0.f;
+          for (int i = 0; i < 32; i += 2) {
+            float pa = ex2_approx(fmaf(__uint_as_float(a[i]), sl2, -m1)) * c1 -
+                       ex2_approx(fmaf(__uint_as_float(bb[i]), sl2, -m2)) * c2;
+            float pb = ex2_approx(fmaf(__uint_as_float(a[i + 1]), sl2, -m1)) * c1 -
+                       ex2_approx(fmaf(__uint_as_float(bb[i + 1]), sl2, -m2)) * c2;
+            if (masked) {
+              pa = (kc + i <= lim) ? pa : 0.f;
+              pb = (kc + i + 1 <= lim) ? pb : 0.f;
+            }
+            pk[i / 2] = pack_bf16x2(pa, pb);
           }
-          pk[i / 2] = pack_bf16x2(pa, pb);
+          // Over S1 columns 64g + c0/2 .. +15: read in this or the previous chunk.
+          tmem_st_x16(tmem + lane_addr + tm_s(0, true, t) + 64 * g + c0 / 2, pk);
         }
-        // Over S1[b] columns 32g .. 32g+15, which this group has just read.
-        tmem_st_x16(tmem + lane_addr + tm_s1(b) + 32 * g, pk);
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(&ctrl->s_done[b]);
@@ -472,7 +492,7 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1,
   const void *bases[5] = {q1, k1, q2, k2, v};
   for (int i = 0; i < 5; ++i) {
     const uint64_t width = (i == 4) ? DV : HD;
-    const uint32_t rows = (i == 0 || i == 2) ? BM : BN;
+    const uint32_t rows = 128;
     if (encode_map(&maps[i], bases[i], width, static_cast<uint64_t>(N),
                    static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B), rows) !=
         CUDA_SUCCESS)
