@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float sl2 = p.scale_log2;
     const int qpos = q0 + r;
     float m = -INFINITY, l = 0.f;               // pass 1: statistics of map g + 1
-    float m1 = 0.f, m2 = 0.f, c1 = 0.f, c2 = 0.f;  // pass 2
+    float m1 = 0.f, m2 = 0.f, c2 = 0.f;  // pass 2: log2-sum-exp of each map, lambda
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int b = t & 1;
@@ -297,8 +297,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int lim = p.causal ? (qpos - kv0) : (p.N - 1 - kv0);
       const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
       if (!pass2) {
-        // Online statistics over four 32-column chunks; the buffer is released
-        // once the last chunk has been read.
+        // Online statistics over four 32-column chunks.  As in the d = 64
+        // kernel, exponentials are taken against the current reference m and a
+        // chunk whose sum is at most 2^8 needs nothing else; otherwise its
+        // maximum (from the registers) moves m first.  The buffer is released
+        // as soon as the last chunk has been read.
         const uint32_t t_s = tmem + lane_addr + tm_s(g, false, t);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -308,36 +311,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before_sync();
             mbar_arrive(&ctrl->s_done[b]);
           }
-          float x[32];
-          float mt = -INFINITY;
+          if (masked) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[i] = __uint_as_float(a[i]) * sl2;
-            if (masked) x[i] = (c0 + i <= lim) ? x[i] : -INFINITY;
-            mt = fmaxf(mt, x[i]);
+            for (int i = 0; i < 32; ++i)
+              a[i] = (c0 + i <= lim) ? a[i] : __float_as_uint(-INFINITY);
           }
-          const float m_new = fmaxf(m, mt);
-          if (m_new != -INFINITY) {
-            float sum = 0.f;
+          float2 acc = make_float2(0.f, 0.f);
+          const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m, -m);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sum += ex2_approx(x[i] - m_new);
-            l = l * ex2_approx(m - m_new) + sum;
-            m = m_new;
+          for (int i = 0; i < 32; i += 2) {
+            float2 e = __ffma2_rn(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                                  sc, nm);
+            e.x = ex2_approx(e.x);
+            e.y = ex2_approx(e.y);
+            acc = __fadd2_rn(acc, e);
+          }
+          const float sum = acc.x + acc.y;
+          if (__any_sync(0xffffffffu, !(sum <= 256.f))) {
+            // Exact: the chunk maximum, then the sum against max(m, chunk max).
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(a[i]));
+            const float m_new = fmaxf(m, mt * sl2);
+            if (m_new != -INFINITY) {
+              float2 acc2 = make_float2(0.f, 0.f);
+              const float2 nm2 = make_float2(-m_new, -m_new);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                float2 e = __ffma2_rn(
+                    make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])), sc, nm2);
+                e.x = ex2_approx(e.x);
+                e.y = ex2_approx(e.y);
+                acc2 = __fadd2_rn(acc2, e);
+              }
+              l = l * ex2_approx(m - m_new) + (acc2.x + acc2.y);
+              m = m_new;
+            }
+          } else {
+            l += sum;
           }
         }
         if (t == n_kv - 1) {
-          // Final statistics of both maps for every row.
-          ctrl->xch[2 * g][r] = m;
-          ctrl->xch[2 * g + 1][r] = l;
+          // Final statistics of both maps as log2-sum-exp per row.
+          ctrl->xch[g][r] = m + __log2f(l);
           named_barrier_sync(1, 256);
           m1 = ctrl->xch[0][r];
-          m2 = ctrl->xch[2][r];
-          c1 = 1.f / ctrl->xch[1][r];
-          c2 = p.lambda[h] / ctrl->xch[3][r];
+          m2 = ctrl->xch[1][r];
+          c2 = p.lambda[h];
         }
       } else {
         // Keys 64g .. 64g+63 of both maps in two 32-key chunks:
-        // P = 2^(x1 - m1) / l1 - lambda 2^(x2 - m2) / l2, packed over S1.
+        // P = 2^(x1 - lse1) - lambda 2^(x2 - lse2), packed over S1.
+        const float2 sc = make_float2(sl2, sl2);
+        const float2 n1 = make_float2(-m1, -m1), n2 = make_float2(-m2, -m2);
+        const float2 nl = make_float2(-c2, -c2);
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
           const int kc = 64 * g + c0;  // first key column of the chunk
@@ -349,15 +376,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float pa = ex2_approx(fmaf(__uint_as_float(a[i]), sl2, -m1)) * c1 -
-                       ex2_approx(fmaf(__uint_as_float(bb[i]), sl2, -m2)) * c2;
-            float pb = ex2_approx(fmaf(__uint_as_float(a[i + 1]), sl2, -m1)) * c1 -
-                       ex2_approx(fmaf(__uint_as_float(bb[i + 1]), sl2, -m2)) * c2;
+            float2 e1 = __ffma2_rn(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                                   sc, n1);
+            float2 e2 = __ffma2_rn(
+                make_float2(__uint_as_float(bb[i]), __uint_as_float(bb[i + 1])), sc, n2);
+            e1.x = ex2_approx(e1.x);
+            e1.y = ex2_approx(e1.y);
+            e2.x = ex2_approx(e2.x);
+            e2.y = ex2_approx(e2.y);
+            float2 pp = __ffma2_rn(e2, nl, e1);
             if (masked) {
-              pa = (kc + i <= lim) ? pa : 0.f;
-              pb = (kc + i + 1 <= lim) ? pb : 0.f;
+              pp.x = (kc + i <= lim) ? pp.x : 0.f;
+              pp.y = (kc + i + 1 <= lim) ? pp.y : 0.f;
             }
-            pk[i / 2] = pack_bf16x2(pa, pb);
+            pk[i / 2] = pack_bf16x2(pp.x, pp.y);
           }
           // Over S1 columns 64g + c0/2 .. +15: read in this or the previous chunk.
           tmem_st_x16(tmem + lane_addr + tm_s(0, true, t) + 64 * g + c0 / 2, pk);
