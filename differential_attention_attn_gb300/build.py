@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdiffattn.so")
 SOURCES = ["api.cu", "fwd_bf16_sm103.cu", "fwd_f32.cu", "headnorm.cu", "splitkv.cu",
-           "noalloc.cu", "bwd_bf16_sm103.cu", "fwd_d128_sm103.cu"]
+           "noalloc.cu", "bwd_bf16_sm103.cu", "fwd_d128_sm103.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

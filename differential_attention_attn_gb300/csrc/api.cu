@@ -241,6 +241,13 @@ diffattn_status diffattn_headnorm(const diffattn_desc *desc, const float *x, con
   return launch_headnorm(*desc, x, norm_w, out, static_cast<cudaStream_t>(stream));
 }
 
+diffattn_status diffattn_selftest_wait(int32_t *status_dev, int64_t timeout_ns, void *stream) {
+  if (status_dev == nullptr || timeout_ns <= 0 || timeout_ns > 2000000000) return DIFFATTN_ERR_INVALID_ARG;
+  diffattn_status st = check_sm103();
+  if (st != DIFFATTN_OK) return st;
+  return launch_selftest_wait(status_dev, timeout_ns, static_cast<cudaStream_t>(stream));
+}
+
 double diffattn_lambda_init(int layer) {
   return 0.8 - 0.6 * std::exp(-0.3 * (static_cast<double>(layer) - 1.0));
 }

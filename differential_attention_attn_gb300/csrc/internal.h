@@ -79,6 +79,9 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1,
                                       const float *lambda, const float *norm_w, void *out,
                                       cudaStream_t stream);
 
+// Bounded-wait self-test (selftest.cu).
+diffattn_status launch_selftest_wait(int32_t *status, int64_t timeout_ns, cudaStream_t stream);
+
 // fp32 forward on CUDA cores (d <= 128, N <= 4096).
 diffattn_status launch_fwd_f32(const diffattn_desc &desc, const float *q1, const float *k1,
                                const float *q2, const float *k2, const float *v,

@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH):
         lib.diffattn_fwd_strided.restype = ctypes.c_int
         lib.diffattn_fwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp,
                                              ctypes.POINTER(Strides), vp]
+        lib.diffattn_selftest_wait.restype = ctypes.c_int
+        lib.diffattn_selftest_wait.argtypes = [vp, ctypes.c_int64, vp]
         lib.diffattn_headnorm.restype = ctypes.c_int
         lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
         lib.diffattn_lambda_init.restype = ctypes.c_double
@@ -408,3 +410,12 @@ def headnorm(x, *, H: int, norm_w=None, eps: float = 1e-5, lambda_init: float = 
     _check(load().diffattn_headnorm(ctypes.byref(desc), _ptr(x), _ptr(norm_w), _ptr(out),
                                     _stream_handle(stream)))
     return out
+
+
+def selftest_wait(timeout_ns: int = 50_000_000, stream=None):
+    """`diffattn_selftest_wait`: returns (status code, first wait us, second wait us)."""
+    st = torch.zeros(3, dtype=torch.int32, device="cuda")
+    _check(load().diffattn_selftest_wait(_ptr(st), int(timeout_ns), _stream_handle(stream)))
+    torch.cuda.synchronize()
+    code, w0, w1 = (int(x) for x in st.cpu())
+    return code, w0, w1

@@ -302,6 +302,19 @@ diffattn_status diffattn_headnorm(const diffattn_desc *desc, const float *x,
  */
 double diffattn_lambda_init(int layer);
 
+/*
+ * diffattn_selftest_wait — diagnostic with no counterpart on the pages: it
+ * exercises the bounded pipeline wait every kernel here relies on (see
+ * status_dev above) without faulting or hanging the device.  One warp waits
+ * on an mbarrier that nothing ever arrives on, limited to timeout_ns; a second
+ * warp waits on another such barrier with the kernels' full 2 s limit and
+ * leaves as soon as the first raises the shared abort flag.
+ * status_dev: device int32[3], written as {DIFFATTN_ERR_TIMEOUT if the wait
+ * ran out and raised the flag (else 0), first wait in microseconds, second
+ * wait in microseconds}.  timeout_ns in (0, 2e9].  Asynchronous on stream.
+ */
+diffattn_status diffattn_selftest_wait(int32_t *status_dev, int64_t timeout_ns, void *stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *diffattn_strerror(diffattn_status status);
 
