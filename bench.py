@@ -9,7 +9,8 @@ B=2, H=16, N=4096, d=64 (value width 128).  Prints one JSON line.
 
 --workload picks another measured shape (default needle_4k, the headline).
 wide_4k is the forward with query/key halves of width d = 128 (B=2, H=8,
-N=4096, causal; value width 256).
+N=4096, causal; value width 256).  needle_4k_fp8 is the headline shape with
+q1, k1, q2, k2 in fp8 e4m3 (v and out bf16).
 needle_4k_bwd times the backward pass (diffattn_bwd given the saved
 activations of diffattn_fwd_train) on the needle_4k shape, at 20*d
 algorithmic flops per visible pair.
@@ -55,9 +56,10 @@ def alg_flops(B, H, N, d, causal=True) -> float:
     return 8.0 * d * pairs
 
 
-def alg_bytes(B, H, N, d, elem=2) -> float:
+def alg_bytes(B, H, N, d, elem=2, qk_elem=None) -> float:
     # q1, k1, q2, k2 (4 * d) + v (2d) in, out (2d) out, per token per head
-    return float(B * H * N * (4 * d + 2 * d + 2 * d) * elem)
+    qk = elem if qk_elem is None else qk_elem
+    return float(B * H * N * (4 * d * qk + (2 * d + 2 * d) * elem))
 
 
 def row_flops(i, d, causal=True) -> float:
@@ -571,9 +573,14 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     ops.load()
 
+    fp8 = WORKLOAD == "needle_4k_fp8"
     if WORKLOAD == "wide_4k":  # d = 128 per half (value width 256)
         w = W.custom(3000 + rank, B=2, H=8, N=4096, d=128, causal=True, headnorm=True,
                      random_w=True, layer=12)
+    elif fp8:  # the needle inputs with q1, k1, q2, k2 rounded to e4m3
+        w = W.make("needle_4k", seed_offset=rank)
+        for name in ("q1", "k1", "q2", "k2"):
+            setattr(w, name, getattr(w, name).float().to(torch.float8_e4m3fn))
     else:
         w = W.make(WORKLOAD, seed_offset=rank)
     B, H, N, d = w.B, w.H, w.N, w.d
@@ -593,9 +600,11 @@ def run_ours(args):
     kw = dict(causal=True, headnorm=True, norm_w=norm_w, eps=float(np.float32(w.eps)),
               lambda_init=li, stream=stream)
 
+    fwd = ops.fwd_fp8 if fp8 else ops.fwd
+
     def step(i):
         ins, out = sets[i % n_sets]
-        ops.fwd(*ins, lam, out=out, **kw)
+        fwd(*ins, lam, out=out, **kw)
 
     for i in range(args.warmup):
         step(i)
@@ -632,7 +641,7 @@ def run_ours(args):
     def e2e_step():
         for dst, src in zip(dev_in, pinned):
             dst.copy_(src, non_blocking=True)
-        ops.fwd(*dev_in, lam, out=dev_out, **kw)
+        fwd(*dev_in, lam, out=dev_out, **kw)
         host_out.copy_(dev_out, non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 3))):
@@ -667,9 +676,11 @@ def run_ours(args):
     peak = float(peaks["bf16_tflops"])
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC.replace("bf16", "e4m3 q/k, bf16 v") if fp8 else METRIC,
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 q/k, bf16 v/out" if fp8 else "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": d, "dv": 2 * d,
                    "causal": True, "headnorm": True,
                    "flops_convention": "8*d per visible pair, B*H*N^2/2 pairs",
@@ -682,9 +693,10 @@ def run_ours(args):
                      "kernel": ("diffattn_fwd_d128_sm103_kernel" if d == 128
                                 else "diffattn_fwd_bf16_sm103_kernel"),
                      "alg_flops_per_launch": flops_step,
-                     "alg_bytes_per_launch": alg_bytes(B, H, N, d),
-                     "achieved_gbs": alg_bytes(B, H, N, d) / (launch_ms * 1e-3) / 1e9,
-                     "traffic": read_traffic(WORKLOAD) if d == 64 else None},
+                     "alg_bytes_per_launch": alg_bytes(B, H, N, d, qk_elem=1 if fp8 else 2),
+                     "achieved_gbs": alg_bytes(B, H, N, d, qk_elem=1 if fp8 else 2)
+                     / (launch_ms * 1e-3) / 1e9,
+                     "traffic": read_traffic(WORKLOAD) if d == 64 and not fp8 else None},
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
                 "d2h_bytes_per_step": int(host_out.numel() * host_out.element_size())},
@@ -708,7 +720,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["needle_4k", "small_causal", "mid_causal", "long_16k", *DECODE,
-                             "needle_4k_bwd", "wide_4k"])
+                             "needle_4k_bwd", "wide_4k", "needle_4k_fp8"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":

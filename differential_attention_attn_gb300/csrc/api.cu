@@ -17,7 +17,9 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 diffattn_status check_desc(const diffattn_desc *desc) {
   if (desc == nullptr) return DIFFATTN_ERR_INVALID_ARG;
   if (desc->B < 0 || desc->H < 0 || desc->N < 0 || desc->d <= 0) return DIFFATTN_ERR_INVALID_ARG;
-  if (desc->dtype != DIFFATTN_BF16 && desc->dtype != DIFFATTN_F32) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->dtype != DIFFATTN_BF16 && desc->dtype != DIFFATTN_F32 &&
+      desc->dtype != DIFFATTN_E4M3_QK)
+    return DIFFATTN_ERR_INVALID_ARG;
   if (!(desc->eps >= 0.f) || !std::isfinite(desc->eps) || !std::isfinite(desc->lambda_init))
     return DIFFATTN_ERR_INVALID_ARG;
   if (desc->headnorm < 0 || desc->headnorm > 2) return DIFFATTN_ERR_INVALID_ARG;
@@ -101,8 +103,10 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
   if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
   if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out) return DIFFATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (desc->dtype == DIFFATTN_BF16) {
+  if (desc->dtype == DIFFATTN_BF16 || desc->dtype == DIFFATTN_E4M3_QK) {
     if (desc->d != 64 && desc->d != 128) return DIFFATTN_ERR_UNSUPPORTED;
+    if (desc->dtype == DIFFATTN_E4M3_QK && (desc->d != 64 || desc->headnorm == 2))
+      return DIFFATTN_ERR_UNSUPPORTED;
     if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
         !aligned16(out))
       return DIFFATTN_ERR_INVALID_ARG;

@@ -159,6 +159,30 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
+// e4m3 operands (kind::f8f6f4): instruction descriptor with A and B both
+// E4M3 (format code 0), fp32 D, K-major; and the shared-memory descriptor of
+// a tile of 64-byte rows with 64-byte swizzle (layout code 4, 8-row groups
+// 512 bytes apart).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  desc |= static_cast<uint64_t>(1) << 16;
+  desc |= static_cast<uint64_t>(512 >> 4) << 32;
+  desc |= static_cast<uint64_t>(1) << 46;
+  desc |= static_cast<uint64_t>(4) << 61;
+  return desc;
+}
+__device__ __forceinline__ void umma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // One 32-column chunk of a softmax row: mask (key column c0 + i visible iff
 // c0 + i <= lim), x = s * log2(e)/sqrt(d) - m, p = 2^x, accumulate the sum
 // in four packed partial sums and pack p as bf16 pairs into pk[c0/2 ..].
@@ -242,7 +266,10 @@ __device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
 // states to p.part, no epilogue); otherwise the whole forward of a query tile.
 // kSave (with !kPartial): also store the activations the backward pass needs.
 // kGroup (with !kPartial): the head norm is the mean-subtracting form.
-template <bool kPartial, bool kSave, bool kGroup>
+// kFp8 (single pass only): q1, k1, q2, k2 are e4m3 (one byte per element, 64-byte
+// rows with 64-byte swizzle in the same shared-memory slots); S is computed by
+// kind::f8f6f4 MMAs, everything from P on is unchanged.
+template <bool kPartial, bool kSave, bool kGroup, bool kFp8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     diffattn_fwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
                                    const __grid_constant__ CUtensorMap tm_k1,
@@ -254,6 +281,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                               ~static_cast<uintptr_t>(1023));
   Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + OFF_CTRL);
   volatile int *abort_flag = &ctrl->abort;
+  constexpr uint32_t QK_LOAD_BYTES = kFp8 ? TILE_QK_BYTES / 2 : TILE_QK_BYTES;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -323,7 +351,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-      mbar_arrive_expect_tx(&ctrl->q_full, 2 * TILE_QK_BYTES);
+      mbar_arrive_expect_tx(&ctrl->q_full, 2 * QK_LOAD_BYTES);
       tma_load_4d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, q0, h, b_idx);
       tma_load_4d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, q0, h, b_idx);
       for (int j = 0; j < n_kv; ++j) {
@@ -333,7 +361,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
         const int32_t y = (kv_lo + j) * BN;
-        mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * TILE_QK_BYTES);
+        mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * QK_LOAD_BYTES);
         tma_load_4d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, h, b_idx);
         tma_load_4d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, h, b_idx);
         mbar_arrive_expect_tx(&ctrl->v_full[s], TILE_V_BYTES);
@@ -355,6 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
+      constexpr uint32_t IDESC_QK8 = idesc_e4m3_f32(BM, BN);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
       // Operand descriptors are built once.  Every operand is a base tile plus a
       // byte offset below 256 KB, so advancing it only adds offset >> 4 to the
@@ -366,10 +395,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t dvb =
           smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_V), TILE_QK_BYTES, 1024);
       auto qk = [&](int k, int s) {  // S_k = Q_k K_k^T, K from stage s; K slices of 32 bytes
-        const uint64_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
+        if (kFp8) {
+          // e4m3 rows of 64 bytes, 64-byte swizzle (8-row atoms of 512 bytes); an
+          // f8f6f4 MMA takes 32 elements (32 bytes) of K, so two cover d = 64.
+          const uint64_t a = smem_desc_sw64(smem_u32(smem + (k ? OFF_Q2 : OFF_Q1)));
+          const uint64_t b = smem_desc_sw64(smem_u32(smem + OFF_STAGES + s * STAGE_BYTES +
+                                                     (k ? STAGE_K2 : STAGE_K1)));
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK, kk > 0);
+          for (int kk = 0; kk < 2; ++kk)
+            umma_e4m3_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK8, kk > 0);
+        } else {
+          const uint64_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK, kk > 0);
+        }
       };
       auto pv = [&](int k, int s, bool accumulate) {  // O_k += P_k V; 16 keys = 2048 bytes
         const uint64_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
@@ -638,16 +678,19 @@ EncodeTiledFn encode_tiled_fn() {
 // 4-D view {inner, rows, H, B} of a bf16 tensor with element strides (sn, sh,
 // sb) and contiguous rows; 128-row x 64-column boxes with 128-byte swizzle.
 CUresult encode_tile_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t n,
-                         uint64_t H, uint64_t B, const diffattn_strides &st) {
+                         uint64_t H, uint64_t B, const diffattn_strides &st, bool e4m3 = false) {
   EncodeTiledFn encode = encode_tiled_fn();
   if (encode == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const uint64_t es = e4m3 ? 1 : 2;  // element bytes
   cuuint64_t dims[4] = {inner, n, H, B};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
-                           static_cast<cuuint64_t>(st.b) * 2};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * es, static_cast<cuuint64_t>(st.h) * es,
+                           static_cast<cuuint64_t>(st.b) * es};
   cuuint32_t box[4] = {64, 128, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
-                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                const_cast<void *>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                e4m3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
@@ -662,8 +705,11 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   const int64_t N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
   const int64_t n_ktiles = (n_kv + BN - 1) / BN;
+  const bool fp8 = desc.dtype == DIFFATTN_E4M3_QK;
   if (splits < 1 || (splits > 1 && part == nullptr) || (splits > 1 && save != nullptr))
     return DIFFATTN_ERR_INVALID_ARG;
+  if (fp8 && (splits > 1 || save != nullptr || desc.headnorm == 2))
+    return DIFFATTN_ERR_UNSUPPORTED;
   const int64_t split_tiles = (n_ktiles + splits - 1) / splits;
   if (BH * n_qtiles * splits > INT32_MAX || N > INT32_MAX / 2 || n_kv > INT32_MAX / 2 ||
       desc.H > INT32_MAX)
@@ -682,7 +728,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
     const uint64_t inner = (i == 4) ? DV : HD;
     const uint64_t rows = (i == 0 || i == 2) ? N : n_kv;
     if (encode_tile_map(&maps[i], bases[i], inner, rows, static_cast<uint64_t>(desc.H),
-                        static_cast<uint64_t>(desc.B), st[i]) != CUDA_SUCCESS)
+                        static_cast<uint64_t>(desc.B), st[i], fp8 && i < 4) != CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
 
@@ -691,10 +737,11 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
   if (!attr_set[dev]) {
-    auto *k0 = diffattn_fwd_bf16_sm103_kernel<false, false, false>;
-    auto *k1 = diffattn_fwd_bf16_sm103_kernel<true, false, false>;
-    auto *k2 = diffattn_fwd_bf16_sm103_kernel<false, true, false>;
-    auto *k3 = diffattn_fwd_bf16_sm103_kernel<false, false, true>;
+    auto *k0 = diffattn_fwd_bf16_sm103_kernel<false, false, false, false>;
+    auto *k1 = diffattn_fwd_bf16_sm103_kernel<true, false, false, false>;
+    auto *k2 = diffattn_fwd_bf16_sm103_kernel<false, true, false, false>;
+    auto *k3 = diffattn_fwd_bf16_sm103_kernel<false, false, true, false>;
+    auto *k4 = diffattn_fwd_bf16_sm103_kernel<false, false, false, true>;
     if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
         cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -702,6 +749,8 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
         cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
         cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
     attr_set[dev] = true;
@@ -734,17 +783,20 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.save_lse = save ? save + 2 * BH * N * DV : nullptr;
 
   dim3 grid(static_cast<unsigned>(BH * n_qtiles * splits));
-  if (splits > 1)
-    diffattn_fwd_bf16_sm103_kernel<true, false, false>
+  if (fp8)
+    diffattn_fwd_bf16_sm103_kernel<false, false, false, true>
+        <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  else if (splits > 1)
+    diffattn_fwd_bf16_sm103_kernel<true, false, false, false>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else if (save != nullptr)
-    diffattn_fwd_bf16_sm103_kernel<false, true, false>
+    diffattn_fwd_bf16_sm103_kernel<false, true, false, false>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else if (desc.headnorm == 2)
-    diffattn_fwd_bf16_sm103_kernel<false, false, true>
+    diffattn_fwd_bf16_sm103_kernel<false, false, true, false>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else
-    diffattn_fwd_bf16_sm103_kernel<false, false, false>
+    diffattn_fwd_bf16_sm103_kernel<false, false, false, false>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libdiffattn.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "diffattn.h")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
-BF16, F32 = 0, 1
+BF16, F32, E4M3_QK = 0, 1, 2
 _DTYPE_CODE = {torch.bfloat16: BF16, torch.float32: F32}
 
 
@@ -169,6 +169,29 @@ def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm_w=None,
     if tuple(out.shape) != (B, H, N, 2 * d) or out.dtype != dtype:
         raise ValueError("out must be [B, H, N, 2d] of the input dtype")
     desc = make_desc(B, H, N, d, _DTYPE_CODE[dtype], causal, headnorm, eps, lambda_init, status)
+    st = load().diffattn_fwd(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
+                             _ptr(lam), _ptr(norm_w), _ptr(out), _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return out
+
+
+def fwd_fp8(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm_w=None,
+            eps: float = 1e-5, lambda_init: float = 0.0, out=None, status=None, stream=None,
+            raw_status: bool = False):
+    """`diffattn_fwd` with DIFFATTN_E4M3_QK: q1, k1, q2, k2 torch.float8_e4m3fn
+    [B, H, N, 64]; v bf16 [B, H, N, 128]; returns bf16 out [B, H, N, 128]."""
+    B, H, N, d = q1.shape
+    for t in (q1, k1, q2, k2):
+        if t.dtype != torch.float8_e4m3fn or tuple(t.shape) != (B, H, N, d):
+            raise ValueError("q1, k1, q2, k2 must be float8_e4m3fn [B, H, N, d]")
+    if v.dtype != torch.bfloat16 or tuple(v.shape) != (B, H, N, 2 * d):
+        raise ValueError("v must be bfloat16 [B, H, N, 2d]")
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=torch.bfloat16, device=q1.device)
+    _cuda_contig([q1, k1, q2, k2, v, lam, norm_w, out])
+    desc = make_desc(B, H, N, d, E4M3_QK, causal, headnorm, eps, lambda_init, status)
     st = load().diffattn_fwd(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
                              _ptr(lam), _ptr(norm_w), _ptr(out), _stream_handle(stream))
     if raw_status:

@@ -59,8 +59,10 @@ typedef enum diffattn_status {
 } diffattn_status;
 
 typedef enum diffattn_dtype {
-    DIFFATTN_BF16 = 0, /* q/k/v/out bf16, fp32 accumulation */
-    DIFFATTN_F32 = 1   /* q/k/v/out fp32 throughout */
+    DIFFATTN_BF16 = 0,    /* q/k/v/out bf16, fp32 accumulation */
+    DIFFATTN_F32 = 1,     /* q/k/v/out fp32 throughout */
+    DIFFATTN_E4M3_QK = 2  /* q1, k1, q2, k2 fp8 e4m3 (one byte each); v and out bf16;
+                             fp32 accumulation (diffattn_fwd, d == 64 only) */
 } diffattn_dtype;
 
 /* Problem description shared by every entry point. */
@@ -106,6 +108,12 @@ typedef struct diffattn_desc {
  *     needs an sm_103 device.  The other entry points take d == 64 only.
  *   - DIFFATTN_F32: 1 <= d <= 128, N <= 4096.  Plain CUDA-core kernel
  *     (accurate expf, fp32 accumulation).
+ *   - DIFFATTN_E4M3_QK: d == 64, headnorm 0 or 1: the d == 64 kernel with the
+ *     two Q K^T products on fp8 (e4m3) tensor-core MMAs; P V stays bf16.  The
+ *     result is that of the same formula applied to the e4m3 input values
+ *     (exactly representable, so only P and the output are rounded as in the
+ *     bf16 path).  The page remarks that differential attention keeps its
+ *     accuracy under low-bit quantisation; this is that input format.
  * B * H * N == 0 returns DIFFATTN_OK without launching anything.
  */
 diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
