@@ -73,6 +73,8 @@ constexpr int HD = 64;           // query/key half width d
 constexpr int DV = 2 * HD;       // value width 2d
 constexpr int STAGES = 3;        // K/V pipeline depth
 constexpr int NUM_THREADS = 384;
+constexpr uint32_t REGS_CTRL = 56;      // per thread, warps 0-3 (loads, MMA issue)
+constexpr uint32_t REGS_SOFTMAX = 216;  // per thread, warps 4-11 (softmax, epilogue)
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
 
 constexpr uint32_t TILE_QK_BYTES = BM * HD * 2;     // 16 KB: one [128 x 64] bf16 tile
@@ -345,119 +347,128 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = ctrl->tmem_base;
+  // Registers move from the load/MMA warpgroup to the two softmax warpgroups:
+  // 128 x REGS_CTRL + 256 x REGS_SOFTMAX stays within the 384 x 168 of the launch.
+  // (The e4m3 instantiation keeps the launch allocation: with the split, ptxas
+  // spills in it.)
+  static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= NUM_THREADS * 168, "register split");
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      uint32_t issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-      mbar_arrive_expect_tx(&ctrl->q_full, 2 * QK_LOAD_BYTES);
-      tma_load_4d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, q0, h, b_idx);
-      tma_load_4d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, q0, h, b_idx);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % STAGES;
-        const uint32_t u = static_cast<uint32_t>(j / STAGES);
-        if (u > 0 && !mbar_wait(&ctrl->kv_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
-          break;
-        uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
-        const int32_t y = (kv_lo + j) * BN;
-        mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * QK_LOAD_BYTES);
-        tma_load_4d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, h, b_idx);
-        tma_load_4d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, h, b_idx);
-        mbar_arrive_expect_tx(&ctrl->v_full[s], TILE_V_BYTES);
-        tma_load_4d(st + STAGE_V, &tm_v, &ctrl->v_full[s], 0, y, h, b_idx);
-        tma_load_4d(st + STAGE_V + TILE_QK_BYTES, &tm_v, &ctrl->v_full[s], HD, y, h, b_idx);
-        issued[s] = u + 1;
-      }
-      // Never leave with a copy in flight: wait (bounded) for every issued load.
-      drain_wait(&ctrl->q_full, 0);
-      for (int s = 0; s < STAGES; ++s) {
-        if (issued[s] > 0) {
-          drain_wait(&ctrl->k_full[s], (issued[s] - 1) & 1);
-          drain_wait(&ctrl->v_full[s], (issued[s] - 1) & 1);
-        }
-      }
-    }
-    __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
-      constexpr uint32_t IDESC_QK8 = idesc_e4m3_f32(BM, BN);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
-      // Operand descriptors are built once.  Every operand is a base tile plus a
-      // byte offset below 256 KB, so advancing it only adds offset >> 4 to the
-      // 14-bit start-address field (no carry into the other fields).
-      const uint64_t dq[2] = {smem_desc_sw128(smem_u32(smem + OFF_Q1), 16, 1024),
-                              smem_desc_sw128(smem_u32(smem + OFF_Q2), 16, 1024)};
-      const uint64_t dk[2] = {smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K1), 16, 1024),
-                              smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K2), 16, 1024)};
-      const uint64_t dvb =
-          smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_V), TILE_QK_BYTES, 1024);
-      auto qk = [&](int k, int s) {  // S_k = Q_k K_k^T, K from stage s; K slices of 32 bytes
-        if (kFp8) {
-          // e4m3 rows of 64 bytes, 64-byte swizzle (8-row atoms of 512 bytes); an
-          // f8f6f4 MMA takes 32 elements (32 bytes) of K, so two cover d = 64.
-          const uint64_t a = smem_desc_sw64(smem_u32(smem + (k ? OFF_Q2 : OFF_Q1)));
-          const uint64_t b = smem_desc_sw64(smem_u32(smem + OFF_STAGES + s * STAGE_BYTES +
-                                                     (k ? STAGE_K2 : STAGE_K1)));
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            umma_e4m3_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK8, kk > 0);
-        } else {
-          const uint64_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK, kk > 0);
-        }
-      };
-      auto pv = [&](int k, int s, bool accumulate) {  // O_k += P_k V; 16 keys = 2048 bytes
-        const uint64_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_bf16_ts(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, b + 128 * kk, IDESC_PV,
-                       (accumulate || kk > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag, WAIT_TIMEOUT_NS);
-      tc_fence_after_sync();
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % STAGES;
-        const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1;
-        if (!(ok = mbar_wait(&ctrl->k_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
-        tc_fence_after_sync();
-        qk(0, s);
-        umma_commit(&ctrl->s_full[0]);
-        if (j > 0) {
-          if (!(ok = mbar_wait(&ctrl->p_ready[1], (j - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+  if (warp < 4) {
+    if (!kFp8) setmaxnreg_dec<REGS_CTRL>();  // warps 2 and 3 only give up registers
+    if (warp == 0) {
+      // ---------------------------------------------------------------- producer
+      if (lane == 0) {
+        uint32_t issued[STAGES];
+        for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+        mbar_arrive_expect_tx(&ctrl->q_full, 2 * QK_LOAD_BYTES);
+        tma_load_4d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, q0, h, b_idx);
+        tma_load_4d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, q0, h, b_idx);
+        for (int j = 0; j < n_kv; ++j) {
+          const int s = j % STAGES;
+          const uint32_t u = static_cast<uint32_t>(j / STAGES);
+          if (u > 0 && !mbar_wait(&ctrl->kv_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
             break;
-          tc_fence_after_sync();
-          const int sp = (j - 1) % STAGES;
-          pv(1, sp, j - 1 > 0);
-          umma_commit(&ctrl->kv_empty[sp]);
+          uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
+          const int32_t y = (kv_lo + j) * BN;
+          mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * QK_LOAD_BYTES);
+          tma_load_4d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, h, b_idx);
+          tma_load_4d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, h, b_idx);
+          mbar_arrive_expect_tx(&ctrl->v_full[s], TILE_V_BYTES);
+          tma_load_4d(st + STAGE_V, &tm_v, &ctrl->v_full[s], 0, y, h, b_idx);
+          tma_load_4d(st + STAGE_V + TILE_QK_BYTES, &tm_v, &ctrl->v_full[s], HD, y, h, b_idx);
+          issued[s] = u + 1;
         }
-        qk(1, s);
-        umma_commit(&ctrl->s_full[1]);
-        if (!(ok = mbar_wait(&ctrl->v_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
-        if (!(ok = mbar_wait(&ctrl->p_ready[0], j & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+        // Never leave with a copy in flight: wait (bounded) for every issued load.
+        drain_wait(&ctrl->q_full, 0);
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued[s] > 0) {
+            drain_wait(&ctrl->k_full[s], (issued[s] - 1) & 1);
+            drain_wait(&ctrl->v_full[s], (issued[s] - 1) & 1);
+          }
+        }
+      }
+      __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
+        constexpr uint32_t IDESC_QK8 = idesc_e4m3_f32(BM, BN);
+        constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
+        // Operand descriptors are built once.  Every operand is a base tile plus a
+        // byte offset below 256 KB, so advancing it only adds offset >> 4 to the
+        // 14-bit start-address field (no carry into the other fields).
+        const uint64_t dq[2] = {smem_desc_sw128(smem_u32(smem + OFF_Q1), 16, 1024),
+                                smem_desc_sw128(smem_u32(smem + OFF_Q2), 16, 1024)};
+        const uint64_t dk[2] = {smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K1), 16, 1024),
+                                smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K2), 16, 1024)};
+        const uint64_t dvb =
+            smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_V), TILE_QK_BYTES, 1024);
+        auto qk = [&](int k, int s) {  // S_k = Q_k K_k^T, K from stage s; K slices of 32 bytes
+          if (kFp8) {
+            // e4m3 rows of 64 bytes, 64-byte swizzle (8-row atoms of 512 bytes); an
+            // f8f6f4 MMA takes 32 elements (32 bytes) of K, so two cover d = 64.
+            const uint64_t a = smem_desc_sw64(smem_u32(smem + (k ? OFF_Q2 : OFF_Q1)));
+            const uint64_t b = smem_desc_sw64(smem_u32(smem + OFF_STAGES + s * STAGE_BYTES +
+                                                       (k ? STAGE_K2 : STAGE_K1)));
+  #pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+              umma_e4m3_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK8, kk > 0);
+          } else {
+            const uint64_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
+  #pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk)
+              umma_bf16_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK, kk > 0);
+          }
+        };
+        auto pv = [&](int k, int s, bool accumulate) {  // O_k += P_k V; 16 keys = 2048 bytes
+          const uint64_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
+  #pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_bf16_ts(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, b + 128 * kk, IDESC_PV,
+                         (accumulate || kk > 0) ? 1u : 0u);
+        };
+        bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag, WAIT_TIMEOUT_NS);
         tc_fence_after_sync();
-        pv(0, s, j > 0);
-      }
-      if (ok && n_kv > 0) {
-        const int jl = n_kv - 1;
-        if (mbar_wait(&ctrl->p_ready[1], jl & 1, abort_flag, WAIT_TIMEOUT_NS)) {
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int s = j % STAGES;
+          const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1;
+          if (!(ok = mbar_wait(&ctrl->k_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
           tc_fence_after_sync();
-          const int sl = jl % STAGES;
-          pv(1, sl, jl > 0);
-          umma_commit(&ctrl->kv_empty[sl]);
-          umma_commit(&ctrl->o_done);
+          qk(0, s);
+          umma_commit(&ctrl->s_full[0]);
+          if (j > 0) {
+            if (!(ok = mbar_wait(&ctrl->p_ready[1], (j - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+              break;
+            tc_fence_after_sync();
+            const int sp = (j - 1) % STAGES;
+            pv(1, sp, j - 1 > 0);
+            umma_commit(&ctrl->kv_empty[sp]);
+          }
+          qk(1, s);
+          umma_commit(&ctrl->s_full[1]);
+          if (!(ok = mbar_wait(&ctrl->v_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+          if (!(ok = mbar_wait(&ctrl->p_ready[0], j & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+          tc_fence_after_sync();
+          pv(0, s, j > 0);
         }
+        if (ok && n_kv > 0) {
+          const int jl = n_kv - 1;
+          if (mbar_wait(&ctrl->p_ready[1], jl & 1, abort_flag, WAIT_TIMEOUT_NS)) {
+            tc_fence_after_sync();
+            const int sl = jl % STAGES;
+            pv(1, sl, jl > 0);
+            umma_commit(&ctrl->kv_empty[sl]);
+            umma_commit(&ctrl->o_done);
+          }
+        }
+        // Never free tensor memory under a running MMA: wait for all of them.
+        umma_commit(&ctrl->drain);
+        drain_wait(&ctrl->drain, 0);
       }
-      // Never free tensor memory under a running MMA: wait for all of them.
-      umma_commit(&ctrl->drain);
-      drain_wait(&ctrl->drain, 0);
+      __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
     }
-    __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
-  } else if (warp >= 4) {
+  } else {
+    if (!kFp8) setmaxnreg_inc<REGS_SOFTMAX>();
     // ---------------------------------------------------------------- softmax
     const int k = (warp - 4) / 4;          // which map
     const int r = (warp % 4) * 32 + lane;  // query row within the tile = TMEM lane

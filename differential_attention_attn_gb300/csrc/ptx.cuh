@@ -329,6 +329,18 @@ __device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bo
   return r != 0;
 }
 
+// Per-warpgroup register budgets (every warp of the warpgroup executes the same
+// instruction).  The increases are paid for by the decreases out of the block's
+// launch allocation: callers keep the sum within threads x registers at launch.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ex2.approx (the MUFU base-2 exponential), flush-to-zero.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
