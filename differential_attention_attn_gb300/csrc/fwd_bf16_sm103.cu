@@ -11,7 +11,11 @@
 // attention; that is what makes the flash-style online softmax below valid
 // for each map separately.
 //
-// Work item: one (batch*head, 128-row query tile).  Per key tile of 128 keys:
+// Work item: one (batch*head, 128-row query tile).  The single-pass grid is
+// persistent (one CTA per SM at most), each CTA walking a fixed share of the
+// items: the next item's Q load and first S MMAs overlap the current item's
+// last P V products and epilogue, instead of a CTA exit, launch and prologue
+// per item.  Per key tile of 128 keys:
 //   S1 = Q1 K1^T, S2 = Q2 K2^T              tcgen05 SS MMAs into TMEM
 //   P_k = exp2(S_k * log2(e)/sqrt(d) - m_k)  per map, thread-per-row softmax
 //   O1 += P1 V, O2 += P2 V                   tcgen05 TS MMAs (P read from TMEM)
@@ -30,7 +34,8 @@
 //   warps 8-11  softmax of map 2
 // The epilogue is split by value columns: map-1 warps do columns 0-63, map-2
 // warps columns 64-127, exchanging 1/l and partial sums of squares through
-// shared memory.
+// shared memory.  Once both have read O1 and O2 into registers they release
+// them (o_free) to the next item's first P V.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) S1 (P1 as packed bf16 over its first 64 columns)
@@ -58,6 +63,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -90,15 +96,18 @@ constexpr uint32_t OFF_CTRL = OFF_STAGES + STAGES * STAGE_BYTES;
 
 struct Ctrl {
   uint64_t q_full;
+  uint64_t q_empty;   // the item's last Q K^T MMAs completed: Q may be replaced
   uint64_t k_full[STAGES];
   uint64_t v_full[STAGES];
   uint64_t kv_empty[STAGES];
   uint64_t s_full[2];
   uint64_t p_ready[2];
   uint64_t o_done;
+  uint64_t o_free;    // the epilogue has read O1 and O2: the next item's P V may overwrite
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  float xch[2 * BM];  // epilogue exchange of per-row values between the two maps
 };
 
 constexpr uint32_t SMEM_BYTES = OFF_CTRL + sizeof(Ctrl) + 1024;  // + alignment slack
@@ -128,6 +137,7 @@ struct Params {
   int32_t q_off;      // sequence position of query row 0 (N_kv - N): causal alignment
   int32_t n_qtiles;
   int32_t n_ktiles;
+  uint32_t n_items;   // BH * n_qtiles
   int32_t causal;
   int32_t headnorm;
   float scale_log2;   // log2(e) / sqrt(d)
@@ -264,6 +274,51 @@ __device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
   return m;
 }
 
+// One work item: a (batch, head, 128-row query tile) and its key tiles.
+struct Item {
+  int q0;       // first query row
+  int h, b;     // head, batch
+  int64_t bh;   // b * H + h
+  int kv_lo;    // first key tile (split-KV key range; 0 otherwise)
+  int n_kv;     // key tiles to process
+};
+
+// The r-th work item of this CTA; false past the end.  The items are the
+// (b*h, query tile) pairs, heaviest first: all heads' last query tiles, then the
+// previous ones.  Single pass: the grid is persistent (at most one CTA per SM)
+// and CTA c takes items c, 2G-1-c, 2G+c, 4G-1-c, ... of G, a deal whose
+// direction alternates every round so that every CTA gets a similar mix of long
+// and short items.  Split-KV: the CTA's single (query tile, key range),
+// consecutive CTAs taking consecutive ranges of one query tile.  The decode uses
+// 32-bit division (fewer than 2^31 items, checked at launch): a 64-bit one is a
+// long software sequence.  The single-pass key range origin is a compile-time
+// zero: a run-time origin measurably slows the loops.
+template <bool kPartial>
+__device__ __forceinline__ bool next_item(const Params &p, uint32_t r, Item &it) {
+  uint32_t idx;
+  int split = 0;
+  if (kPartial) {
+    if (r > 0) return false;
+    idx = blockIdx.x / static_cast<uint32_t>(p.splits);
+    split = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.splits));
+  } else {
+    const uint32_t G = gridDim.x, c = blockIdx.x;
+    idx = r * G + ((r & 1) ? G - 1 - c : c);
+    if (idx >= p.n_items) return false;
+  }
+  const uint32_t BH32 = static_cast<uint32_t>(p.BH), H32 = static_cast<uint32_t>(p.H);
+  const int qt = p.n_qtiles - 1 - static_cast<int>(idx / BH32);
+  const uint32_t bh = idx % BH32;
+  it.h = static_cast<int>(bh % H32);
+  it.b = static_cast<int>(bh / H32);
+  it.bh = bh;
+  it.q0 = qt * BM;
+  const int n_all = static_cast<int>(key_tiles_seen(qt, p.N, p.N_kv, p.causal != 0));
+  it.kv_lo = kPartial ? split * p.split_tiles : 0;
+  it.n_kv = kPartial ? min(n_all, it.kv_lo + p.split_tiles) - it.kv_lo : n_all;
+  return true;
+}
+
 // kPartial: split-KV partial mode (a key range per CTA, partial softmax
 // states to p.part, no epilogue); otherwise the whole forward of a query tile.
 // kSave (with !kPartial): also store the activations the backward pass needs.
@@ -292,32 +347,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // before reading the partial blocks.
   if (kPartial) grid_dependents_launch();
 
-  // Heaviest tiles first: all heads' last query tiles, then the previous ones.
-  // With split-KV, consecutive CTAs take consecutive key ranges of one item.
-  // (The single-pass instantiation keeps the key range origin a compile-time
-  // zero: a run-time origin measurably slows its loops.)
-  // The grid has fewer than 2^31 CTAs (checked at launch), so the decode uses
-  // 32-bit division: a 64-bit one is a long software sequence that every CTA
-  // would run before its first load.
-  const uint32_t BH32 = static_cast<uint32_t>(p.BH), H32 = static_cast<uint32_t>(p.H);
-  const uint32_t item32 = kPartial ? blockIdx.x / static_cast<uint32_t>(p.splits) : blockIdx.x;
-  const int64_t item = item32;
-  const int split = kPartial ? static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.splits)) : 0;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(item32 / BH32);
-  const uint32_t bh32 = item32 % BH32;
-  const int64_t bh = bh32;
-  const int h = static_cast<int>(bh32 % H32);
-  const int b_idx = static_cast<int>(bh32 / H32);
-  const int q0 = qt * BM;
-  const int n_all = static_cast<int>(key_tiles_seen(qt, p.N, p.N_kv, p.causal != 0));
-  const int kv_lo = split * p.split_tiles;  // first key tile of this CTA
-  const int n_kv = min(n_all, kv_lo + p.split_tiles) - kv_lo;
-  // Early causal query tiles see fewer key tiles than there are splits; the
-  // combine step skips those empty ranges, so the CTA has nothing to do.
-  if (kPartial && n_kv <= 0) return;
+  // Split-KV partial mode: one (query tile, key range) per CTA, consecutive
+  // CTAs taking consecutive key ranges of one query tile.  A CTA whose range is
+  // empty (early causal query tiles see fewer key tiles than there are splits)
+  // has nothing to do; the combine step skips it.
+  if (kPartial) {
+    const uint32_t item32 = blockIdx.x / static_cast<uint32_t>(p.splits);
+    const int split = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.splits));
+    const int qt = p.n_qtiles - 1 - static_cast<int>(item32 / static_cast<uint32_t>(p.BH));
+    const int n_all = static_cast<int>(key_tiles_seen(qt, p.N, p.N_kv, p.causal != 0));
+    if (min(n_all, (split + 1) * p.split_tiles) - split * p.split_tiles <= 0) return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
+    mbar_init(&ctrl->q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctrl->k_full[s], 1);
       mbar_init(&ctrl->v_full[s], 1);
@@ -328,6 +372,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&ctrl->p_ready[k], BM);
     }
     mbar_init(&ctrl->o_done, 1);
+    mbar_init(&ctrl->o_free, 2 * BM);
     mbar_init(&ctrl->drain, 1);
     ctrl->abort = 0;
     fence_barrier_init();
@@ -353,6 +398,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // spills in it.)
   static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= NUM_THREADS * 168, "register split");
 
+  // Every role walks the same sequence of work items (next_item) and counts
+  // barrier phases by item (q_full, q_empty, o_done, o_free) or by key tile
+  // over all items (k_full, v_full, kv_empty per stage; s_full, p_ready).
   if (warp < 4) {
     if (!kFp8) setmaxnreg_dec<REGS_CTRL>();  // warps 2 and 3 only give up registers
     if (warp == 0) {
@@ -360,26 +408,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         uint32_t issued[STAGES];
         for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-        mbar_arrive_expect_tx(&ctrl->q_full, 2 * QK_LOAD_BYTES);
-        tma_load_4d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, q0, h, b_idx);
-        tma_load_4d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, q0, h, b_idx);
-        for (int j = 0; j < n_kv; ++j) {
-          const int s = j % STAGES;
-          const uint32_t u = static_cast<uint32_t>(j / STAGES);
-          if (u > 0 && !mbar_wait(&ctrl->kv_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
+        uint32_t q_loads = 0;
+        uint32_t g = 0;  // key tiles loaded so far
+        bool ok = true;
+        Item it;
+        for (uint32_t r = 0; ok && next_item<kPartial>(p, r, it); ++r) {
+          // The previous item's Q is dead once its last Q K^T MMAs completed.
+          if (r > 0 && !(ok = mbar_wait(&ctrl->q_empty, (r - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
             break;
-          uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
-          const int32_t y = (kv_lo + j) * BN;
-          mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * QK_LOAD_BYTES);
-          tma_load_4d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, h, b_idx);
-          tma_load_4d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, h, b_idx);
-          mbar_arrive_expect_tx(&ctrl->v_full[s], TILE_V_BYTES);
-          tma_load_4d(st + STAGE_V, &tm_v, &ctrl->v_full[s], 0, y, h, b_idx);
-          tma_load_4d(st + STAGE_V + TILE_QK_BYTES, &tm_v, &ctrl->v_full[s], HD, y, h, b_idx);
-          issued[s] = u + 1;
+          mbar_arrive_expect_tx(&ctrl->q_full, 2 * QK_LOAD_BYTES);
+          tma_load_4d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, it.q0, it.h, it.b);
+          tma_load_4d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, it.q0, it.h, it.b);
+          q_loads = r + 1;
+          for (int j = 0; j < it.n_kv; ++j, ++g) {
+            const int s = static_cast<int>(g % STAGES);
+            const uint32_t u = g / STAGES;
+            if (u > 0 &&
+                !(ok = mbar_wait(&ctrl->kv_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+              break;
+            uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
+            const int32_t y = (it.kv_lo + j) * BN;
+            mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * QK_LOAD_BYTES);
+            tma_load_4d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, it.h, it.b);
+            tma_load_4d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, it.h, it.b);
+            mbar_arrive_expect_tx(&ctrl->v_full[s], TILE_V_BYTES);
+            tma_load_4d(st + STAGE_V, &tm_v, &ctrl->v_full[s], 0, y, it.h, it.b);
+            tma_load_4d(st + STAGE_V + TILE_QK_BYTES, &tm_v, &ctrl->v_full[s], HD, y, it.h, it.b);
+            issued[s] = u + 1;
+          }
         }
         // Never leave with a copy in flight: wait (bounded) for every issued load.
-        drain_wait(&ctrl->q_full, 0);
+        if (q_loads > 0) drain_wait(&ctrl->q_full, (q_loads - 1) & 1);
         for (int s = 0; s < STAGES; ++s) {
           if (issued[s] > 0) {
             drain_wait(&ctrl->k_full[s], (issued[s] - 1) & 1);
@@ -396,13 +455,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
         // Operand descriptors are built once.  Every operand is a base tile plus a
         // byte offset below 256 KB, so advancing it only adds offset >> 4 to the
-        // 14-bit start-address field (no carry into the other fields).
-        const uint64_t dq[2] = {smem_desc_sw128(smem_u32(smem + OFF_Q1), 16, 1024),
-                                smem_desc_sw128(smem_u32(smem + OFF_Q2), 16, 1024)};
-        const uint64_t dk[2] = {smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K1), 16, 1024),
-                                smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K2), 16, 1024)};
-        const uint64_t dvb =
-            smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_V), TILE_QK_BYTES, 1024);
+        // 14-bit start-address field (no carry into the other fields).  All of
+        // them share the high word (stride offset 1024, version, 128-byte
+        // swizzle), so only their low words are kept.
+        auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
+        const uint32_t dhi =
+            static_cast<uint32_t>(smem_desc_sw128(smem_u32(smem + OFF_Q1), 16, 1024) >> 32);
+        const uint32_t dq[2] = {lo(smem_desc_sw128(smem_u32(smem + OFF_Q1), 16, 1024)),
+                                lo(smem_desc_sw128(smem_u32(smem + OFF_Q2), 16, 1024))};
+        const uint32_t dk[2] = {
+            lo(smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K1), 16, 1024)),
+            lo(smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_K2), 16, 1024))};
+        const uint32_t dvb =
+            lo(smem_desc_sw128(smem_u32(smem + OFF_STAGES + STAGE_V), TILE_QK_BYTES, 1024));
         auto qk = [&](int k, int s) {  // S_k = Q_k K_k^T, K from stage s; K slices of 32 bytes
           if (kFp8) {
             // e4m3 rows of 64 bytes, 64-byte swizzle (8-row atoms of 512 bytes); an
@@ -410,56 +475,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t a = smem_desc_sw64(smem_u32(smem + (k ? OFF_Q2 : OFF_Q1)));
             const uint64_t b = smem_desc_sw64(smem_u32(smem + OFF_STAGES + s * STAGE_BYTES +
                                                        (k ? STAGE_K2 : STAGE_K1)));
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < 2; ++kk)
               umma_e4m3_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK8, kk > 0);
           } else {
-            const uint64_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
-  #pragma unroll
+            const uint32_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
+#pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
-              umma_bf16_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK, kk > 0);
+              umma_bf16_ss_lo(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, dhi, IDESC_QK, kk > 0);
           }
         };
         auto pv = [&](int k, int s, bool accumulate) {  // O_k += P_k V; 16 keys = 2048 bytes
-          const uint64_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
-  #pragma unroll
+          const uint32_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
+#pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_bf16_ts(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, b + 128 * kk, IDESC_PV,
-                         (accumulate || kk > 0) ? 1u : 0u);
+            umma_bf16_ts_lo(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, b + 128 * kk, dhi, IDESC_PV,
+                            (accumulate || kk > 0) ? 1u : 0u);
         };
-        bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag, WAIT_TIMEOUT_NS);
-        tc_fence_after_sync();
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int s = j % STAGES;
-          const uint32_t ph = static_cast<uint32_t>(j / STAGES) & 1;
-          if (!(ok = mbar_wait(&ctrl->k_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+        bool ok = true;
+        uint32_t g = 0;  // key tiles processed so far
+        Item it;
+        for (uint32_t r = 0; ok && next_item<kPartial>(p, r, it); ++r) {
+          if (!(ok = mbar_wait(&ctrl->q_full, r & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
           tc_fence_after_sync();
-          qk(0, s);
-          umma_commit(&ctrl->s_full[0]);
-          if (j > 0) {
-            if (!(ok = mbar_wait(&ctrl->p_ready[1], (j - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+          for (int j = 0; j < it.n_kv; ++j, ++g) {
+            const int s = static_cast<int>(g % STAGES);
+            const uint32_t ph = (g / STAGES) & 1;
+            if (!(ok = mbar_wait(&ctrl->k_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+            tc_fence_after_sync();
+            qk(0, s);
+            umma_commit(&ctrl->s_full[0]);
+            if (j > 0) {
+              if (!(ok = mbar_wait(&ctrl->p_ready[1], (g - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+                break;
+              tc_fence_after_sync();
+              const int sp = static_cast<int>((g - 1) % STAGES);
+              pv(1, sp, j - 1 > 0);
+              umma_commit(&ctrl->kv_empty[sp]);
+            }
+            qk(1, s);
+            umma_commit(&ctrl->s_full[1]);
+            if (j == it.n_kv - 1) umma_commit(&ctrl->q_empty);  // last use of this item's Q
+            if (!(ok = mbar_wait(&ctrl->v_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+            if (!(ok = mbar_wait(&ctrl->p_ready[0], g & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+            // The first P V of an item overwrites O: the previous item's epilogue
+            // must have read it.
+            if (j == 0 && r > 0 &&
+                !(ok = mbar_wait(&ctrl->o_free, (r - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
               break;
             tc_fence_after_sync();
-            const int sp = (j - 1) % STAGES;
-            pv(1, sp, j - 1 > 0);
-            umma_commit(&ctrl->kv_empty[sp]);
+            pv(0, s, j > 0);
           }
-          qk(1, s);
-          umma_commit(&ctrl->s_full[1]);
-          if (!(ok = mbar_wait(&ctrl->v_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
-          if (!(ok = mbar_wait(&ctrl->p_ready[0], j & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+          if (!ok) break;
+          const uint32_t gl = g - 1;  // the item's last key tile
+          if (!(ok = mbar_wait(&ctrl->p_ready[1], gl & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
           tc_fence_after_sync();
-          pv(0, s, j > 0);
-        }
-        if (ok && n_kv > 0) {
-          const int jl = n_kv - 1;
-          if (mbar_wait(&ctrl->p_ready[1], jl & 1, abort_flag, WAIT_TIMEOUT_NS)) {
-            tc_fence_after_sync();
-            const int sl = jl % STAGES;
-            pv(1, sl, jl > 0);
-            umma_commit(&ctrl->kv_empty[sl]);
-            umma_commit(&ctrl->o_done);
-          }
+          const int sl = static_cast<int>(gl % STAGES);
+          pv(1, sl, it.n_kv > 1);
+          umma_commit(&ctrl->kv_empty[sl]);
+          umma_commit(&ctrl->o_done);
         }
         // Never free tensor memory under a running MMA: wait for all of them.
         umma_commit(&ctrl->drain);
@@ -476,169 +550,122 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t t_s = tmem + lane_addr + tm_s(k);
     const uint32_t t_o = tmem + lane_addr + tm_o(k);
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY;  // reference maximum (log2 units) used by the exponentials
-    float l_run = 0.f;        // running sum of exp2(x - m_run)
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = mbar_wait(&ctrl->s_full[k], j & 1, abort_flag, WAIT_TIMEOUT_NS);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
-      // Key column c of this tile is visible to this row iff c <= lim.
-      const int kv0 = (kv_lo + j) * BN;
-      const int lim = p.causal ? (p.q_off + q0 + r - kv0) : (p.N_kv - 1 - kv0);
-      const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
-      uint32_t pk[BN / 2];
-      float tile_sum = 0.f;
-      // Steady state: exponentials against the current reference maximum; the
-      // row sum bounds every entry, so sum <= 2^8 certifies that no P exceeds
-      // 2^8 and the maximum is never computed.  Otherwise (and on the first
-      // tile) the exact path below recomputes the tile from S, which is still
-      // intact in TMEM because P is only stored once certified.
-      bool exact = (j == 0);
-      if (!exact) {
-        tile_sum = masked ? softmax_tile_exp<true>(t_s, m_run, sl2, lim, pk)
-                          : softmax_tile_exp<false>(t_s, m_run, sl2, lim, pk);
-        exact = __any_sync(0xffffffffu, !(tile_sum <= 256.f));
-      }
-      if (exact) {
-        const float mt = masked ? softmax_tile_max<true>(t_s, lim) : softmax_tile_max<false>(t_s, lim);
-        // A row can see no key at all in the first tile of a split key range
-        // (mt = -inf); it then keeps m = -inf, its p are 0 and the next tile
-        // rescales by 2^-inf = 0.
-        const float m_new = fmaxf(m_run, mt * sl2);
-        float alpha = 1.f;
-        if (j == 0) {
-          m_run = m_new;
-        } else if (m_new > m_run + RESCALE_THRESHOLD) {
-          alpha = ex2_approx(m_run - m_new);
-          m_run = m_new;
+    float *xch = ctrl->xch;  // [2][BM]: per-row values of both maps
+    uint32_t g = 0;  // key tiles processed so far
+    for (uint32_t ri = 0;; ++ri) {
+      Item it;
+      if (!next_item<kPartial>(p, ri, it)) break;
+      const int n_kv = it.n_kv;
+      // Key column c of tile j is visible to this row iff c <= lim0 - 128 j.
+      const int kv_first = kPartial ? it.kv_lo * BN : 0;
+      const int lim0 = p.causal ? (p.q_off + it.q0 + r - kv_first) : (p.N_kv - 1 - kv_first);
+      float m_run = -INFINITY;  // reference maximum (log2 units) used by the exponentials
+      float l_run = 0.f;        // running sum of exp2(x - m_run)
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j, ++g) {
+        ok = mbar_wait(&ctrl->s_full[k], g & 1, abort_flag, WAIT_TIMEOUT_NS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const int lim = lim0 - j * BN;
+        const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
+        uint32_t pk[BN / 2];
+        float tile_sum = 0.f;
+        // Steady state: exponentials against the current reference maximum; the
+        // row sum bounds every entry, so sum <= 2^8 certifies that no P exceeds
+        // 2^8 and the maximum is never computed.  Otherwise (and on the first
+        // tile) the exact path below recomputes the tile from S, which is still
+        // intact in TMEM because P is only stored once certified.
+        bool exact = (j == 0);
+        if (!exact) {
+          tile_sum = masked ? softmax_tile_exp<true>(t_s, m_run, sl2, lim, pk)
+                            : softmax_tile_exp<false>(t_s, m_run, sl2, lim, pk);
+          exact = __any_sync(0xffffffffu, !(tile_sum <= 256.f));
         }
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          // O_k of this row is complete up to tile j-1 (certified by s_full).
+        if (exact) {
+          const float mt =
+              masked ? softmax_tile_max<true>(t_s, lim) : softmax_tile_max<false>(t_s, lim);
+          // A row can see no key at all in the first tile of a split key range
+          // (mt = -inf); it then keeps m = -inf, its p are 0 and the next tile
+          // rescales by 2^-inf = 0.
+          const float m_new = fmaxf(m_run, mt * sl2);
+          float alpha = 1.f;
+          if (j == 0) {
+            m_run = m_new;
+          } else if (m_new > m_run + RESCALE_THRESHOLD) {
+            alpha = ex2_approx(m_run - m_new);
+            m_run = m_new;
+          }
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            // O_k of this row is complete up to tile j-1 (certified by s_full).
 #pragma unroll 1
-          for (int c0 = 0; c0 < DV; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(t_o + c0, o);
+            for (int c0 = 0; c0 < DV; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(t_o + c0, o);
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float2 v = __fmul2_rn(
-                  make_float2(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
-                  make_float2(alpha, alpha));
-              o[c] = __float_as_uint(v.x);
-              o[c + 1] = __float_as_uint(v.y);
+              for (int c = 0; c < 32; c += 2) {
+                const float2 v = __fmul2_rn(
+                    make_float2(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
+                    make_float2(alpha, alpha));
+                o[c] = __float_as_uint(v.x);
+                o[c + 1] = __float_as_uint(v.y);
+              }
+              tmem_st_x32(t_o + c0, o);
             }
-            tmem_st_x32(t_o + c0, o);
           }
+          l_run *= alpha;
+          const float m_use = m_run == -INFINITY ? 0.f : m_run;
+          tile_sum = masked ? softmax_tile_exp<true>(t_s, m_use, sl2, lim, pk)
+                            : softmax_tile_exp<false>(t_s, m_use, sl2, lim, pk);
         }
-        l_run *= alpha;
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        tile_sum = masked ? softmax_tile_exp<true>(t_s, m_use, sl2, lim, pk)
-                          : softmax_tile_exp<false>(t_s, m_use, sl2, lim, pk);
-      }
-      l_run += tile_sum;
-      // P_k as packed bf16 pairs over the first 64 columns of S_k.
+        l_run += tile_sum;
+        // P_k as packed bf16 pairs over the first 64 columns of S_k.
 #pragma unroll
-      for (int c0 = 0; c0 < BN / 2; c0 += 16) {
-        uint32_t part[16];
+        for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+          uint32_t part[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) part[c] = pk[c0 + c];
-        tmem_st_x16(t_s + c0, part);
+          for (int c = 0; c < 16; ++c) part[c] = pk[c0 + c];
+          tmem_st_x16(t_s + c0, part);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&ctrl->p_ready[k]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&ctrl->p_ready[k]);
-    }
 
-    // ---------------------------------------------------------------- epilogue
-    if (ok) ok = mbar_wait(&ctrl->o_done, 0, abort_flag, WAIT_TIMEOUT_NS);
-    // Both warpgroups take the same branch: the barrier ORs every thread's view.
-    const bool failed = named_barrier_or(1, 256, !ok || *abort_flag != 0);
-    if (kPartial && !failed) {
-      // Split-KV partial result of this map for real query rows: O_k column-major
-      // (a warp stores 32 consecutive rows of one column), as accumulated against
-      // the reference maximum, then that maximum and the running sum.
+      // -------------------------------------------------------------- epilogue
+      if (ok) ok = mbar_wait(&ctrl->o_done, ri & 1, abort_flag, WAIT_TIMEOUT_NS);
+      // Both warpgroups take the same branch: the barrier ORs every thread's view.
+      if (named_barrier_or(1, 256, !ok || *abort_flag != 0)) break;
       tc_fence_after_sync();
-      float *blk = p.part + (item * p.splits + split) * PART_FLOATS + k * PART_MAP_FLOATS;
-      const bool real = q0 + r < p.N;
+      if (kPartial) {
+        // Split-KV partial result of this map for real query rows: O_k column-major
+        // (a warp stores 32 consecutive rows of one column), as accumulated against
+        // the reference maximum, then that maximum and the running sum.
+        float *blk = p.part + static_cast<int64_t>(blockIdx.x) * PART_FLOATS + k * PART_MAP_FLOATS;
+        const bool real = it.q0 + r < p.N;
 #pragma unroll 1
-      for (int c0 = 0; c0 < DV; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(t_o + c0, v);
-        if (real) {
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(t_o + c0, v);
+          if (real) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) blk[(c0 + c) * BM + r] = __uint_as_float(v[c]);
-        }
-      }
-      if (real) {
-        blk[PART_OFF_M + r] = m_run;
-        blk[PART_OFF_L + r] = l_run;
-      }
-    } else if (!failed) {
-      tc_fence_after_sync();
-      float *xch = reinterpret_cast<float *>(smem + OFF_Q1);  // Q tiles are dead now
-      xch[k * BM + r] = 1.f / l_run;
-      named_barrier_sync(1, 256);
-      const float inv1 = xch[r];
-      const float c2 = p.lambda[h] * xch[BM + r];
-      const int col0 = k * (DV / 2);
-      float o[64];
-      float ss = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t o1r[16], o2r[16];
-        tmem_ld_x16(tmem + lane_addr + tm_o(0) + col0 + c0, o1r);
-        tmem_ld_x16(tmem + lane_addr + tm_o(1) + col0 + c0, o2r);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          o[c0 + c] = __uint_as_float(o1r[c]) * inv1 - __uint_as_float(o2r[c]) * c2;
-          ss = fmaf(o[c0 + c], o[c0 + c], ss);
-        }
-      }
-      if (p.headnorm) {
-        if (kGroup) {  // mean-subtracting (group) form: centre the row first
-          float sm = 0.f;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sm += o[c];
-          xch[4 * BM + k * BM + r] = sm;
-          named_barrier_sync(1, 256);
-          const float mu = (xch[4 * BM + r] + xch[5 * BM + r]) * (1.f / DV);
-          ss = 0.f;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            o[c] -= mu;
-            ss = fmaf(o[c], o[c], ss);
+            for (int c = 0; c < 32; ++c) blk[(c0 + c) * BM + r] = __uint_as_float(v[c]);
           }
         }
-        xch[2 * BM + k * BM + r] = ss;
-        named_barrier_sync(1, 256);
-        const float tot = xch[2 * BM + r] + xch[3 * BM + r];
-        const float rr = rsqrtf(tot * (1.f / DV) + p.eps) * p.out_scale;
-        const float *w = p.norm_w ? p.norm_w + static_cast<int64_t>(h) * DV + col0 : nullptr;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? __ldg(w + c) : 1.f);
-      }
-      if (q0 + r < p.N) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + b_idx * p.out_sb + h * p.out_sh +
-                                               (q0 + r) * p.out_sn + col0);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          uint4 pkt;
-          pkt.x = pack_bf16x2(o[8 * v + 0], o[8 * v + 1]);
-          pkt.y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
-          pkt.z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
-          pkt.w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
-          dst[v] = pkt;
+        if (real) {
+          blk[PART_OFF_M + r] = m_run;
+          blk[PART_OFF_L + r] = l_run;
         }
+        continue;  // the only item of this CTA
       }
+      const float inv = 1.f / l_run;
       if (kSave) {
         // This map's normalised output row and its log2-sum-exp.
-        const float inv = xch[k * BM + r];
         const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BM;
-        p.save_lse[(k * p.BH + bh) * n_pad + q0 + r] = m_run + __log2f(l_run);
-        const bool real = q0 + r < p.N;
+        p.save_lse[(k * p.BH + it.bh) * n_pad + it.q0 + r] = m_run + __log2f(l_run);
+        const bool real = it.q0 + r < p.N;
         float4 *dst = reinterpret_cast<float4 *>(
-            p.save_o + ((k * p.BH + bh) * p.N + (real ? q0 + r : 0)) * DV);
+            p.save_o + ((k * p.BH + it.bh) * p.N + (real ? it.q0 + r : 0)) * DV);
 #pragma unroll 1
         for (int c0 = 0; c0 < DV; c0 += 32) {
           uint32_t v[32];
@@ -653,6 +680,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+      xch[k * BM + r] = inv;
+      named_barrier_sync(1, 256);
+      const float inv1 = xch[r];
+      const float c2 = p.lambda[it.h] * xch[BM + r];
+      const int col0 = k * (DV / 2);
+      float o[64];
+      float ss = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        uint32_t o1r[16], o2r[16];
+        tmem_ld_x16(tmem + lane_addr + tm_o(0) + col0 + c0, o1r);
+        tmem_ld_x16(tmem + lane_addr + tm_o(1) + col0 + c0, o2r);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          o[c0 + c] = __uint_as_float(o1r[c]) * inv1 - __uint_as_float(o2r[c]) * c2;
+          ss = fmaf(o[c0 + c], o[c0 + c], ss);
+        }
+      }
+      // O1 and O2 are in registers: the next item's P V may overwrite them.
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->o_free);
+      if (p.headnorm) {
+        named_barrier_sync(1, 256);  // both maps have read the 1/l exchange
+        if (kGroup) {  // mean-subtracting (group) form: centre the row first
+          float sm = 0.f;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sm += o[c];
+          xch[k * BM + r] = sm;
+          named_barrier_sync(1, 256);
+          const float mu = (xch[r] + xch[BM + r]) * (1.f / DV);
+          named_barrier_sync(1, 256);  // both maps have read the sums
+          ss = 0.f;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            o[c] -= mu;
+            ss = fmaf(o[c], o[c], ss);
+          }
+        }
+        xch[k * BM + r] = ss;
+        named_barrier_sync(1, 256);
+        const float tot = xch[r] + xch[BM + r];
+        const float rr = rsqrtf(tot * (1.f / DV) + p.eps) * p.out_scale;
+        const float *w = p.norm_w ? p.norm_w + static_cast<int64_t>(it.h) * DV + col0 : nullptr;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? __ldg(w + c) : 1.f);
+      }
+      if (it.q0 + r < p.N) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + it.b * p.out_sb + it.h * p.out_sh +
+                                               (it.q0 + r) * p.out_sn + col0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint4 pkt;
+          pkt.x = pack_bf16x2(o[8 * v + 0], o[8 * v + 1]);
+          pkt.y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
+          pkt.z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
+          pkt.w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
+          dst[v] = pkt;
+        }
+      }
+      // The exchange slots are written again by the next item only after a
+      // barrier that both warpgroups reach once done reading here.
+      named_barrier_sync(1, 256);
     }
   }
 
@@ -775,6 +864,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.q_off = static_cast<int32_t>(n_kv - N);
   p.n_qtiles = static_cast<int32_t>(n_qtiles);
   p.n_ktiles = static_cast<int32_t>(n_ktiles);
+  p.n_items = static_cast<uint32_t>(BH * n_qtiles);
   p.causal = desc.causal ? 1 : 0;
   p.headnorm = desc.headnorm ? 1 : 0;  // the form is the kGroup instantiation
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
@@ -793,7 +883,16 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.out_sn = st[5].n;
   p.save_lse = save ? save + 2 * BH * N * DV : nullptr;
 
-  dim3 grid(static_cast<unsigned>(BH * n_qtiles * splits));
+  // Split-KV: one CTA per (query tile, key range).  Otherwise persistent: one
+  // CTA per SM at most (one fits, by shared and tensor memory), each walking
+  // its share of the items.
+  static int sms[64] = {0};
+  if (sms[dev] == 0 &&
+      cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DIFFATTN_ERR_CUDA;
+  const int64_t items = BH * n_qtiles;
+  if (items == 0) return DIFFATTN_OK;
+  dim3 grid(static_cast<unsigned>(splits > 1 ? items * splits : std::min<int64_t>(items, sms[dev])));
   if (fp8)
     diffattn_fwd_bf16_sm103_kernel<false, false, false, true>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
