@@ -66,7 +66,9 @@ diffattn_status plan_kv(const diffattn_desc *desc, int64_t n_kv, int splits, int
   if (st != DIFFATTN_OK) return st;
   if (n_kv < 0 || splits < 0 || splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
   if (desc->causal && n_kv < desc->N) return DIFFATTN_ERR_INVALID_ARG;
-  if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if ((desc->dtype != DIFFATTN_BF16 && desc->dtype != DIFFATTN_E4M3_QK) || desc->d != 64)
+    return DIFFATTN_ERR_UNSUPPORTED;
+  if (desc->dtype == DIFFATTN_E4M3_QK && desc->headnorm == 2) return DIFFATTN_ERR_UNSUPPORTED;
   const int64_t BH = desc->B * desc->H;
   if (BH * desc->N == 0) {
     *splits_out = 1;

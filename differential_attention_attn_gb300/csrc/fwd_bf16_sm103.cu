@@ -323,7 +323,7 @@ __device__ __forceinline__ bool next_item(const Params &p, uint32_t r, Item &it)
 // states to p.part, no epilogue); otherwise the whole forward of a query tile.
 // kSave (with !kPartial): also store the activations the backward pass needs.
 // kGroup (with !kPartial): the head norm is the mean-subtracting form.
-// kFp8 (single pass only): q1, k1, q2, k2 are e4m3 (one byte per element, 64-byte
+// kFp8: q1, k1, q2, k2 are e4m3 (one byte per element, 64-byte
 // rows with 64-byte swizzle in the same shared-memory slots); S is computed by
 // kind::f8f6f4 MMAs, everything from P on is unchanged.
 template <bool kPartial, bool kSave, bool kGroup, bool kFp8>
@@ -808,8 +808,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   const bool fp8 = desc.dtype == DIFFATTN_E4M3_QK;
   if (splits < 1 || (splits > 1 && part == nullptr) || (splits > 1 && save != nullptr))
     return DIFFATTN_ERR_INVALID_ARG;
-  if (fp8 && (splits > 1 || save != nullptr || desc.headnorm == 2))
-    return DIFFATTN_ERR_UNSUPPORTED;
+  if (fp8 && (save != nullptr || desc.headnorm == 2)) return DIFFATTN_ERR_UNSUPPORTED;
   const int64_t split_tiles = (n_ktiles + splits - 1) / splits;
   if (BH * n_qtiles * splits > INT32_MAX || N > INT32_MAX / 2 || n_kv > INT32_MAX / 2 ||
       desc.H > INT32_MAX)
@@ -842,6 +841,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
     auto *k2 = diffattn_fwd_bf16_sm103_kernel<false, true, false, false>;
     auto *k3 = diffattn_fwd_bf16_sm103_kernel<false, false, true, false>;
     auto *k4 = diffattn_fwd_bf16_sm103_kernel<false, false, false, true>;
+    auto *k5 = diffattn_fwd_bf16_sm103_kernel<true, false, false, true>;
     if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
         cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -851,6 +851,8 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
         cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
         cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(k5, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
     attr_set[dev] = true;
@@ -893,7 +895,10 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   const int64_t items = BH * n_qtiles;
   if (items == 0) return DIFFATTN_OK;
   dim3 grid(static_cast<unsigned>(splits > 1 ? items * splits : std::min<int64_t>(items, sms[dev])));
-  if (fp8)
+  if (fp8 && splits > 1)
+    diffattn_fwd_bf16_sm103_kernel<true, false, false, true>
+        <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  else if (fp8)
     diffattn_fwd_bf16_sm103_kernel<false, false, false, true>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else if (splits > 1)

@@ -242,29 +242,40 @@ def fwd_kv_plan(B, H, N, n_kv, *, causal: bool, splits: int = 0, d: int = 64,
     return sp.value, nb.value
 
 
+def _kv_dtypes(q1):
+    """(dtype code, value and output dtype) of a key/value-cache call: bf16
+    throughout, or e4m3 queries/keys (DIFFATTN_E4M3_QK) with bf16 values and output."""
+    if q1.dtype == torch.float8_e4m3fn:
+        return E4M3_QK, torch.bfloat16
+    return _DTYPE_CODE.get(q1.dtype, -1), q1.dtype
+
+
 def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_w=None,
            eps: float = 1e-5, lambda_init: float = 0.0, splits: int = 0, workspace=None,
            out=None, status=None, stream=None, raw_status: bool = False):
-    """Forward of Nq queries against Nkv keys through `diffattn_fwd_kv` (bf16, d = 64).
+    """Forward of Nq queries against Nkv keys through `diffattn_fwd_kv` (d = 64).
 
     q1, q2: [B, H, Nq, 64]; k1, k2: [B, H, Nkv, 64]; v: [B, H, Nkv, 128]; the
-    queries are the last Nq positions.  splits = 0 lets the library choose.
-    workspace: a CUDA tensor of at least the planned bytes, or None (a torch
-    buffer of the planned size is used).  Returns out [B, H, Nq, 128].
+    queries are the last Nq positions.  All bf16, or q1, k1, q2, k2
+    float8_e4m3fn with bf16 v (DIFFATTN_E4M3_QK).  splits = 0 lets the library
+    choose.  workspace: a CUDA tensor of at least the planned bytes, or None (a
+    torch buffer of the planned size is used).  Returns bf16 out [B, H, Nq, 128].
     """
     if q1.dim() != 4 or k1.dim() != 4:
         raise ValueError("q1 and k1 must be [B, H, N, d]")
     B, H, N, d = q1.shape
     n_kv = k1.shape[2]
-    dtype = q1.dtype
-    for name, t, shape in (("q2", q2, (B, H, N, d)), ("k1", k1, (B, H, n_kv, d)),
-                           ("k2", k2, (B, H, n_kv, d)), ("v", v, (B, H, n_kv, 2 * d))):
-        if tuple(t.shape) != shape or t.dtype != dtype:
-            raise ValueError(f"{name} must be {shape} {dtype}")
+    code, vdtype = _kv_dtypes(q1)
+    for name, t, shape, dt in (("q2", q2, (B, H, N, d), q1.dtype),
+                               ("k1", k1, (B, H, n_kv, d), q1.dtype),
+                               ("k2", k2, (B, H, n_kv, d), q1.dtype),
+                               ("v", v, (B, H, n_kv, 2 * d), vdtype)):
+        if tuple(t.shape) != shape or t.dtype != dt:
+            raise ValueError(f"{name} must be {shape} {dt}")
     if out is None:
-        out = torch.empty((B, H, N, 2 * d), dtype=dtype, device=q1.device)
-    if tuple(out.shape) != (B, H, N, 2 * d) or out.dtype != dtype:
-        raise ValueError("out must be [B, H, Nq, 2d] of the input dtype")
+        out = torch.empty((B, H, N, 2 * d), dtype=vdtype, device=q1.device)
+    if tuple(out.shape) != (B, H, N, 2 * d) or out.dtype != vdtype:
+        raise ValueError(f"out must be [B, H, Nq, 2d] {vdtype}")
     tensors = [q1, k1, q2, k2, v, lam, out] + ([norm_w] if norm_w is not None else [])
     for t in tensors:
         if not t.is_cuda or not t.is_contiguous():
@@ -273,8 +284,7 @@ def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_
         raise ValueError("lam must be float32 [H]")
     if norm_w is not None and (norm_w.dtype != torch.float32 or norm_w.numel() != H * 2 * d):
         raise ValueError("norm_w must be float32 [H, 2d]")
-    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(dtype, -1), causal, headnorm, eps, lambda_init,
-                     status)
+    desc = make_desc(B, H, N, d, code, causal, headnorm, eps, lambda_init, status)
     lib = load()
     if workspace is None:
         sp, nb = ctypes.c_int(0), ctypes.c_size_t(0)
@@ -392,8 +402,9 @@ def fwd_kv_noalloc(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = Tru
     """
     B, H, N, d = q1.shape
     n_kv = k1.shape[2]
+    code, vdtype = _kv_dtypes(q1)
     if out is None:
-        out = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=q1.device)
+        out = torch.empty((B, H, N, 2 * d), dtype=vdtype, device=q1.device)
     for t in [q1, k1, q2, k2, v, lam, out] + ([norm_w] if norm_w is not None else []):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all tensors must be contiguous CUDA tensors")
@@ -401,8 +412,7 @@ def fwd_kv_noalloc(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = Tru
             tuple(v.shape) != (B, H, n_kv, 2 * d) or tuple(out.shape) != (B, H, N, 2 * d):
         raise ValueError("q1, q2 [B, H, Nq, d]; k1, k2 [B, H, Nkv, d]; v [B, H, Nkv, 2d]; "
                          "out [B, H, Nq, 2d]")
-    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
-                     lambda_init, status)
+    desc = make_desc(B, H, N, d, code, causal, headnorm, eps, lambda_init, status)
     st = load().diffattn_fwd_kv_noalloc(ctypes.byref(desc), int(n_kv), _ptr(q1), _ptr(k1),
                                         _ptr(q2), _ptr(k2), _ptr(v), _ptr(lam), _ptr(norm_w),
                                         _ptr(out), int(splits), _stream_handle(stream))

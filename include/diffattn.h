@@ -166,6 +166,8 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
  * Arguments: q1, q2 device bf16 [B, H, N, 64]; k1, k2 device bf16
  * [B, H, n_kv, 64]; v device bf16 [B, H, n_kv, 128]; out device bf16
  * [B, H, N, 128], fully overwritten; lambda and norm_w as for diffattn_fwd.
+ * With dtype DIFFATTN_E4M3_QK, q1, k1, q2, k2 are e4m3 (one byte each, same
+ * shapes) and v, out stay bf16, as for diffattn_fwd.
  * splits: 0 lets the library choose (diffattn_fwd_kv_plan reports the
  * choice), 1 is the single-pass kernel (no workspace), 2..256 cut each row's
  * keys into that many ranges of ceil(ceil(n_kv / 128) / splits) 128-key tiles
@@ -178,7 +180,8 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
  * Errors: DIFFATTN_ERR_INVALID_ARG for a negative n_kv, causal with
  * n_kv < N, n_kv = 0 with queries present, splits outside 0..256, a missing
  * or short workspace, or misaligned buffers; DIFFATTN_ERR_UNSUPPORTED unless
- * dtype is DIFFATTN_BF16 and d == 64, or on a non-sm_103 device.
+ * d == 64 and dtype is DIFFATTN_BF16, or DIFFATTN_E4M3_QK with headnorm 0 or 1,
+ * or on a non-sm_103 device.
  * B * H * N == 0 returns DIFFATTN_OK without launching anything.
  */
 diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const void *q1,

@@ -62,3 +62,37 @@ def test_e4m3_unsupported_modes():
     dev = [t.cuda() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
     assert ops.fwd_fp8(*dev, lam, causal=True, headnorm=2, lambda_init=li,
                        raw_status=True) == ops.ERR_UNSUPPORTED
+
+
+# diffattn_fwd_kv with e4m3 queries/keys: single pass and split-KV (partial
+# kernel + combine), against the float64 oracle on the same e4m3 values.
+@pytest.mark.parametrize("nq,nkv,splits,causal", [
+    (1, 3000, 0, True), (1, 3000, 4, True), (16, 2000, 3, True), (16, 2000, 1, True),
+    (200, 1000, 2, True), (200, 1000, 1, False), (7, 640, 5, False)])
+@pytest.mark.parametrize("headnorm", [1, 0])
+def test_e4m3_kv_matches_oracle(nq, nkv, splits, causal, headnorm):
+    w = _e4m3(W.kv_cache(970 + nq + nkv, B=1, H=4, Nq=nq, Nkv=nkv, causal=causal, layer=7))
+    w.headnorm = headnorm
+    gpu = harness.run_gpu_kv(w, splits=splits)
+    assert gpu.dtype == torch.bfloat16
+    _cmp(gpu, harness.run_oracle_kv(w),
+         f"e4m3 kv nq={nq} nkv={nkv} splits={splits} causal={causal} headnorm={headnorm}")
+
+
+def test_e4m3_kv_noalloc_equals_workspace_call():
+    w = _e4m3(W.kv_cache(985, B=1, H=8, Nq=1, Nkv=8192, causal=True, layer=12))
+    a = harness.run_gpu_kv(w, splits=4)
+    li = harness.lambda_init_for(w, "gpu")
+    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device="cuda")
+    nw = torch.tensor(w.w, dtype=torch.float32, device="cuda")
+    dev = [t.cuda() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    b = ops.fwd_kv_noalloc(*dev, lam, causal=True, headnorm=w.headnorm, norm_w=nw,
+                           lambda_init=li, eps=float(np.float32(w.eps)), splits=4)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_e4m3_kv_group_norm_unsupported():
+    w = _e4m3(W.kv_cache(986, B=1, H=2, Nq=4, Nkv=512, causal=True))
+    w.headnorm = 2
+    assert harness.run_gpu_kv(w, splits=2, raw_status=True) == ops.ERR_UNSUPPORTED
