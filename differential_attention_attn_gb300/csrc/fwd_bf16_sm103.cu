@@ -108,6 +108,7 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort;
   float xch[2 * BM];  // epilogue exchange of per-row values between the two maps
+  float w_row[DV];    // the item's head-norm weights (staged for the epilogue)
 };
 
 constexpr uint32_t SMEM_BYTES = OFF_CTRL + sizeof(Ctrl) + 1024;  // + alignment slack
@@ -559,6 +560,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Key column c of tile j is visible to this row iff c <= lim0 - 128 j.
       const int kv_first = kPartial ? it.kv_lo * BN : 0;
       const int lim0 = p.causal ? (p.q_off + it.q0 + r - kv_first) : (p.N_kv - 1 - kv_first);
+      // The epilogue's per-head parameters, loaded now so that the key loop hides
+      // their latency: lambda_h, and one head-norm weight per thread (threads
+      // 0-63 of each map's warpgroup cover that map's 64 output columns).
+      const float lam_h = kPartial ? 0.f : __ldg(p.lambda + it.h);
+      const bool w_mine = !kPartial && p.norm_w != nullptr && r < DV / 2;
+      const float w_pref = w_mine ? __ldg(p.norm_w + static_cast<int64_t>(it.h) * DV + k * (DV / 2) + r) : 1.f;
       float m_run = -INFINITY;  // reference maximum (log2 units) used by the exponentials
       float l_run = 0.f;        // running sum of exp2(x - m_run)
       bool ok = true;
@@ -659,6 +666,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;  // the only item of this CTA
       }
       const float inv = 1.f / l_run;
+      if (w_mine) ctrl->w_row[k * (DV / 2) + r] = w_pref;  // read after the barriers below
       if (kSave) {
         // This map's normalised output row and its log2-sum-exp.
         const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BM;
@@ -683,7 +691,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       xch[k * BM + r] = inv;
       named_barrier_sync(1, 256);
       const float inv1 = xch[r];
-      const float c2 = p.lambda[it.h] * xch[BM + r];
+      const float c2 = lam_h * xch[BM + r];
       const int col0 = k * (DV / 2);
       float o[64];
       float ss = 0.f;
@@ -722,9 +730,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         named_barrier_sync(1, 256);
         const float tot = xch[r] + xch[BM + r];
         const float rr = rsqrtf(tot * (1.f / DV) + p.eps) * p.out_scale;
-        const float *w = p.norm_w ? p.norm_w + static_cast<int64_t>(it.h) * DV + col0 : nullptr;
+        const float *w = p.norm_w ? ctrl->w_row + col0 : nullptr;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? __ldg(w + c) : 1.f);
+        for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? w[c] : 1.f);
       }
       if (it.q0 + r < p.N) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.out + it.b * p.out_sb + it.h * p.out_sh +
