@@ -747,9 +747,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           dst[v] = pkt;
         }
       }
-      // The exchange slots are written again by the next item only after a
-      // barrier that both warpgroups reach once done reading here.
-      named_barrier_sync(1, 256);
+      // No barrier is needed before the next item writes xch and w_row again:
+      // that happens after its o_done, which needs the other map's P for its
+      // last key tile, which that map's threads produce only after finishing
+      // their reads here.
     }
   }
 
