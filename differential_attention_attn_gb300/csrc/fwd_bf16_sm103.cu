@@ -748,9 +748,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       // No barrier is needed before the next item writes xch and w_row again:
-      // that happens after its o_done, which needs the other map's P for its
-      // last key tile, which that map's threads produce only after finishing
-      // their reads here.
+      // its epilogue starts with the OR barrier of both warpgroups, which no
+      // thread passes before every thread has finished its reads here.
     }
   }
 
