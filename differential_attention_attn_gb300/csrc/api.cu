@@ -131,7 +131,8 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
                                      const diffattn_strides *strides, void *stream) {
   diffattn_status st = check_desc(desc);
   if (st != DIFFATTN_OK) return st;
-  if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (desc->dtype != DIFFATTN_BF16 || (desc->d != 64 && desc->d != 128))
+    return DIFFATTN_ERR_UNSUPPORTED;
   if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
   if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out || !strides)
     return DIFFATTN_ERR_INVALID_ARG;
@@ -145,6 +146,9 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
   }
   if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  if (desc->d == 128)
+    return launch_fwd_d128_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w, out,
+                                 static_cast<cudaStream_t>(stream), strides);
   return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
                                static_cast<cudaStream_t>(stream), 1, nullptr, nullptr, strides);
 }

@@ -94,6 +94,7 @@ struct Params {
   const float *norm_w;
   __nv_bfloat16 *out;
   int32_t *status;
+  int64_t out_sb, out_sh, out_sn;  // element strides of `out` (rows of 256 contiguous)
 };
 
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -443,7 +444,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool real = qpos < p.N;
       const float *w = (p.headnorm && p.norm_w) ? p.norm_w + static_cast<int64_t>(h) * DV + 128 * g
                                                 : nullptr;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + (bh * p.N + (real ? qpos : 0)) * DV +
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + b_idx * p.out_sb + h * p.out_sh +
+                                             static_cast<int64_t>(real ? qpos : 0) * p.out_sn +
                                              128 * g);
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -485,10 +487,10 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// 4-D view {width, N, H, B} of a contiguous [B, H, N, width] bf16 tensor; boxes
-// of `rows` rows x 64 columns, 128-byte swizzle.
+// 4-D view {width, N, H, B} of a bf16 tensor with element strides (sn, sh, sb)
+// and contiguous rows; boxes of `rows` rows x 64 columns, 128-byte swizzle.
 CUresult encode_map(CUtensorMap *map, const void *base, uint64_t width, uint64_t N, uint64_t H,
-                    uint64_t B, uint32_t rows) {
+                    uint64_t B, uint32_t rows, const diffattn_strides &st) {
   static EncodeTiledFn fn = [] {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -500,7 +502,8 @@ CUresult encode_map(CUtensorMap *map, const void *base, uint64_t width, uint64_t
   }();
   if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t dims[4] = {width, N, H, B};
-  cuuint64_t strides[3] = {width * 2, width * 2 * N, width * 2 * N * H};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                           static_cast<cuuint64_t>(st.b) * 2};
   cuuint32_t box[4] = {64, rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
@@ -513,20 +516,26 @@ CUresult encode_map(CUtensorMap *map, const void *base, uint64_t width, uint64_t
 diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
                                       const void *q2, const void *k2, const void *v,
                                       const float *lambda, const float *norm_w, void *out,
-                                      cudaStream_t stream) {
+                                      cudaStream_t stream, const diffattn_strides *strides) {
   const int64_t BH = desc.B * desc.H, N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
   const int64_t n_ktiles = (N + BN - 1) / BN;
   if (BH * n_qtiles > INT32_MAX || N > INT32_MAX / 2 || desc.B > INT32_MAX ||
       desc.H > INT32_MAX)
     return DIFFATTN_ERR_UNSUPPORTED;
+  // Element strides of q1, k1, q2, k2, v, out: given, or contiguous [B, H, N, width].
+  diffattn_strides st[6];
+  for (int i = 0; i < 6; ++i) {
+    const int64_t width = (i >= 4) ? DV : HD;
+    st[i] = strides ? strides[i] : diffattn_strides{desc.H * N * width, N * width, width};
+  }
   CUtensorMap maps[5];
   const void *bases[5] = {q1, k1, q2, k2, v};
   for (int i = 0; i < 5; ++i) {
     const uint64_t width = (i == 4) ? DV : HD;
     const uint32_t rows = 128;
     if (encode_map(&maps[i], bases[i], width, static_cast<uint64_t>(N),
-                   static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B), rows) !=
+                   static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B), rows, st[i]) !=
         CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
@@ -556,6 +565,9 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1,
   p.norm_w = norm_w;
   p.out = static_cast<__nv_bfloat16 *>(out);
   p.status = desc.status_dev;
+  p.out_sb = st[5].b;
+  p.out_sh = st[5].h;
+  p.out_sn = st[5].n;
   dim3 grid(static_cast<unsigned>(BH * n_qtiles));
   diffattn_fwd_d128_sm103_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
       maps[0], maps[1], maps[2], maps[3], maps[4], p);

@@ -105,7 +105,8 @@ typedef struct diffattn_desc {
  *     k1, q2, k2, v must be 16-byte aligned (DIFFATTN_ERR_INVALID_ARG
  *     otherwise).  Runs a fused tcgen05/TMEM/TMA kernel (for d == 128 a
  *     two-pass one: row statistics, then a single normalised accumulator);
- *     needs an sm_103 device.  The other entry points take d == 64 only.
+ *     needs an sm_103 device.  diffattn_fwd_strided takes both head widths;
+ *     the other entry points take d == 64 only.
  *   - DIFFATTN_F32: 1 <= d <= 128, N <= 4096.  Plain CUDA-core kernel
  *     (accurate expf, fp32 accumulation).
  *   - DIFFATTN_E4M3_QK: d == 64, headnorm 0 or 1: the d == 64 kernel with the
@@ -138,8 +139,8 @@ typedef struct diffattn_strides {
  * strides[0..5] are those of q1, k1, q2, k2, v, out, in elements.  Rows must
  * be contiguous; every stride must be a positive multiple of 8 elements (16
  * bytes, the tensor-copy engine's rule) and below 2^39.  Domain: DIFFATTN_BF16,
- * d == 64, any N >= 1, headnorm 0, 1 or 2, 16-byte aligned bases, an sm_103
- * device; anything else returns an error before launching.
+ * d == 64 or d == 128, any N >= 1, headnorm 0, 1 or 2, 16-byte aligned bases,
+ * an sm_103 device; anything else returns an error before launching.
  */
 diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, const void *k1,
                                      const void *q2, const void *k2, const void *v,

@@ -67,3 +67,23 @@ def test_strided_validation():
     assert ops.fwd_strided(q_bad, *dev[1:], lam, raw_status=True, **kw) == ops.ERR_INVALID_ARG
     with pytest.raises(ValueError):
         ops.fwd_strided(dev[0].transpose(2, 3).contiguous().transpose(2, 3), *dev[1:], lam, **kw)
+
+
+@pytest.mark.parametrize("N,causal,headnorm", [(128, True, 1), (300, True, 2), (256, False, 1),
+                                               (200, False, 0)])
+def test_d128_bnhd_layout_matches_contiguous(N, causal, headnorm):
+    """The d = 128 kernel on [B, N, H, c] storage views (value width 256), with the
+    output written into a [B, N, H, 256] view."""
+    w = W.custom(820 + N, B=2, H=2, N=N, d=128, causal=causal, headnorm=headnorm,
+                 random_w=True, layer=9)
+    dev, lam, kw = _args(w)
+    ref = ops.fwd(*dev, lam, **kw)
+    views = [_bnhd_view(t) for t in dev]
+    out_store = torch.full((2, N, 2, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = out_store.permute(0, 2, 1, 3)
+    ops.fwd_strided(*views, lam, out=out, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    oracle_out = harness.run_oracle(w)
+    err = float(np.max(np.abs(out.double().cpu().numpy() - oracle_out)))
+    assert err <= harness.bf16_tolerance(oracle_out)
