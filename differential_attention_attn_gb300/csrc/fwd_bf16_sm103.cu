@@ -275,6 +275,34 @@ __device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
   return m;
 }
 
+// Eight 16-byte chunks per lane (lane = one row of an 8-row group) transposed
+// within each group of 8 lanes: afterwards lane i holds chunk i of the group's
+// rows 0..7, so that a store per row index writes each row's 8 chunks from 8
+// adjacent lanes (128 contiguous bytes) instead of one chunk of 32 rows.  A
+// butterfly: at stage m a lane trades the 4 chunks whose index differs from its
+// lane index in bit m with lane i ^ m.
+__device__ __forceinline__ void transpose8_chunks(uint4 (&a)[8], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c & m) continue;
+      const int lo = c, hi = c | m;
+      const uint4 out = up ? a[lo] : a[hi];
+      uint4 in;
+      in.x = __shfl_xor_sync(0xffffffffu, out.x, m);
+      in.y = __shfl_xor_sync(0xffffffffu, out.y, m);
+      in.z = __shfl_xor_sync(0xffffffffu, out.z, m);
+      in.w = __shfl_xor_sync(0xffffffffu, out.w, m);
+      if (up)
+        a[lo] = in;
+      else
+        a[hi] = in;
+    }
+  }
+}
+
 // One work item: a (batch, head, 128-row query tile) and its key tiles.
 struct Item {
   int q0;       // first query row
@@ -734,18 +762,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? w[c] : 1.f);
       }
-      if (it.q0 + r < p.N) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + it.b * p.out_sb + it.h * p.out_sh +
-                                               (it.q0 + r) * p.out_sn + col0);
+      // bf16 row chunks, transposed across each 8-lane group so that every
+      // store instruction writes four 128-byte row segments (row-per-lane
+      // stores touched 32 rows each and held up the memory pipe at every item
+      // boundary).
+      uint4 pkt[8];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          uint4 pkt;
-          pkt.x = pack_bf16x2(o[8 * v + 0], o[8 * v + 1]);
-          pkt.y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
-          pkt.z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
-          pkt.w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
-          dst[v] = pkt;
-        }
+      for (int v = 0; v < 8; ++v) {
+        pkt[v].x = pack_bf16x2(o[8 * v + 0], o[8 * v + 1]);
+        pkt[v].y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
+        pkt[v].z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
+        pkt[v].w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
+      }
+      transpose8_chunks(pkt, lane);
+      const int row0 = it.q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
+      __nv_bfloat16 *obase = p.out + it.b * p.out_sb + it.h * p.out_sh + col0 + 8 * (lane & 7);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (row0 + j < p.N)
+          *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row0 + j) * p.out_sn) = pkt[j];
       }
       // No barrier is needed before the next item writes xch and w_row again:
       // its epilogue starts with the OR barrier of both warpgroups, which no
