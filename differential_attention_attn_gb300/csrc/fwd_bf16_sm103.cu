@@ -65,6 +65,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 
 #include "internal.h"
@@ -108,10 +109,11 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort;
   float xch[2 * BM];  // epilogue exchange of per-row values between the two maps
-  float w_row[DV];    // the item's head-norm weights (staged for the epilogue)
+  alignas(16) float w_row[DV];  // the item's head-norm weights (staged for the epilogue)
 };
 
 constexpr uint32_t SMEM_BYTES = OFF_CTRL + sizeof(Ctrl) + 1024;  // + alignment slack
+static_assert(offsetof(Ctrl, w_row) % 16 == 0 && OFF_CTRL % 16 == 0, "w_row is read as float4");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(OFF_STAGES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "SW128 tiles need 1 KB alignment");
 static_assert(SMEM_BYTES + 1024 < (1u << 18), "descriptor start addresses must stay below 256 KB");
@@ -758,9 +760,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         named_barrier_sync(1, 256);
         const float tot = xch[r] + xch[BM + r];
         const float rr = rsqrtf(tot * (1.f / DV) + p.eps) * p.out_scale;
-        const float *w = p.norm_w ? ctrl->w_row + col0 : nullptr;
+        if (p.norm_w != nullptr) {  // uniform: per-column weights from shared memory
+          const float4 *w4 = reinterpret_cast<const float4 *>(ctrl->w_row + col0);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) o[c] *= rr * (w ? w[c] : 1.f);
+          for (int c = 0; c < 64; c += 4) {
+            const float4 wv = w4[c / 4];
+            o[c] *= rr * wv.x;
+            o[c + 1] *= rr * wv.y;
+            o[c + 2] *= rr * wv.z;
+            o[c + 3] *= rr * wv.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) o[c] *= rr;
+        }
       }
       // bf16 row chunks, transposed across each 8-lane group so that every
       // store instruction writes four 128-byte row segments (row-per-lane
