@@ -425,15 +425,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = ctrl->tmem_base;
   // Registers move from the load/MMA warpgroup to the two softmax warpgroups:
   // 128 x REGS_CTRL + 256 x REGS_SOFTMAX stays within the 384 x 168 of the launch.
-  // (The e4m3 instantiation keeps the launch allocation: with the split, ptxas
-  // spills in it.)
+  // (The e4m3 split-KV instantiation keeps the launch allocation: with the split,
+  // ptxas spills in it.)
   static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= NUM_THREADS * 168, "register split");
+  constexpr bool kSplitRegs = !(kFp8 && kPartial);
 
   // Every role walks the same sequence of work items (next_item) and counts
   // barrier phases by item (q_full, q_empty, o_done, o_free) or by key tile
   // over all items (k_full, v_full, kv_empty per stage; s_full, p_ready).
   if (warp < 4) {
-    if (!kFp8) setmaxnreg_dec<REGS_CTRL>();  // warps 2 and 3 only give up registers
+    if (kSplitRegs) setmaxnreg_dec<REGS_CTRL>();  // warps 2 and 3 only give up registers
     if (warp == 0) {
       // ---------------------------------------------------------------- producer
       if (lane == 0) {
@@ -573,7 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
     }
   } else {
-    if (!kFp8) setmaxnreg_inc<REGS_SOFTMAX>();
+    if (kSplitRegs) setmaxnreg_inc<REGS_SOFTMAX>();
     // ---------------------------------------------------------------- softmax
     const int k = (warp - 4) / 4;          // which map
     const int r = (warp % 4) * 32 + lane;  // query row within the tile = TMEM lane
