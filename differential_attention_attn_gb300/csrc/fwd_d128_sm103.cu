@@ -441,32 +441,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           rr = rsqrtf(tss * (1.f / DV) + p.eps) * p.out_scale;
         }
       }
-      const bool real = qpos < p.N;
       const float *w = (p.headnorm && p.norm_w) ? p.norm_w + static_cast<int64_t>(h) * DV + 128 * g
                                                 : nullptr;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + b_idx * p.out_sb + h * p.out_sh +
-                                             static_cast<int64_t>(real ? qpos : 0) * p.out_sn +
-                                             128 * g);
+      // 64 columns at a time: packed to bf16, transposed across each 8-lane
+      // group (rows) so that every store instruction writes four 128-byte row
+      // segments instead of one 16-byte piece of 32 rows.
+      const int row0 = q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
+      __nv_bfloat16 *obase =
+          p.out + b_idx * p.out_sb + h * p.out_sh + 128 * g + 8 * (lane & 7);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(t_o + c0, v);  // warp-collective: every lane loads, real rows store
-        if (real) {
+      for (int c64 = 0; c64 < 128; c64 += 64) {
+        uint4 pkt[8];
+#pragma unroll
+        for (int c32 = 0; c32 < 64; c32 += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(t_o + c64 + c32, v);  // warp-collective
+          float y[32];
+          if (w != nullptr) {  // uniform
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              y[c] = (__uint_as_float(v[c]) - mu) * rr * __ldg(w + c64 + c32 + c);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) y[c] = (__uint_as_float(v[c]) - mu) * rr;
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float y[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int col = c0 + 8 * q + c;
-              y[c] = (__uint_as_float(v[8 * q + c]) - mu) * rr * (w ? __ldg(w + col) : 1.f);
-            }
-            uint4 pkt;
-            pkt.x = pack_bf16x2(y[0], y[1]);
-            pkt.y = pack_bf16x2(y[2], y[3]);
-            pkt.z = pack_bf16x2(y[4], y[5]);
-            pkt.w = pack_bf16x2(y[6], y[7]);
-            dst[c0 / 8 + q] = pkt;
+            uint4 &pk = pkt[c32 / 8 + q];
+            pk.x = pack_bf16x2(y[8 * q + 0], y[8 * q + 1]);
+            pk.y = pack_bf16x2(y[8 * q + 2], y[8 * q + 3]);
+            pk.z = pack_bf16x2(y[8 * q + 4], y[8 * q + 5]);
+            pk.w = pack_bf16x2(y[8 * q + 6], y[8 * q + 7]);
           }
+        }
+        transpose8_chunks(pkt, lane);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (row0 + j < p.N)
+            *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row0 + j) * p.out_sn + c64) =
+                pkt[j];
         }
       }
     }

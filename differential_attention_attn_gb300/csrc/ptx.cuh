@@ -376,6 +376,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Eight 16-byte chunks per lane (lane = one row of an 8-row group) transposed
+// within each group of 8 lanes: afterwards lane i holds chunk i of the group's
+// rows 0..7, so that a store per row index writes each row's 8 chunks from 8
+// adjacent lanes (128 contiguous bytes) instead of one chunk of 32 rows.  A
+// butterfly: at stage m a lane trades the 4 chunks whose index differs from its
+// lane index in bit m with lane i ^ m.
+__device__ __forceinline__ void transpose8_chunks(uint4 (&a)[8], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c & m) continue;
+      const int lo = c, hi = c | m;
+      const uint4 out = up ? a[lo] : a[hi];
+      uint4 in;
+      in.x = __shfl_xor_sync(0xffffffffu, out.x, m);
+      in.y = __shfl_xor_sync(0xffffffffu, out.y, m);
+      in.z = __shfl_xor_sync(0xffffffffu, out.z, m);
+      in.w = __shfl_xor_sync(0xffffffffu, out.w, m);
+      if (up)
+        a[lo] = in;
+      else
+        a[hi] = in;
+    }
+  }
+}
+
 // Pack two floats into bf16x2, round to nearest even: `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
