@@ -499,17 +499,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld_wait_x32(b);
         tc_fence_before_sync();
         mbar_arrive(&ctrl->dq_free);
-        const int q = q0 + kr;
-        if (q < p.N) {
-          float *row = dq_base + static_cast<int64_t>(q) * HD;
+        // dQ rows, transposed across each 8-lane group so that every vector
+        // reduction covers four 128-byte row segments (one row per lane made
+        // each instruction touch 32 rows).
+        const int row0 = q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
+        float *col_base = dq_base + 4 * (lane & 7);
 #pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            red_add_v4(row + c, __uint_as_float(a[c]) * p.scale,
-                       __uint_as_float(a[c + 1]) * p.scale, __uint_as_float(a[c + 2]) * p.scale,
-                       __uint_as_float(a[c + 3]) * p.scale);
-            red_add_v4(row + 32 + c, __uint_as_float(b[c]) * p.scale,
-                       __uint_as_float(b[c + 1]) * p.scale, __uint_as_float(b[c + 2]) * p.scale,
-                       __uint_as_float(b[c + 3]) * p.scale);
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t(&src)[32] = half ? b : a;
+          uint4 ch[8];
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            ch[v] = make_uint4(__float_as_uint(__uint_as_float(src[4 * v]) * p.scale),
+                               __float_as_uint(__uint_as_float(src[4 * v + 1]) * p.scale),
+                               __float_as_uint(__uint_as_float(src[4 * v + 2]) * p.scale),
+                               __float_as_uint(__uint_as_float(src[4 * v + 3]) * p.scale));
+          transpose8_chunks(ch, lane);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (row0 + j < p.N)
+              red_add_v4(col_base + static_cast<int64_t>(row0 + j) * HD + 32 * half,
+                         __uint_as_float(ch[j].x), __uint_as_float(ch[j].y),
+                         __uint_as_float(ch[j].z), __uint_as_float(ch[j].w));
           }
         }
       }
