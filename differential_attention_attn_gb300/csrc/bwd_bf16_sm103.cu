@@ -531,44 +531,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
     if (ok) {
       tc_fence_after_sync();
-      // dV columns of this group's chunks, times c (both maps add into the
-      // fp32 accumulator).
-      float *dv_row = p.dv_acc + (bh * p.N + kpos) * DV;
+      // dV times c (both maps add into the fp32 accumulator), in 32-column
+      // blocks (group 0: blocks 0-1, group 1: block 2, group 2: block 3), each
+      // transposed across 8-lane groups so that every vector reduction covers
+      // four 128-byte row segments.
+      const int blk_lo = g == 0 ? 0 : g + 1, blk_hi = g == 0 ? 2 : g + 2;
+      const int krow0 = k0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first key row
+      float *dv_col = p.dv_acc + bh * static_cast<int64_t>(p.N) * DV + 4 * (lane & 7);
 #pragma unroll 1
-      for (int c = c_lo; c < c_hi; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_addr + TM_DV + 16 * c, v);
-        tmem_wait16(v);
-        if (key_ok) {
+      for (int bk = blk_lo; bk < blk_hi; ++bk) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_addr + TM_DV + 32 * bk, v);  // warp-collective
+        uint4 ch[8];
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            red_add_v4(dv_row + 16 * c + j, coef * __uint_as_float(v[j]),
-                       coef * __uint_as_float(v[j + 1]), coef * __uint_as_float(v[j + 2]),
-                       coef * __uint_as_float(v[j + 3]));
+        for (int q = 0; q < 8; ++q)
+          ch[q] = make_uint4(__float_as_uint(coef * __uint_as_float(v[4 * q])),
+                             __float_as_uint(coef * __uint_as_float(v[4 * q + 1])),
+                             __float_as_uint(coef * __uint_as_float(v[4 * q + 2])),
+                             __float_as_uint(coef * __uint_as_float(v[4 * q + 3])));
+        transpose8_chunks(ch, lane);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (krow0 + j < p.N)
+            red_add_v4(dv_col + static_cast<int64_t>(krow0 + j) * DV + 32 * bk,
+                       __uint_as_float(ch[j].x), __uint_as_float(ch[j].y),
+                       __uint_as_float(ch[j].z), __uint_as_float(ch[j].w));
         }
       }
-      // dK 16-column chunks g and g + 3, scaled by 1/sqrt(d), stored once as bf16.
-#pragma unroll 1
-      for (int c = g; c < HD / 16; c += 3) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_addr + TM_DK + 16 * c, v);
-        tmem_wait16(v);
-        if (key_ok) {
-          uint4 *dst = reinterpret_cast<uint4 *>((map ? p.dk2 : p.dk1) + (bh * p.N + kpos) * HD +
-                                                 16 * c);
+      // dK (64 columns, by group 1), scaled by 1/sqrt(d), stored once as bf16:
+      // packed, transposed across 8-lane groups, four 128-byte row segments per
+      // store instruction.
+      if (g == 1) {
+        uint4 pkt[8];
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            uint4 pkt;
-            pkt.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * p.scale,
-                                __uint_as_float(v[8 * j + 1]) * p.scale);
-            pkt.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * p.scale,
-                                __uint_as_float(v[8 * j + 3]) * p.scale);
-            pkt.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * p.scale,
-                                __uint_as_float(v[8 * j + 5]) * p.scale);
-            pkt.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * p.scale,
-                                __uint_as_float(v[8 * j + 7]) * p.scale);
-            dst[j] = pkt;
+        for (int c32 = 0; c32 < HD; c32 += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_addr + TM_DK + c32, v);  // warp-collective
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 &pk = pkt[c32 / 8 + q];
+            pk.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * p.scale,
+                               __uint_as_float(v[8 * q + 1]) * p.scale);
+            pk.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * p.scale,
+                               __uint_as_float(v[8 * q + 3]) * p.scale);
+            pk.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * p.scale,
+                               __uint_as_float(v[8 * q + 5]) * p.scale);
+            pk.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * p.scale,
+                               __uint_as_float(v[8 * q + 7]) * p.scale);
           }
+        }
+        transpose8_chunks(pkt, lane);
+        __nv_bfloat16 *dk_col = (map ? p.dk2 : p.dk1) + bh * static_cast<int64_t>(p.N) * HD +
+                                8 * (lane & 7);
+#pragma unroll
+        for (int j2 = 0; j2 < 8; ++j2) {
+          if (krow0 + j2 < p.N)
+            *reinterpret_cast<uint4 *>(dk_col + static_cast<int64_t>(krow0 + j2) * HD) = pkt[j2];
         }
       }
     }
