@@ -674,20 +674,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // This map's normalised output row and its log2-sum-exp.
         const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BM;
         p.save_lse[(k * p.BH + it.bh) * n_pad + it.q0 + r] = m_run + __log2f(l_run);
-        const bool real = it.q0 + r < p.N;
-        float4 *dst = reinterpret_cast<float4 *>(
-            p.save_o + ((k * p.BH + it.bh) * p.N + (real ? it.q0 + r : 0)) * DV);
+        // 32 columns at a time, transposed across 8-lane groups so that every
+        // store writes four 128-byte row segments.
+        const int row0 = it.q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
+        float *so = p.save_o + (k * p.BH + it.bh) * static_cast<int64_t>(p.N) * DV + 4 * (lane & 7);
 #pragma unroll 1
         for (int c0 = 0; c0 < DV; c0 += 32) {
           uint32_t v[32];
-          tmem_ld_x32(t_o + c0, v);  // warp-collective: every lane loads, real rows store
-          if (real) {
+          tmem_ld_x32(t_o + c0, v);  // warp-collective
+          uint4 ch[8];
 #pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              dst[(c0 + c) / 4] = make_float4(__uint_as_float(v[c]) * inv,
-                                              __uint_as_float(v[c + 1]) * inv,
-                                              __uint_as_float(v[c + 2]) * inv,
-                                              __uint_as_float(v[c + 3]) * inv);
+          for (int q = 0; q < 8; ++q)
+            ch[q] = make_uint4(__float_as_uint(__uint_as_float(v[4 * q]) * inv),
+                               __float_as_uint(__uint_as_float(v[4 * q + 1]) * inv),
+                               __float_as_uint(__uint_as_float(v[4 * q + 2]) * inv),
+                               __float_as_uint(__uint_as_float(v[4 * q + 3]) * inv));
+          transpose8_chunks(ch, lane);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (row0 + j < p.N)
+              *reinterpret_cast<uint4 *>(so + static_cast<int64_t>(row0 + j) * DV + c0) = ch[j];
           }
         }
       }
