@@ -712,27 +712,43 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
 
 // ---------------------------------------------------------------- kernel 3
 // fp32 accumulators -> bf16: dq_acc [2][BH][N][64] -> dq1, dq2; dv_acc -> dv.
+// Each thread has FINISH_UNROLL 16-byte loads in flight before it stores (one
+// at a time left the copy well short of the memory bandwidth).
+constexpr int FINISH_UNROLL = 4;
 __global__ void diffattn_bwd_finish_kernel(const float *dq_acc, const float *dv_acc,
                                            __nv_bfloat16 *dq1, __nv_bfloat16 *dq2,
                                            __nv_bfloat16 *dv, int64_t n_q4, int64_t n_v4) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-       i < 2 * n_q4 + n_v4; i += stride) {
-    const float *src;
-    __nv_bfloat16 *dst;
-    int64_t j;
-    if (i < n_q4) {
-      src = dq_acc; dst = dq1; j = i;
-    } else if (i < 2 * n_q4) {
-      src = dq_acc + 4 * n_q4; dst = dq2; j = i - n_q4;
-    } else {
-      src = dv_acc; dst = dv; j = i - 2 * n_q4;
+  const int64_t total = 2 * n_q4 + n_v4;
+  auto src_of = [&](int64_t i, int64_t &j) -> const float4 * {
+    if (i < n_q4) { j = i; return reinterpret_cast<const float4 *>(dq_acc); }
+    if (i < 2 * n_q4) { j = i - n_q4; return reinterpret_cast<const float4 *>(dq_acc + 4 * n_q4); }
+    j = i - 2 * n_q4;
+    return reinterpret_cast<const float4 *>(dv_acc);
+  };
+  for (int64_t base = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; base < total;
+       base += FINISH_UNROLL * stride) {
+    float4 v[FINISH_UNROLL];
+#pragma unroll
+    for (int u = 0; u < FINISH_UNROLL; ++u) {
+      const int64_t i = base + u * stride;
+      int64_t j = 0;
+      if (i < total) v[u] = src_of(i, j)[j];
     }
-    const float4 v = reinterpret_cast<const float4 *>(src)[j];
-    uint2 o;
-    o.x = pack_bf16x2(v.x, v.y);
-    o.y = pack_bf16x2(v.z, v.w);
-    reinterpret_cast<uint2 *>(dst)[j] = o;
+#pragma unroll
+    for (int u = 0; u < FINISH_UNROLL; ++u) {
+      const int64_t i = base + u * stride;
+      if (i >= total) continue;
+      __nv_bfloat16 *dst;
+      int64_t j;
+      if (i < n_q4) { dst = dq1; j = i; }
+      else if (i < 2 * n_q4) { dst = dq2; j = i - n_q4; }
+      else { dst = dv; j = i - 2 * n_q4; }
+      uint2 o;
+      o.x = pack_bf16x2(v[u].x, v[u].y);
+      o.y = pack_bf16x2(v[u].z, v[u].w);
+      reinterpret_cast<uint2 *>(dst)[j] = o;
+    }
   }
 }
 
