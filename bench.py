@@ -184,6 +184,15 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """The job's times are its slowest rank's: the element-wise maximum of every
+    rank's values (an all-reduce when a process group is given)."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 def cpu_baseline(w, seconds: float, seed: int = 3):
     """Time the float64 oracle on a bounded, seeded sample of the workload's rows.
 
@@ -377,10 +386,7 @@ def run_decode(args):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
-    times = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_total, e2e_ms = float(times[0]), float(times[1])
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dist, dev)
     nbytes = decode_bytes(B, H, Nq, Nkv, d)
     value = world * nbytes * args.steps / (ms_total * 1e-3) / 1e9
     if rank != 0:
@@ -512,10 +518,7 @@ def run_bwd(args):
     if sampler:
         time.sleep(0.15)
         sampler.stop()
-    times = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_total = float(times[0])
+    (ms_total,) = max_over_ranks([ms_total], dist, dev)
     flops_step = alg_flops(B, H, N, d) * 20.0 / 8.0
     value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
     if rank != 0:
@@ -686,10 +689,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
 
-    times = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_total, e2e_ms = float(times[0]), float(times[1])
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dist, dev)
     flops_step = alg_flops(B, H, N, d)
     value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
     e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
