@@ -205,3 +205,33 @@ def test_strided_validation_before_launch(lib):
     arr = (ops.Strides * 6)(*good)
     assert lib.diffattn_fwd_strided(ctypes.byref(f32), f, f, f, f, f, f, None, f, arr,
                                     None) == ops.ERR_UNSUPPORTED
+
+
+def test_kv_plan_accepts_e4m3_queries_keys(lib):
+    """The key/value-cache entries take DIFFATTN_E4M3_QK (d = 64, headnorm 0 or 1):
+    the planner answers as for bf16; the group norm is refused before any launch."""
+    bf = ops.make_desc(1, 4, 512, 64, ops.BF16, True, True, 1e-5, 0.2)
+    e4 = ops.make_desc(1, 4, 512, 64, ops.E4M3_QK, True, True, 1e-5, 0.2)
+    assert _plan(lib, e4, 512, 3) == _plan(lib, bf, 512, 3)
+    dec = ops.make_desc(1, 8, 1, 64, ops.E4M3_QK, True, 0, 1e-5, 0.2)
+    assert _plan(lib, dec, 16384, 4) == (ops.OK, 4, 8 * 4 * PART_FLOATS * 4)
+    grp = ops.make_desc(1, 4, 512, 64, ops.E4M3_QK, True, 2, 1e-5, 0.2)
+    assert _plan(lib, grp, 512, 2)[0] == ops.ERR_UNSUPPORTED
+    wide = ops.make_desc(1, 4, 512, 128, ops.E4M3_QK, True, True, 1e-5, 0.2)
+    assert _plan(lib, wide, 512, 2)[0] == ops.ERR_UNSUPPORTED
+
+
+def test_strided_domain_takes_both_head_widths(lib):
+    """diffattn_fwd_strided serves d = 64 and d = 128; any other width is refused as
+    unsupported.  The accepted widths are stopped by a misaligned output pointer, the
+    next check, so nothing is ever launched whatever the machine."""
+    f = ctypes.c_void_p(FAKE)
+    misaligned = ctypes.c_void_p(FAKE + 4)
+    for d_half, ok in ((64, True), (128, True), (96, False), (32, False)):
+        desc = ops.make_desc(1, 2, 256, d_half, ops.BF16, True, 1, 1e-5, 0.2)
+        arr = (ops.Strides * 6)(*([ops.Strides(2 * 256 * d_half, 256 * d_half, d_half)] * 4 +
+                                  [ops.Strides(2 * 256 * 2 * d_half, 256 * 2 * d_half,
+                                               2 * d_half)] * 2))
+        st = lib.diffattn_fwd_strided(ctypes.byref(desc), f, f, f, f, f, f, None, misaligned,
+                                      arr, None)
+        assert st == (ops.ERR_INVALID_ARG if ok else ops.ERR_UNSUPPORTED), (d_half, st)
