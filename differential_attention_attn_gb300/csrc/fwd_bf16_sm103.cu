@@ -26,19 +26,25 @@
 // maxima and sums, so a single running (P1 - lambda P2) V cannot be
 // renormalised exactly once the final sums are known.
 //
-// Warp roles (384 threads):
+// Warp roles (640 threads):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM allocator and MMA issuer (one lane)
 //   warps 2-3   idle
-//   warps 4-7   softmax of map 1 (thread t owns query row t: TMEM lane t)
-//   warps 8-11  softmax of map 2
-// The epilogue is split by value columns: map-1 warps do columns 0-63, map-2
-// warps columns 64-127, exchanging 1/l and partial sums of squares through
-// shared memory.  Once both have read O1 and O2 into registers they release
-// them (o_free) to the next item's first P V.
+//   warps 4-11  softmax of map 1, warps 12-19 softmax of map 2
+// A softmax warp covers 16 query rows (TMEM lanes) of its warp's quarter, two
+// threads per row: lanes 0-15 take keys 0-63 of each key tile, lanes 16-31
+// keys 64-127 (the 16x32bx2 TMEM access shape).  The two threads of a row
+// agree through warp shuffles, so a row's softmax state never waits on
+// another warp, and each map's tile is spread over two warps per SM
+// sub-partition.  The epilogue gives each of a row's four threads (two maps x
+// two halves) 32 of its 128 value columns; 1/l and partial sums of squares
+// are exchanged through shared memory.  Once every thread has read O1 and O2
+// into registers they are released (o_free) to the next item's first P V.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,128) S1 (P1 as packed bf16 over its first 64 columns)
+//   [0,128) S1: P1 as packed bf16, keys 0-63 over columns 0-31 and keys
+//           64-127 over columns 64-95 (each half-row thread overwrites only
+//           the S columns it has read)
 //   [128,256) S2 (P2 likewise)   [256,384) O1   [384,512) O2
 //
 // MMA issue order per key tile j keeps the tensor pipe busy while the
@@ -49,16 +55,17 @@
 // softmax needs before it rescales O_k).  Operand descriptors are built once
 // and advanced by adding to their start-address field.
 //
-// Softmax (one thread per row, 128 key columns per tile).  Each map keeps a
-// reference maximum m (log2 units) per row and P = 2^(x - m), x = S log2(e) /
-// sqrt(d).  m is only raised when a row's maximum exceeds it by more than 2^8
-// (lazy rescaling), so in steady state a tile needs no maximum at all: the
+// Softmax (two threads per row, 64 key columns each per tile).  Each map
+// keeps a reference maximum m (log2 units) per row and P = 2^(x - m), x = S
+// log2(e) / sqrt(d).  In steady state a tile needs no maximum at all: the
 // exponentials are computed against the current m, and since every P is at
-// most the row's tile sum, a sum <= 2^8 certifies the tile.  Otherwise (and
-// on the first tile) the warp takes the exact path: the true maximum from S
-// (still intact in TMEM, because P is held in registers until certified), a
-// rescale of O_k and of the running sum when m moves, and the exponentials
-// again.  The causal/ragged mask is compiled only into the tiles that need it.
+// most its half row's sum, sums <= 2^16 certify the tile (P, O and the
+// running sums then stay far from the fp32/bf16 range limits).  Otherwise
+// (and on the first tile) the warp takes the exact path: the true maximum
+// from S (still intact in TMEM, because P is held in registers until
+// certified), m moved to it whenever it is larger, a rescale of O_k and of
+// the running sum, and the exponentials again.  The causal/ragged mask is
+// compiled only into the tiles that need it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -79,10 +86,12 @@ constexpr int BN = 128;          // keys per key tile
 constexpr int HD = 64;           // query/key half width d
 constexpr int DV = 2 * HD;       // value width 2d
 constexpr int STAGES = 3;        // K/V pipeline depth
-constexpr int NUM_THREADS = 384;
-constexpr uint32_t REGS_CTRL = 56;      // per thread, warps 0-3 (loads, MMA issue)
-constexpr uint32_t REGS_SOFTMAX = 216;  // per thread, warps 4-11 (softmax, epilogue)
-constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+constexpr int NUM_THREADS = 640;
+constexpr int SOFTMAX_THREADS = 512;    // warps 4-19
+constexpr uint32_t REGS_LAUNCH = 96;    // 65536 / 640, rounded down to a multiple of 8
+constexpr uint32_t REGS_CTRL = 64;      // per thread, warps 0-3 (loads, MMA issue)
+constexpr uint32_t REGS_SOFTMAX = 104;  // per thread, warps 4-19 (softmax, epilogue)
+constexpr float CERT_SUM = 65536.0f;    // half-row sums up to 2^16 certify a tile
 
 constexpr uint32_t TILE_QK_BYTES = BM * HD * 2;     // 16 KB: one [128 x 64] bf16 tile
 constexpr uint32_t TILE_V_BYTES = BN * DV * 2;      // 32 KB: two [128 x 64] column blocks
@@ -198,83 +207,72 @@ __device__ __forceinline__ void umma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, u
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
-// One 32-column chunk of a softmax row: mask (key column c0 + i visible iff
-// c0 + i <= lim), x = s * log2(e)/sqrt(d) - m, p = 2^x, accumulate the sum
-// in four packed partial sums and pack p as bf16 pairs into pk[c0/2 ..].
+// One 32-key chunk of a half row: mask (key key0 + i visible iff key0 + i <=
+// lim), x = s * log2(e)/sqrt(d) - m, p = 2^x, accumulate the sum in four
+// packed partial sums and pack p as bf16 pairs into pk[pk0 ..].
 template <bool kMasked>
-__device__ __forceinline__ void softmax_chunk_exp(const uint32_t (&x)[32], int c0, float m,
-                                                  float sl2, int lim, float2 (&acc)[4],
-                                                  uint32_t (&pk)[BN / 2]) {
+__device__ __forceinline__ void softmax_chunk_exp(const uint32_t (&x)[32], int key0, int pk0,
+                                                  float m, float sl2, int lim, float2 (&acc)[4],
+                                                  uint32_t (&pk)[BN / 4]) {
   const float2 scale = make_float2(sl2, sl2), negm = make_float2(-m, -m);
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
     float a = __uint_as_float(x[i]), b = __uint_as_float(x[i + 1]);
     if (kMasked) {
-      a = (c0 + i <= lim) ? a : -INFINITY;
-      b = (c0 + i + 1 <= lim) ? b : -INFINITY;
+      a = (key0 + i <= lim) ? a : -INFINITY;
+      b = (key0 + i + 1 <= lim) ? b : -INFINITY;
     }
     float2 e = __ffma2_rn(make_float2(a, b), scale, negm);
     e.x = ex2_approx(e.x);
     e.y = ex2_approx(e.y);
     acc[(i / 2) % 4] = __fadd2_rn(acc[(i / 2) % 4], e);
-    pk[(c0 + i) / 2] = pack_bf16x2(e.x, e.y);
+    pk[pk0 + i / 2] = pack_bf16x2(e.x, e.y);
   }
 }
 
-// Exponentials of a whole 128-column S row against reference maximum m; the
-// four 32-column TMEM loads are issued two ahead of their use.  Returns the
-// row sum of the (unrounded) exponentials.
+// Exponentials of this thread's 64 keys of an S row (keys key0 .. key0 + 63,
+// read through the two-threads-per-lane shape) against reference maximum m.
+// Returns the half row's sum of the (unrounded) exponentials.
 template <bool kMasked>
-__device__ __forceinline__ float softmax_tile_exp(uint32_t t_s, float m, float sl2, int lim,
-                                                  uint32_t (&pk)[BN / 2]) {
+__device__ __forceinline__ float softmax_half_exp(uint32_t t_s, int key0, float m, float sl2,
+                                                  int lim, uint32_t (&pk)[BN / 4]) {
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                    make_float2(0.f, 0.f)};
   uint32_t a[32], b[32];
-  tmem_ld_x32_nowait(t_s, a);
-  tmem_ld_x32_nowait(t_s + 32, b);
+  tmem_ld16_x32_nowait(t_s, a);
+  tmem_ld16_x32_nowait(t_s + 32, b);
   tmem_ld_wait_x32(a);
   tmem_ld_wait_x32(b);
-  softmax_chunk_exp<kMasked>(a, 0, m, sl2, lim, acc, pk);
-  tmem_ld_x32_nowait(t_s + 64, a);
-  softmax_chunk_exp<kMasked>(b, 32, m, sl2, lim, acc, pk);
-  tmem_ld_x32_nowait(t_s + 96, b);
-  tmem_ld_wait_x32(a);
-  tmem_ld_wait_x32(b);
-  softmax_chunk_exp<kMasked>(a, 64, m, sl2, lim, acc, pk);
-  softmax_chunk_exp<kMasked>(b, 96, m, sl2, lim, acc, pk);
+  softmax_chunk_exp<kMasked>(a, key0, 0, m, sl2, lim, acc, pk);
+  softmax_chunk_exp<kMasked>(b, key0 + 32, 16, m, sl2, lim, acc, pk);
   const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
   return (s01.x + s01.y) + (s23.x + s23.y);
 }
 
-// Maximum of a 128-column S row over its visible columns (tree reduction).
+// Maximum of this thread's 64 keys of an S row over the visible ones.
 template <bool kMasked>
-__device__ __forceinline__ float softmax_tile_max(uint32_t t_s, int lim) {
-  float m = -INFINITY;
+__device__ __forceinline__ float softmax_half_max(uint32_t t_s, int key0, int lim) {
+  uint32_t a[32], b[32];
+  tmem_ld16_x32_nowait(t_s, a);
+  tmem_ld16_x32_nowait(t_s + 32, b);
+  tmem_ld_wait_x32(a);
+  tmem_ld_wait_x32(b);
+  float v[64];
 #pragma unroll
-  for (int c0 = 0; c0 < BN; c0 += 64) {
-    uint32_t a[32], b[32];
-    tmem_ld_x32_nowait(t_s + c0, a);
-    tmem_ld_x32_nowait(t_s + c0 + 32, b);
-    tmem_ld_wait_x32(a);
-    tmem_ld_wait_x32(b);
-    float v[64];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = __uint_as_float(a[i]);
-      v[32 + i] = __uint_as_float(b[i]);
-    }
-    if (kMasked) {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) v[i] = (c0 + i <= lim) ? v[i] : -INFINITY;
-    }
-#pragma unroll
-    for (int w = 32; w >= 1; w /= 2) {
-#pragma unroll
-      for (int i = 0; i < w; ++i) v[i] = fmaxf(v[i], v[i + w]);
-    }
-    m = fmaxf(m, v[0]);
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(a[i]);
+    v[32 + i] = __uint_as_float(b[i]);
   }
-  return m;
+  if (kMasked) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = (key0 + i <= lim) ? v[i] : -INFINITY;
+  }
+#pragma unroll
+  for (int w = 32; w >= 1; w /= 2) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) v[i] = fmaxf(v[i], v[i + w]);
+  }
+  return v[0];
 }
 
 // One work item: a (batch, head, 128-row query tile) and its key tiles.
@@ -372,10 +370,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&ctrl->s_full[k], 1);
-      mbar_init(&ctrl->p_ready[k], BM);
+      mbar_init(&ctrl->p_ready[k], 8);  // one arrival per softmax warp of map k
     }
     mbar_init(&ctrl->o_done, 1);
-    mbar_init(&ctrl->o_free, 2 * BM);
+    mbar_init(&ctrl->o_free, SOFTMAX_THREADS / 32);  // one arrival per softmax warp
     mbar_init(&ctrl->drain, 1);
     ctrl->abort = 0;
     fence_barrier_init();
@@ -395,11 +393,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = ctrl->tmem_base;
-  // Registers move from the load/MMA warpgroup to the two softmax warpgroups:
-  // 128 x REGS_CTRL + 256 x REGS_SOFTMAX stays within the 384 x 168 of the launch.
-  // (The e4m3 split-KV instantiation keeps the launch allocation: with the split,
-  // ptxas spills in it.)
-  static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= NUM_THREADS * 168, "register split");
+  // Registers move from the load/MMA warpgroup to the four softmax warpgroups:
+  // 128 x REGS_CTRL + 512 x REGS_SOFTMAX stays within the 640 x 96 of the launch.
+  // (The e4m3 split-KV instantiation keeps the launch allocation.)
+  static_assert(128 * REGS_CTRL + SOFTMAX_THREADS * REGS_SOFTMAX <= NUM_THREADS * REGS_LAUNCH,
+                "register split");
   constexpr bool kSplitRegs = !(kFp8 && kPartial);
 
   // Every role walks the same sequence of work items (next_item) and counts
@@ -489,12 +487,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               umma_bf16_ss_lo(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, dhi, IDESC_QK, kk > 0);
           }
         };
-        auto pv = [&](int k, int s, bool accumulate) {  // O_k += P_k V; 16 keys = 2048 bytes
+        // O_k += P_k V; 16 keys = 2048 bytes of V.  P_k's keys 0-63 are packed over
+        // S_k columns 0-31 and keys 64-127 over columns 64-95.
+        auto pv = [&](int k, int s, bool accumulate) {
           const uint32_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_bf16_ts_lo(tmem + tm_o(k), tmem + tm_s(k) + kk * 8, b + 128 * kk, dhi, IDESC_PV,
-                            (accumulate || kk > 0) ? 1u : 0u);
+            umma_bf16_ts_lo(tmem + tm_o(k), tmem + tm_s(k) + kk * 8 + (kk >= 4 ? 32 : 0),
+                            b + 128 * kk, dhi, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
         };
         bool ok = true;
         uint32_t g = 0;  // key tiles processed so far
@@ -548,9 +548,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     if (kSplitRegs) setmaxnreg_inc<REGS_SOFTMAX>();
     // ---------------------------------------------------------------- softmax
-    const int k = (warp - 4) / 4;          // which map
-    const int r = (warp % 4) * 32 + lane;  // query row within the tile = TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const int sw = warp - 4;                     // softmax warp 0..15
+    const int k = sw >> 3;                       // which map
+    const int quarter = warp & 3;                // TMEM lane quarter of this warp
+    const int hl = lane & 15;                    // row within the warp's 16
+    const int hc = lane >> 4;                    // key half: keys 64 hc .. 64 hc + 63
+    const int r = quarter * 32 + ((sw >> 2) & 1) * 16 + hl;  // query row = TMEM lane
+    const int key0 = 64 * hc;
+    const uint32_t lane_addr = static_cast<uint32_t>(r - hl) << 16;
     const uint32_t t_s = tmem + lane_addr + tm_s(k);
     const uint32_t t_o = tmem + lane_addr + tm_o(k);
     const float sl2 = p.scale_log2;
@@ -564,13 +569,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kv_first = kPartial ? it.kv_lo * BN : 0;
       const int lim0 = p.causal ? (p.q_off + it.q0 + r - kv_first) : (p.N_kv - 1 - kv_first);
       // The epilogue's per-head parameters, loaded now so that the key loop hides
-      // their latency: lambda_h, and one head-norm weight per thread (threads
-      // 0-63 of each map's warpgroup cover that map's 64 output columns).
+      // their latency: lambda_h, and one head-norm weight per thread of the first
+      // four softmax warps (weight (warp % 4) * 32 + lane).
       const float lam_h = kPartial ? 0.f : __ldg(p.lambda + it.h);
-      const bool w_mine = !kPartial && p.norm_w != nullptr && r < DV / 2;
-      const float w_pref = w_mine ? __ldg(p.norm_w + static_cast<int64_t>(it.h) * DV + k * (DV / 2) + r) : 1.f;
+      const bool w_mine = !kPartial && p.norm_w != nullptr && sw < 4;
+      const float w_pref =
+          w_mine ? __ldg(p.norm_w + static_cast<int64_t>(it.h) * DV + quarter * 32 + lane) : 1.f;
       float m_run = -INFINITY;  // reference maximum (log2 units) used by the exponentials
-      float l_run = 0.f;        // running sum of exp2(x - m_run)
+      float l_run = 0.f;        // this half row's running sum of exp2(x - m_run)
       bool ok = true;
       for (int j = 0; j < n_kv; ++j, ++g) {
         ok = mbar_wait(&ctrl->s_full[k], g & 1, abort_flag, WAIT_TIMEOUT_NS);
@@ -579,22 +585,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after_sync();
         const int lim = lim0 - j * BN;
         const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
-        uint32_t pk[BN / 2];
+        uint32_t pk[BN / 4];
         float tile_sum = 0.f;
-        // Steady state: exponentials against the current reference maximum; the
-        // row sum bounds every entry, so sum <= 2^8 certifies that no P exceeds
-        // 2^8 and the maximum is never computed.  Otherwise (and on the first
+        // Steady state: exponentials against the current reference maximum; a
+        // half row's sum bounds each of its entries, so sums <= 2^16 certify the
+        // tile and the maximum is never computed.  Otherwise (and on the first
         // tile) the exact path below recomputes the tile from S, which is still
-        // intact in TMEM because P is only stored once certified.
+        // intact in TMEM because P is only stored once certified.  Both threads of
+        // a row are in this warp, so the warp-wide vote keeps them together.
         bool exact = (j == 0);
         if (!exact) {
-          tile_sum = masked ? softmax_tile_exp<true>(t_s, m_run, sl2, lim, pk)
-                            : softmax_tile_exp<false>(t_s, m_run, sl2, lim, pk);
-          exact = __any_sync(0xffffffffu, !(tile_sum <= 256.f));
+          tile_sum = masked ? softmax_half_exp<true>(t_s, key0, m_run, sl2, lim, pk)
+                            : softmax_half_exp<false>(t_s, key0, m_run, sl2, lim, pk);
+          exact = __any_sync(0xffffffffu, !(tile_sum <= CERT_SUM));
         }
         if (exact) {
-          const float mt =
-              masked ? softmax_tile_max<true>(t_s, lim) : softmax_tile_max<false>(t_s, lim);
+          float mt = masked ? softmax_half_max<true>(t_s, key0, lim)
+                            : softmax_half_max<false>(t_s, key0, lim);
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));  // the row's other half
           // A row can see no key at all in the first tile of a split key range
           // (mt = -inf); it then keeps m = -inf, its p are 0 and the next tile
           // rescales by 2^-inf = 0.
@@ -602,16 +610,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float alpha = 1.f;
           if (j == 0) {
             m_run = m_new;
-          } else if (m_new > m_run + RESCALE_THRESHOLD) {
+          } else if (m_new > m_run) {  // move m whenever the tile exceeds it
             alpha = ex2_approx(m_run - m_new);
             m_run = m_new;
           }
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            // O_k of this row is complete up to tile j-1 (certified by s_full).
+            // O_k of this row is complete up to tile j-1 (certified by s_full);
+            // each thread rescales its 64 of the 128 columns.
 #pragma unroll 1
-            for (int c0 = 0; c0 < DV; c0 += 32) {
+            for (int c0 = 0; c0 < DV / 2; c0 += 32) {
               uint32_t o[32];
-              tmem_ld_x32(t_o + c0, o);
+              tmem_ld16_x32(t_o + c0, o);
 #pragma unroll
               for (int c = 0; c < 32; c += 2) {
                 const float2 v = __fmul2_rn(
@@ -620,68 +629,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 o[c] = __float_as_uint(v.x);
                 o[c + 1] = __float_as_uint(v.y);
               }
-              tmem_st_x32(t_o + c0, o);
+              tmem_st16_x32(t_o + c0, o);
             }
           }
           l_run *= alpha;
           const float m_use = m_run == -INFINITY ? 0.f : m_run;
-          tile_sum = masked ? softmax_tile_exp<true>(t_s, m_use, sl2, lim, pk)
-                            : softmax_tile_exp<false>(t_s, m_use, sl2, lim, pk);
+          tile_sum = masked ? softmax_half_exp<true>(t_s, key0, m_use, sl2, lim, pk)
+                            : softmax_half_exp<false>(t_s, key0, m_use, sl2, lim, pk);
         }
         l_run += tile_sum;
-        // P_k as packed bf16 pairs over the first 64 columns of S_k.
-#pragma unroll
-        for (int c0 = 0; c0 < BN / 2; c0 += 16) {
-          uint32_t part[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) part[c] = pk[c0 + c];
-          tmem_st_x16(t_s + c0, part);
-        }
+        // P_k as packed bf16 pairs over the first 32 of this thread's 64 S columns.
+        tmem_st16_x32(t_s, pk);
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&ctrl->p_ready[k]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->p_ready[k]);
       }
 
       // -------------------------------------------------------------- epilogue
       if (ok) ok = mbar_wait(&ctrl->o_done, ri & 1, abort_flag, WAIT_TIMEOUT_NS);
-      // Both warpgroups take the same branch: the barrier ORs every thread's view.
-      if (named_barrier_or(1, 256, !ok || *abort_flag != 0)) break;
+      // Every softmax warp takes the same branch: the barrier ORs every thread's view.
+      if (named_barrier_or(1, SOFTMAX_THREADS, !ok || *abort_flag != 0)) break;
       tc_fence_after_sync();
+      const float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // both halves
       if (kPartial) {
         // Split-KV partial result of this map for real query rows: O_k column-major
-        // (a warp stores 32 consecutive rows of one column), as accumulated against
-        // the reference maximum, then that maximum and the running sum.
+        // (lanes 0-15 store 16 consecutive rows of a column, lanes 16-31 those of the
+        // column 64 further), as accumulated against the reference maximum, then that
+        // maximum and the running sum.
         float *blk = p.part + static_cast<int64_t>(blockIdx.x) * PART_FLOATS + k * PART_MAP_FLOATS;
         const bool real = it.q0 + r < p.N;
 #pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
+        for (int c0 = 0; c0 < DV / 2; c0 += 32) {
           uint32_t v[32];
-          tmem_ld_x32(t_o + c0, v);
+          tmem_ld16_x32(t_o + c0, v);
           if (real) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) blk[(c0 + c) * BM + r] = __uint_as_float(v[c]);
+            for (int c = 0; c < 32; ++c) blk[(key0 + c0 + c) * BM + r] = __uint_as_float(v[c]);
           }
         }
-        if (real) {
+        if (real && hc == 0) {
           blk[PART_OFF_M + r] = m_run;
-          blk[PART_OFF_L + r] = l_run;
+          blk[PART_OFF_L + r] = l_row;
         }
         continue;  // the only item of this CTA
       }
-      const float inv = 1.f / l_run;
-      if (w_mine) ctrl->w_row[k * (DV / 2) + r] = w_pref;  // read after the barriers below
+      const float inv = 1.f / l_row;
+      if (w_mine) ctrl->w_row[quarter * 32 + lane] = w_pref;  // read after the barriers below
       if (kSave) {
-        // This map's normalised output row and its log2-sum-exp.
+        // This map's normalised output (this thread's 64 columns) and its
+        // log2-sum-exp.  32 columns at a time, transposed across 8-lane groups
+        // (8 rows of one key half) so that every store writes four 128-byte row
+        // segments.
         const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BM;
-        p.save_lse[(k * p.BH + it.bh) * n_pad + it.q0 + r] = m_run + __log2f(l_run);
-        // 32 columns at a time, transposed across 8-lane groups so that every
-        // store writes four 128-byte row segments.
-        const int row0 = it.q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
-        float *so = p.save_o + (k * p.BH + it.bh) * static_cast<int64_t>(p.N) * DV + 4 * (lane & 7);
+        if (hc == 0) p.save_lse[(k * p.BH + it.bh) * n_pad + it.q0 + r] = m_run + __log2f(l_row);
+        const int row0 = it.q0 + r - (lane & 7);  // the 8-lane group's first row
+        float *so = p.save_o + (k * p.BH + it.bh) * static_cast<int64_t>(p.N) * DV + key0 +
+                    4 * (lane & 7);
 #pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
+        for (int c0 = 0; c0 < DV / 2; c0 += 32) {
           uint32_t v[32];
-          tmem_ld_x32(t_o + c0, v);  // warp-collective
+          tmem_ld16_x32(t_o + c0, v);  // warp-collective
           uint4 ch[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -691,58 +699,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                __float_as_uint(__uint_as_float(v[4 * q + 3]) * inv));
           transpose8_chunks(ch, lane);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (row0 + j < p.N)
-              *reinterpret_cast<uint4 *>(so + static_cast<int64_t>(row0 + j) * DV + c0) = ch[j];
+          for (int jr = 0; jr < 8; ++jr) {
+            if (row0 + jr < p.N)
+              *reinterpret_cast<uint4 *>(so + static_cast<int64_t>(row0 + jr) * DV + c0) = ch[jr];
           }
         }
       }
-      xch[k * BM + r] = inv;
-      named_barrier_sync(1, 256);
+      if (hc == 0) xch[k * BM + r] = inv;
+      named_barrier_sync(1, SOFTMAX_THREADS);
       const float inv1 = xch[r];
       const float c2 = lam_h * xch[BM + r];
-      const int col0 = k * (DV / 2);
-      float o[64];
+      // This thread's 32 value columns: 64 hc + 32 k .. + 31, read from O1 and O2
+      // through the two-threads-per-lane shape.
+      const int col0 = key0 + 32 * k;
+      float o[32];
       float ss = 0.f;
+      {
+        uint32_t o1r[32], o2r[32];
+        tmem_ld16_x32_nowait(tmem + lane_addr + tm_o(0) + 32 * k, o1r);
+        tmem_ld16_x32_nowait(tmem + lane_addr + tm_o(1) + 32 * k, o2r);
+        tmem_ld_wait_x32(o1r);
+        tmem_ld_wait_x32(o2r);
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t o1r[16], o2r[16];
-        tmem_ld_x16(tmem + lane_addr + tm_o(0) + col0 + c0, o1r);
-        tmem_ld_x16(tmem + lane_addr + tm_o(1) + col0 + c0, o2r);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          o[c0 + c] = __uint_as_float(o1r[c]) * inv1 - __uint_as_float(o2r[c]) * c2;
-          ss = fmaf(o[c0 + c], o[c0 + c], ss);
+        for (int c = 0; c < 32; ++c) {
+          o[c] = __uint_as_float(o1r[c]) * inv1 - __uint_as_float(o2r[c]) * c2;
+          ss = fmaf(o[c], o[c], ss);
         }
       }
       // O1 and O2 are in registers: the next item's P V may overwrite them.
       tc_fence_before_sync();
-      mbar_arrive(&ctrl->o_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctrl->o_free);
       if (p.headnorm) {
-        named_barrier_sync(1, 256);  // both maps have read the 1/l exchange
+        named_barrier_sync(1, SOFTMAX_THREADS);  // every thread has read the 1/l exchange
         if (kGroup) {  // mean-subtracting (group) form: centre the row first
           float sm = 0.f;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) sm += o[c];
-          xch[k * BM + r] = sm;
-          named_barrier_sync(1, 256);
+          for (int c = 0; c < 32; ++c) sm += o[c];
+          sm += __shfl_xor_sync(0xffffffffu, sm, 16);
+          if (hc == 0) xch[k * BM + r] = sm;
+          named_barrier_sync(1, SOFTMAX_THREADS);
           const float mu = (xch[r] + xch[BM + r]) * (1.f / DV);
-          named_barrier_sync(1, 256);  // both maps have read the sums
+          named_barrier_sync(1, SOFTMAX_THREADS);  // every thread has read the sums
           ss = 0.f;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < 32; ++c) {
             o[c] -= mu;
             ss = fmaf(o[c], o[c], ss);
           }
         }
-        xch[k * BM + r] = ss;
-        named_barrier_sync(1, 256);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+        if (hc == 0) xch[k * BM + r] = ss;
+        named_barrier_sync(1, SOFTMAX_THREADS);
         const float tot = xch[r] + xch[BM + r];
         const float rr = rsqrtf(tot * (1.f / DV) + p.eps) * p.out_scale;
         if (p.norm_w != nullptr) {  // uniform: per-column weights from shared memory
           const float4 *w4 = reinterpret_cast<const float4 *>(ctrl->w_row + col0);
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
+          for (int c = 0; c < 32; c += 4) {
             const float4 wv = w4[c / 4];
             o[c] *= rr * wv.x;
             o[c + 1] *= rr * wv.y;
@@ -751,31 +765,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) o[c] *= rr;
+          for (int c = 0; c < 32; ++c) o[c] *= rr;
         }
       }
-      // bf16 row chunks, transposed across each 8-lane group so that every
-      // store instruction writes four 128-byte row segments (row-per-lane
-      // stores touched 32 rows each and held up the memory pipe at every item
-      // boundary).
-      uint4 pkt[8];
+      // bf16 row chunks (4 x 16 bytes), transposed across each 4-lane group (4
+      // rows of one key half) so that every store instruction writes eight
+      // 64-byte row segments instead of one 16-byte piece of 32 rows.
+      uint4 pkt[4];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
+      for (int v = 0; v < 4; ++v) {
         pkt[v].x = pack_bf16x2(o[8 * v + 0], o[8 * v + 1]);
         pkt[v].y = pack_bf16x2(o[8 * v + 2], o[8 * v + 3]);
         pkt[v].z = pack_bf16x2(o[8 * v + 4], o[8 * v + 5]);
         pkt[v].w = pack_bf16x2(o[8 * v + 6], o[8 * v + 7]);
       }
-      transpose8_chunks(pkt, lane);
-      const int row0 = it.q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
-      __nv_bfloat16 *obase = p.out + it.b * p.out_sb + it.h * p.out_sh + col0 + 8 * (lane & 7);
+      transpose4_chunks(pkt, lane);
+      const int row0 = it.q0 + r - (lane & 3);  // the 4-lane group's first row
+      __nv_bfloat16 *obase = p.out + it.b * p.out_sb + it.h * p.out_sh + col0 + 8 * (lane & 3);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (row0 + j < p.N)
-          *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row0 + j) * p.out_sn) = pkt[j];
+      for (int jr = 0; jr < 4; ++jr) {
+        if (row0 + jr < p.N)
+          *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row0 + jr) * p.out_sn) = pkt[jr];
       }
       // No barrier is needed before the next item writes xch and w_row again:
-      // its epilogue starts with the OR barrier of both warpgroups, which no
+      // its epilogue starts with the OR barrier of every softmax warp, which no
       // thread passes before every thread has finished its reads here.
     }
   }

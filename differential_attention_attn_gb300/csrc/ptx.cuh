@@ -333,6 +333,30 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
       : "memory");
 }
 
+// Two threads per TMEM lane (16x32bx2 shape, column split 64): thread t of the
+// warp reaches TMEM lane base + (t % 16), where base is the lane field of
+// taddr (the warp's quarter, or the quarter + 16), at columns col + i for
+// t < 16 and col + 64 + i for t >= 16 (i = register index).
+__device__ __forceinline__ void tmem_ld16_x32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 64;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld16_x32_nowait(taddr, r);
+  tmem_ld_wait_x32(r);
+}
+
+__device__ __forceinline__ void tmem_st16_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], 64, {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      :
+      : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -388,6 +412,29 @@ __device__ __forceinline__ void transpose8_chunks(uint4 (&a)[8], int lane) {
     const bool up = (lane & m) != 0;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
+      if (c & m) continue;
+      const int lo = c, hi = c | m;
+      const uint4 out = up ? a[lo] : a[hi];
+      uint4 in;
+      in.x = __shfl_xor_sync(0xffffffffu, out.x, m);
+      in.y = __shfl_xor_sync(0xffffffffu, out.y, m);
+      in.z = __shfl_xor_sync(0xffffffffu, out.z, m);
+      in.w = __shfl_xor_sync(0xffffffffu, out.w, m);
+      if (up)
+        a[lo] = in;
+      else
+        a[hi] = in;
+    }
+  }
+}
+
+// The same transpose within groups of 4 lanes for 4 chunks per lane.
+__device__ __forceinline__ void transpose4_chunks(uint4 (&a)[4], int lane) {
+#pragma unroll
+  for (int m = 2; m >= 1; m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
       if (c & m) continue;
       const int lo = c, hi = c | m;
       const uint4 out = up ? a[lo] : a[hi];
