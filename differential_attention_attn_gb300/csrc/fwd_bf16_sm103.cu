@@ -28,7 +28,7 @@
 //
 // Warp roles (640 threads):
 //   warp 0      TMA producer (one lane)
-//   warp 1      TMEM allocator and MMA issuer (one lane)
+//   warp 1      TMEM allocator and MMA issuer (one elected lane of the warp)
 //   warps 2-3   idle
 //   warps 4-11  softmax of map 1, warps 12-19 softmax of map 2
 // A softmax warp covers 16 query rows (TMEM lanes) of its warp's quarter, two
@@ -199,12 +199,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
   desc |= static_cast<uint64_t>(4) << 61;
   return desc;
 }
-__device__ __forceinline__ void umma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
+// Issued by one elected lane of a converged warp (as umma_bf16_ss_lo_warp).
+__device__ __forceinline__ void umma_e4m3_ss_warp(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // One 32-key chunk of a half row: mask (key key0 + i visible iff key0 + i <=
@@ -451,7 +454,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+      // The whole warp walks the loop, so every operand is warp-uniform; one
+      // elected lane issues each MMA and commit (the same lane throughout).
+      {
         constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
         constexpr uint32_t IDESC_QK8 = idesc_e4m3_f32(BM, BN);
         constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, true);
@@ -479,12 +484,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                        (k ? STAGE_K2 : STAGE_K1)));
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
-              umma_e4m3_ss(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK8, kk > 0);
+              umma_e4m3_ss_warp(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK8, kk > 0);
           } else {
             const uint32_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
-              umma_bf16_ss_lo(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, dhi, IDESC_QK, kk > 0);
+              umma_bf16_ss_lo_warp(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, dhi, IDESC_QK, kk > 0);
           }
         };
         // O_k += P_k V; 16 keys = 2048 bytes of V.  P_k's keys 0-63 are packed over
@@ -493,54 +498,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_bf16_ts_lo(tmem + tm_o(k), tmem + tm_s(k) + kk * 8 + (kk >= 4 ? 32 : 0),
+            umma_bf16_ts_lo_warp(tmem + tm_o(k), tmem + tm_s(k) + kk * 8 + (kk >= 4 ? 32 : 0),
                             b + 128 * kk, dhi, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+        };
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+          return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, WAIT_TIMEOUT_NS));
         };
         bool ok = true;
         uint32_t g = 0;  // key tiles processed so far
         Item it;
         for (uint32_t r = 0; ok && next_item<kPartial>(p, r, it); ++r) {
-          if (!(ok = mbar_wait(&ctrl->q_full, r & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+          if (!(ok = wait_all(&ctrl->q_full, r & 1))) break;
           tc_fence_after_sync();
           for (int j = 0; j < it.n_kv; ++j, ++g) {
             const int s = static_cast<int>(g % STAGES);
             const uint32_t ph = (g / STAGES) & 1;
-            if (!(ok = mbar_wait(&ctrl->k_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
+            if (!(ok = wait_all(&ctrl->k_full[s], ph))) break;
             tc_fence_after_sync();
             qk(0, s);
-            umma_commit(&ctrl->s_full[0]);
+            umma_commit_warp(&ctrl->s_full[0]);
             if (j > 0) {
-              if (!(ok = mbar_wait(&ctrl->p_ready[1], (g - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+              if (!(ok = wait_all(&ctrl->p_ready[1], (g - 1) & 1)))
                 break;
               tc_fence_after_sync();
               const int sp = static_cast<int>((g - 1) % STAGES);
               pv(1, sp, j - 1 > 0);
-              umma_commit(&ctrl->kv_empty[sp]);
+              umma_commit_warp(&ctrl->kv_empty[sp]);
             }
             qk(1, s);
-            umma_commit(&ctrl->s_full[1]);
-            if (j == it.n_kv - 1) umma_commit(&ctrl->q_empty);  // last use of this item's Q
-            if (!(ok = mbar_wait(&ctrl->v_full[s], ph, abort_flag, WAIT_TIMEOUT_NS))) break;
-            if (!(ok = mbar_wait(&ctrl->p_ready[0], g & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+            umma_commit_warp(&ctrl->s_full[1]);
+            if (j == it.n_kv - 1) umma_commit_warp(&ctrl->q_empty);  // last use of this item's Q
+            if (!(ok = wait_all(&ctrl->v_full[s], ph))) break;
+            if (!(ok = wait_all(&ctrl->p_ready[0], g & 1))) break;
             // The first P V of an item overwrites O: the previous item's epilogue
             // must have read it.
             if (j == 0 && r > 0 &&
-                !(ok = mbar_wait(&ctrl->o_free, (r - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
+                !(ok = wait_all(&ctrl->o_free, (r - 1) & 1)))
               break;
             tc_fence_after_sync();
             pv(0, s, j > 0);
           }
           if (!ok) break;
           const uint32_t gl = g - 1;  // the item's last key tile
-          if (!(ok = mbar_wait(&ctrl->p_ready[1], gl & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
+          if (!(ok = wait_all(&ctrl->p_ready[1], gl & 1))) break;
           tc_fence_after_sync();
           const int sl = static_cast<int>(gl % STAGES);
           pv(1, sl, it.n_kv > 1);
-          umma_commit(&ctrl->kv_empty[sl]);
-          umma_commit(&ctrl->o_done);
+          umma_commit_warp(&ctrl->kv_empty[sl]);
+          umma_commit_warp(&ctrl->o_done);
         }
         // Never free tensor memory under a running MMA: wait for all of them.
-        umma_commit(&ctrl->drain);
+        umma_commit_warp(&ctrl->drain);
         drain_wait(&ctrl->drain, 0);
       }
       __syncwarp();  // the whole warp leaves together (the barriers below are warp-aligned)
