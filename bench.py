@@ -5,7 +5,8 @@ the head-norm epilogue) over one batch of the needle-style causal workload
 B=2, H=16, N=4096, d=64 (value width 128).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload needle_4k|small_causal|mid_causal|long_16k|decode_16k]
+                  [--workload needle_4k|small_causal|mid_causal|long_16k|rising_4k|decode_16k]
+                  [--scaling strong|weak]
 
 --workload picks another measured shape (default needle_4k, the headline).
 wide_4k is the forward with query/key halves of width d = 128 (B=2, H=8,
@@ -19,11 +20,23 @@ against a 16384-key cache through diffattn_fwd_kv with the library's split
 count; it is bound by HBM, so its metric is algorithmic GB/s (the cache read
 once, queries in, outputs out).
 
+rising_4k is the headline shape with logits that climb along the key axis
+(an adversarial case for the softmax's running maximum).
+
 Metric: algorithmic TFLOP/s with 8*d flops per visible (query, key) pair
 (2*d for each of the two Q K^T maps, 4*d for one combined map times V of
-width 2d) and the causal half convention B*H*N^2/2 pairs.  Under torchrun each
-rank runs its own copy of the workload (weak scaling, no data-path
-collective); value = flops of all ranks / max over ranks of the timed region.
+width 2d) and the causal half convention B*H*N^2/2 pairs.  Every launch is
+bracketed by CUDA events: value is from the whole timed region, and the line
+also reports the median per-launch time.
+
+Several GPUs (--gpus N; launched under torchrun, or relaunched under it when
+started without one): every (batch, head) is independent and the head norm is
+per token, so the forward needs no collective.  --scaling strong (the default)
+partitions the workload's B*H heads into N contiguous, balanced slices, one per
+rank, each run as its own forward (the caller would gather the output
+slices); --scaling weak runs the whole workload on every rank.  value = flops
+of all ranks / max over ranks of the timed region.  The key/value-cache and
+backward workloads always run weak.
 """
 from __future__ import annotations
 
@@ -45,6 +58,7 @@ import torch  # noqa: E402
 WORKLOAD = "needle_4k"
 METRIC = "diff-attn fwd TFLOP/s (causal, bf16) and % of GB300 tensor peak, 1 GPU"
 UNIT = "TFLOP/s"
+SPEC_BF16_TFLOPS = 2250.0  # GB300 nominal dense bf16 rate (context next to the measured peak)
 L2_BYTES = 129 * 1024 * 1024
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["differential_attention_attn_gb300/csrc/fwd_bf16_sm103.cu",
@@ -191,6 +205,31 @@ def max_over_ranks(values, dist=None, device="cpu"):
     if dist is not None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return [float(x) for x in t]
+
+
+def head_slice(BH: int, world: int, rank: int):
+    """Contiguous, balanced slice [lo, hi) of the BH flattened (batch, head)
+    pairs for `rank` of `world`: slice sizes differ by at most one head and the
+    slices tile [0, BH) in rank order."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank / world")
+    return rank * BH // world, (rank + 1) * BH // world
+
+
+def timed_launches(step, steps: int, stream):
+    """Run step(0 .. steps-1) with an event before every launch and one after
+    the last.  Returns (ms from first to last event, per-launch ms, wall-clock
+    start, wall-clock end)."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    t_wall0 = time.time()
+    for i in range(steps):
+        ev[i].record(stream)
+        step(i)
+    ev[steps].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[steps]), per_launch, t_wall0, t_wall1
 
 
 def cpu_baseline(w, seconds: float, seed: int = 3):
@@ -348,17 +387,10 @@ def run_decode(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        step(sets[i % n_sets], out)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
+    ms_total, per_launch, t_wall0, t_wall1 = timed_launches(
+        lambda i: step(sets[i % n_sets], out), args.steps, stream)
     if dist:
         dist.barrier()
-    ms_total = e0.elapsed_time(e1)
     if sampler:
         time.sleep(0.15)
         sampler.stop()
@@ -386,7 +418,8 @@ def run_decode(args):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
-    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dist, dev)
+    med_ms = statistics.median(per_launch)
+    ms_total, e2e_ms, med_ms = max_over_ranks([ms_total, e2e_ms, med_ms], dist, dev)
     nbytes = decode_bytes(B, H, Nq, Nkv, d)
     value = world * nbytes * args.steps / (ms_total * 1e-3) / 1e9
     if rank != 0:
@@ -399,6 +432,7 @@ def run_decode(args):
     line = {
         "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": launch_ms,
+        "median_ms_per_launch": med_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": args.workload, "B": B, "H": H, "Nq": Nq, "Nkv": Nkv, "d": d,
@@ -504,21 +538,14 @@ def run_bwd(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
+    ms_total, per_launch, t_wall0, t_wall1 = timed_launches(step, args.steps, stream)
     if dist:
         dist.barrier()
-    ms_total = e0.elapsed_time(e1)
     if sampler:
         time.sleep(0.15)
         sampler.stop()
-    (ms_total,) = max_over_ranks([ms_total], dist, dev)
+    med_ms = statistics.median(per_launch)
+    ms_total, med_ms = max_over_ranks([ms_total, med_ms], dist, dev)
     flops_step = alg_flops(B, H, N, d) * 20.0 / 8.0
     value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
     if rank != 0:
@@ -531,6 +558,7 @@ def run_bwd(args):
     line = {
         "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": launch_ms,
+        "median_ms_per_launch": med_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "needle_4k_bwd", "B": B, "H": H, "N": N, "d": d, "dv": 2 * d,
@@ -566,6 +594,7 @@ def run_ours(args):
     WORKLOAD = args.workload
 
     world, rank, local = dist_env()
+    strong = args.scaling == "strong"
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -585,13 +614,27 @@ def run_ours(args):
         for name in ("q1", "k1", "q2", "k2"):
             setattr(w, name, getattr(w, name).float().to(torch.float8_e4m3fn))
     else:
-        w = W.make(WORKLOAD, seed_offset=rank)
+        w = W.make(WORKLOAD, seed_offset=0 if strong else rank)
     B, H, N, d = w.B, w.H, w.N, w.d
     li = float(np.float32(w.lambda_init_override if w.layer is None
                           else ops.lambda_init(w.layer)))
-    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device=dev)
-    norm_w = None if w.w is None else torch.tensor(w.w, dtype=torch.float32, device=dev)
+    lam_all = np.asarray(w.lambdas(li), dtype=np.float32)
+    w_all = None if w.w is None else np.asarray(w.w, dtype=np.float32)
     host = [t.contiguous() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    bh_lo, bh_hi = 0, B * H
+    if strong:
+        # This rank's heads: a contiguous slice of the flattened (batch, head)
+        # pairs, run as one batch of hi - lo heads with their own lambda and
+        # norm weights (head h of batch b is flattened index b * H + h).
+        bh_lo, bh_hi = head_slice(B * H, world, rank)
+        heads = np.arange(bh_lo, bh_hi) % H
+        host = [t.reshape(B * H, N, -1)[bh_lo:bh_hi].reshape(1, bh_hi - bh_lo, N, -1).contiguous()
+                for t in host]
+        lam_all = lam_all[heads]
+        w_all = None if w_all is None else w_all[heads]
+        B, H = 1, bh_hi - bh_lo
+    lam = torch.tensor(lam_all, dtype=torch.float32, device=dev)
+    norm_w = None if w_all is None else torch.tensor(w_all, dtype=torch.float32, device=dev)
     set_bytes = sum(t.numel() * t.element_size() for t in host) + B * H * N * 2 * d * 2
     n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
     sets = []
@@ -620,17 +663,9 @@ def run_ours(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
+    ms_total, per_launch, t_wall0, t_wall1 = timed_launches(step, args.steps, stream)
     if dist:
         dist.barrier()
-    ms_total = e0.elapsed_time(e1)
     if sampler:
         time.sleep(0.15)
         sampler.stop()
@@ -689,10 +724,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
 
-    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dist, dev)
-    flops_step = alg_flops(B, H, N, d)
-    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    med_ms = statistics.median(per_launch)
+    ms_total, e2e_ms, med_ms = max_over_ranks([ms_total, e2e_ms, med_ms], dist, dev)
+    flops_step = alg_flops(B, H, N, d)  # this rank's launch
+    # One step of the job: the whole workload once (strong) or once per rank (weak).
+    job_flops = alg_flops(w.B, w.H, N, d) * (1 if strong else world)
+    value = job_flops * args.steps / (ms_total * 1e-3) / 1e12
+    e2e_value = job_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
     launch_ms = ms_total / args.steps
     achieved = flops_step / (launch_ms * 1e-3) / 1e12
 
@@ -703,20 +741,28 @@ def run_ours(args):
     peaks, peak_src = read_peaks()
     peak = float(peaks["bf16_tflops"])
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if strong and world > 1:
+        par = (f"strong x{world}: the {w.B * w.H} (batch, head) pairs in contiguous slices of "
+               f"{w.B * w.H // world} to {-(-w.B * w.H // world)}, one per rank; no collective")
+    else:
+        par = f"weak x{world} (one full workload per rank)"
     line = {
         "metric": METRIC.replace("bf16", "e4m3 q/k, bf16 v") if fp8 else METRIC,
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
+        "scaling": "strong" if (strong and world > 1) else "weak", "vs_baseline": None,
+        "median_ms_per_launch": med_ms,
+        "value_at_median": job_flops / (med_ms * 1e-3) / 1e12,
         "dtype": "e4m3 q/k, bf16 v/out" if fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": d, "dv": 2 * d,
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "N": N, "d": d, "dv": 2 * d,
                    "causal": True, "headnorm": True,
                    "flops_convention": "8*d per visible pair, B*H*N^2/2 pairs",
                    "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
                          f"(> {L2_BYTES / 1e6:.0f} MB L2)",
-                   "parallelism": f"weak x{world} (one full workload per rank)"},
+                   "parallelism": par},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
+                     "spec_peak": SPEC_BF16_TFLOPS, "frac_of_spec": achieved / SPEC_BF16_TFLOPS,
                      "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS bf16 GEMM)",
                      "kernel": ("diffattn_fwd_d128_sm103_kernel" if d == 128
                                 else "diffattn_fwd_bf16_sm103_kernel"),
@@ -731,11 +777,27 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if strong and world > 1:
+        line["config"]["heads_rank0"] = [bh_lo, bh_hi]
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def relaunch(gpus: int):
+    """Run this same command as `gpus` ranks under torch.distributed.run (one
+    process per GPU of this node, rendezvous on 127.0.0.1) and exit with its
+    status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={gpus}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    raise SystemExit(subprocess.call(cmd))
 
 
 def main():
@@ -747,10 +809,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["needle_4k", "small_causal", "mid_causal", "long_16k", *DECODE,
-                             "needle_4k_bwd", "wide_4k", "needle_4k_fp8"])
+                    choices=["needle_4k", "small_causal", "mid_causal", "long_16k", "rising_4k",
+                             *DECODE, "needle_4k_bwd", "wide_4k", "needle_4k_fp8"])
+    ap.add_argument("--scaling", choices=["strong", "weak"], default="strong",
+                    help="with several GPUs: partition the heads (strong) or replicate (weak)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        relaunch(args.gpus)  # does not return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -63,8 +63,8 @@
 // running sums then stay far from the fp32/bf16 range limits).  Otherwise
 // (and on the first tile) the warp takes the exact path: the true maximum
 // from S (still intact in TMEM, because P is held in registers until
-// certified), m moved to it whenever it is larger, a rescale of O_k and of
-// the running sum, and the exponentials again.  The causal/ragged mask is
+// certified), m moved to that maximum plus a headroom whenever it is larger,
+// a rescale of O_k and of the running sum, and the exponentials again.  The causal/ragged mask is
 // compiled only into the tiles that need it.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -92,6 +92,13 @@ constexpr uint32_t REGS_LAUNCH = 96;    // 65536 / 640, rounded down to a multip
 constexpr uint32_t REGS_CTRL = 64;      // per thread, warps 0-3 (loads, MMA issue)
 constexpr uint32_t REGS_SOFTMAX = 104;  // per thread, warps 4-19 (softmax, epilogue)
 constexpr float CERT_SUM = 65536.0f;    // half-row sums up to 2^16 certify a tile
+// When the exact path sets the reference maximum it places it this far (log2
+// units) above the tile's maximum: P then starts at most 2^-24 and later
+// tiles may climb 24 + 16 units before the certificate fails again.  Only the
+// scale of P, O and the sums changes (their relative precision does not); an
+// entry more than about 100 units below the maximum flushes to zero, where
+// its weight (below 2^-100 of the maximum's) is already far below rounding.
+constexpr float M_HEADROOM = 24.0f;
 
 constexpr uint32_t TILE_QK_BYTES = BM * HD * 2;     // 16 KB: one [128 x 64] bf16 tile
 constexpr uint32_t TILE_V_BYTES = BN * DV * 2;      // 32 KB: two [128 x 64] column blocks
@@ -614,7 +621,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // A row can see no key at all in the first tile of a split key range
           // (mt = -inf); it then keeps m = -inf, its p are 0 and the next tile
           // rescales by 2^-inf = 0.
-          const float m_new = fmaxf(m_run, mt * sl2);
+          const float m_new = fmaxf(m_run, mt * sl2 + M_HEADROOM);
           float alpha = 1.f;
           if (j == 0) {
             m_run = m_new;
@@ -656,10 +663,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       // -------------------------------------------------------------- epilogue
       if (ok) ok = mbar_wait(&ctrl->o_done, ri & 1, abort_flag, WAIT_TIMEOUT_NS);
+      const float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // both halves
+      const float inv = 1.f / l_row;
+      if (!kPartial) {
+        // Published by the barrier below.  Every thread finished reading the
+        // previous item's exchange before this item's o_done could complete
+        // (each thread's last P of this item follows its previous epilogue).
+        if (hc == 0) xch[k * BM + r] = inv;
+        if (w_mine) ctrl->w_row[quarter * 32 + lane] = w_pref;
+      }
       // Every softmax warp takes the same branch: the barrier ORs every thread's view.
       if (named_barrier_or(1, SOFTMAX_THREADS, !ok || *abort_flag != 0)) break;
       tc_fence_after_sync();
-      const float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // both halves
       if (kPartial) {
         // Split-KV partial result of this map for real query rows: O_k column-major
         // (lanes 0-15 store 16 consecutive rows of a column, lanes 16-31 those of the
@@ -682,8 +697,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;  // the only item of this CTA
       }
-      const float inv = 1.f / l_row;
-      if (w_mine) ctrl->w_row[quarter * 32 + lane] = w_pref;  // read after the barriers below
       if (kSave) {
         // This map's normalised output (this thread's 64 columns) and its
         // log2-sum-exp.  32 columns at a time, transposed across 8-lane groups
@@ -713,8 +726,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (hc == 0) xch[k * BM + r] = inv;
-      named_barrier_sync(1, SOFTMAX_THREADS);
       const float inv1 = xch[r];
       const float c2 = lam_h * xch[BM + r];
       // This thread's 32 value columns: 64 hc + 32 k .. + 31, read from O1 and O2
@@ -795,9 +806,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (row0 + jr < p.N)
           *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row0 + jr) * p.out_sn) = pkt[jr];
       }
-      // No barrier is needed before the next item writes xch and w_row again:
-      // its epilogue starts with the OR barrier of every softmax warp, which no
-      // thread passes before every thread has finished its reads here.
+      // The next item writes xch and w_row only after its o_done, which needs
+      // every thread's P of that item, so every thread has finished here.
     }
   }
 

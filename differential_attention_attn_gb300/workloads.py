@@ -25,6 +25,10 @@ works"):
                  replacement from [0, N - 6); lambda = 0.8, lambda_init = 0.8.
   long_16k       bf16, B=1, H=32, N=16384, d=64, causal, layer 24,
                  lambda_h ~ U[0.6, 0.9], norm weight 1.
+  rising_4k      bf16, B=2, H=16, N=4096, d=64, causal, logits that climb
+                 along the key axis (see rising()); layer 8,
+                 lambda_h ~ U[0.3, 0.9], norm weight 1.  An adversarial case
+                 for softmax kernels that keep a stale running maximum.
 
 Random source: numpy.random.default_rng(1000 + workload number) drawing in
 float64 in the order Q1, K1, Q2, K2, V, [needle positions], lambda, w; the
@@ -38,7 +42,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-WORKLOADS = ("pages_example", "small_causal", "mid_causal", "needle_4k", "long_16k")
+WORKLOADS = ("pages_example", "small_causal", "mid_causal", "needle_4k", "long_16k",
+             "rising_4k")
 WORKLOAD_NUMBER = {name: i + 1 for i, name in enumerate(WORKLOADS)}
 
 
@@ -135,6 +140,8 @@ def make(name: str, *, seed_offset: int = 0) -> Workload:
         lam = rng.uniform(0.6, 0.9, size=H)
         return Workload(name, B, H, N, d, torch.bfloat16, True, True, 1e-5, q1, k1, q2, k2, v,
                         lam, False, 24, None, None)
+    if name == "rising_4k":
+        return rising(seed, B=2, H=16, N=4096, d=64)
     raise KeyError(f"unknown workload {name!r}; known: {WORKLOADS}")
 
 
@@ -165,6 +172,34 @@ def needle(seed: int, *, B: int, H: int, N: int, d: int, n_needles: int = 6,
                     dtype, True, True, 1e-5, t(q1), t(k1), t(q2), t(k2), t(v),
                     np.full(H, 0.8), False, None, 0.8, None,
                     meta={"needle_pos": pos, "needle_query": N - n_needles + np.arange(n_needles)})
+
+
+def rising(seed: int, *, B: int, H: int, N: int, d: int, slope: float = 3.5,
+           q_gain: float = 4.0, dtype=torch.bfloat16, name: str | None = None) -> Workload:
+    """Causal inputs whose logits climb along the key axis, for both maps.
+
+    Per head and map a random unit direction u is drawn; queries are
+    q_gain * u + 0.5 N(0,1) and key j is (0.5 + slope * j / 128) * u + N(0,1).
+    With the defaults (|q . u| = 4, d = 64) the mean logit q . k_j / sqrt(d)
+    grows by about 1.75 natural units (2.5 in base 2) per 128 keys, so every
+    key tile of a row lies a few base-2 units above the one before and the row
+    maximum moves on nearly every tile.  V ~ N(0,1).  Draw order: u1, u2, the
+    noise of Q1, K1, Q2, K2, then V, lambda."""
+    rng = np.random.default_rng(seed)
+    u = [rng.standard_normal(size=(B, H, 1, d)) for _ in range(2)]
+    u = [x / np.linalg.norm(x, axis=-1, keepdims=True) for x in u]
+    pos = (0.5 + slope * np.arange(N) / 128.0).reshape(1, 1, N, 1)
+    out = []
+    for k in range(2):
+        q = q_gain * u[k] + 0.5 * _normal(rng, (B, H, N, d))
+        key = pos * u[k] + _normal(rng, (B, H, N, d))
+        out += [q, key]
+    v = _normal(rng, (B, H, N, 2 * d))
+    lam = rng.uniform(0.3, 0.9, size=H)
+    t = lambda x: _to_storage(x, dtype)
+    nm = name or ("rising_4k" if (B, H, N, d) == (2, 16, 4096, 64) else f"rising_B{B}H{H}N{N}")
+    return Workload(nm, B, H, N, d, dtype, True, True, 1e-5, t(out[0]), t(out[1]), t(out[2]),
+                    t(out[3]), t(v), lam, False, 8, None, None)
 
 
 def custom(seed: int, *, B: int, H: int, N: int, d: int, causal: bool, headnorm: bool = True,

@@ -108,7 +108,8 @@ def test_bf16_small_causal_full():
 
 
 @pytest.mark.parametrize("name,per_head,full_heads", [
-    ("mid_causal", 48, (0, 63)), ("needle_4k", 48, (0, 31)), ("long_16k", 16, (31,))])
+    ("mid_causal", 48, (0, 63)), ("needle_4k", 48, (0, 31)), ("long_16k", 16, (31,)),
+    ("rising_4k", 48, (0, 31))])
 def test_bf16_workload_sampled(name, per_head, full_heads):
     w = W.make(name)
     gpu = harness.run_gpu(w)
@@ -117,6 +118,18 @@ def test_bf16_workload_sampled(name, per_head, full_heads):
     got = got.double().cpu().numpy()
     ref = harness.run_oracle_rows(w, bh, ri)
     _cmp_bf16(got, ref, name)
+
+
+@pytest.mark.parametrize("slope,causal,headnorm", [
+    (3.5, True, True), (1.0, True, False), (8.0, True, True), (3.5, False, True)])
+def test_rising_logits_full(slope, causal, headnorm):
+    """Logits that climb by a few base-2 units per key tile (both maps), every row
+    compared: the running maximum moves on most tiles, exercising the exact path
+    and the rescale of O."""
+    w = W.rising(17, B=1, H=2, N=1000, d=64, slope=slope)
+    w.causal, w.headnorm = causal, headnorm
+    gpu = harness.run_gpu(w).double().cpu().numpy()
+    _cmp_bf16(gpu, harness.run_oracle(w), f"rising slope {slope}")
 
 
 def test_needle_rows_follow_the_needle():
