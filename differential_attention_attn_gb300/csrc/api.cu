@@ -2,6 +2,7 @@
 // Every entry point is declared, with its contract, in include/diffattn.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -31,31 +32,46 @@ diffattn_status check_desc(const diffattn_desc *desc) {
 }
 
 // The bf16 kernel is built for sm_103a only.
+// Per-device caches are atomics: host threads may call the library at once
+// (two threads filling the same entry compute the same value).
 diffattn_status check_sm103() {
-  static int cached[64];  // 0 unknown, 1 yes, 2 no
+  static std::atomic<int> cached[64];  // 0 unknown, 1 yes, 2 no
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
-  if (cached[dev] == 0) {
+  int c = cached[dev].load(std::memory_order_acquire);
+  if (c == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
-    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    c = (major == 10 && minor == 3) ? 1 : 2;
+    cached[dev].store(c, std::memory_order_release);
   }
-  return cached[dev] == 1 ? DIFFATTN_OK : DIFFATTN_ERR_UNSUPPORTED;
+  return c == 1 ? DIFFATTN_OK : DIFFATTN_ERR_UNSUPPORTED;
 }
 
 int sm_count() {
-  static int cached[64];
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_release);
   }
-  return cached[dev];
+  return n;
+}
+
+// Strides of q1, k1, q2, k2, v, out: positive multiples of 8 elements (16
+// bytes, the tensor-copy rule) below 2^39.
+diffattn_status check_strides(const diffattn_strides *strides) {
+  for (int i = 0; i < 6; ++i) {
+    const int64_t s3[3] = {strides[i].b, strides[i].h, strides[i].n};
+    for (int64_t x : s3)
+      if (x <= 0 || (x & 7) != 0 || x >= (int64_t{1} << 39)) return DIFFATTN_ERR_INVALID_ARG;
+  }
+  return DIFFATTN_OK;
 }
 
 // Validation shared by diffattn_fwd_kv_plan and diffattn_fwd_kv; on success
@@ -139,11 +155,7 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
   if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
       !aligned16(out))
     return DIFFATTN_ERR_INVALID_ARG;
-  for (int i = 0; i < 6; ++i) {
-    const int64_t s3[3] = {strides[i].b, strides[i].h, strides[i].n};
-    for (int64_t x : s3)
-      if (x <= 0 || (x & 7) != 0 || x >= (int64_t{1} << 39)) return DIFFATTN_ERR_INVALID_ARG;
-  }
+  if ((st = check_strides(strides)) != DIFFATTN_OK) return st;
   if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
   if (desc->d == 128)
@@ -186,6 +198,36 @@ diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const v
   st = launch_fwd_bf16_sm103(*desc, n_kv, q1, k1, q2, k2, v, lambda, norm_w, out, s, sp, part);
   if (st != DIFFATTN_OK || sp == 1) return st;
   return launch_splitkv_combine(*desc, n_kv, sp, part, lambda, norm_w, out, s);
+}
+
+diffattn_status diffattn_fwd_kv_strided(const diffattn_desc *desc, int64_t n_kv, const void *q1,
+                                        const void *k1, const void *q2, const void *k2,
+                                        const void *v, const float *lambda,
+                                        const float *norm_w, void *out, int splits,
+                                        void *workspace, size_t workspace_bytes,
+                                        const diffattn_strides *strides, void *stream) {
+  int sp = 1;
+  size_t need = 0;
+  diffattn_status st = plan_kv(desc, n_kv, splits, &sp, &need);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->dtype != DIFFATTN_BF16) return DIFFATTN_ERR_UNSUPPORTED;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out || !strides)
+    return DIFFATTN_ERR_INVALID_ARG;
+  if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+      !aligned16(out))
+    return DIFFATTN_ERR_INVALID_ARG;
+  if ((st = check_strides(strides)) != DIFFATTN_OK) return st;
+  if (sp > 1 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need))
+    return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
+  if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *part = sp > 1 ? static_cast<float *>(workspace) : nullptr;
+  st = launch_fwd_bf16_sm103(*desc, n_kv, q1, k1, q2, k2, v, lambda, norm_w, out, s, sp, part,
+                             nullptr, strides);
+  if (st != DIFFATTN_OK || sp == 1) return st;
+  return launch_splitkv_combine(*desc, n_kv, sp, part, lambda, norm_w, out, s, &strides[5]);
 }
 
 diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_bytes,

@@ -34,6 +34,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include <cmath>
 #include <cstdint>
 
@@ -851,16 +853,16 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
                      static_cast<uint64_t>(BH)) != CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device (concurrent callers may both set)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(diffattn_bwd_bf16_sm103_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   BwdParams p;
   p.BH = BH;

@@ -71,6 +71,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -897,11 +898,11 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
       return DIFFATTN_ERR_CUDA;
   }
 
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device (concurrent callers may both set)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     auto *k0 = diffattn_fwd_bf16_sm103_kernel<false, false, false, false>;
     auto *k1 = diffattn_fwd_bf16_sm103_kernel<true, false, false, false>;
     auto *k2 = diffattn_fwd_bf16_sm103_kernel<false, true, false, false>;
@@ -921,7 +922,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
         cudaFuncSetAttribute(k5, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
 
   Params p;
@@ -954,13 +955,16 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
   // Split-KV: one CTA per (query tile, key range).  Otherwise persistent: one
   // CTA per SM at most (one fits, by shared and tensor memory), each walking
   // its share of the items.
-  static int sms[64] = {0};
-  if (sms[dev] == 0 &&
-      cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return DIFFATTN_ERR_CUDA;
+  static std::atomic<int> sm_cache[64];
+  int sms = sm_cache[dev].load(std::memory_order_acquire);
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DIFFATTN_ERR_CUDA;
+    sm_cache[dev].store(sms, std::memory_order_release);
+  }
   const int64_t items = BH * n_qtiles;
   if (items == 0) return DIFFATTN_OK;
-  dim3 grid(static_cast<unsigned>(splits > 1 ? items * splits : std::min<int64_t>(items, sms[dev])));
+  dim3 grid(static_cast<unsigned>(splits > 1 ? items * splits : std::min<int64_t>(items, sms)));
   if (fp8 && splits > 1)
     diffattn_fwd_bf16_sm103_kernel<true, false, false, true>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);

@@ -38,6 +38,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include <cmath>
 #include <cstdint>
 
@@ -552,16 +554,16 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1,
         CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device (concurrent callers may both set)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(diffattn_fwd_d128_sm103_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   Params p;
   p.BH = BH;

@@ -53,10 +53,14 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
                                       float *dnorm_w, float *workspace, cudaStream_t stream);
 
 // Merge of the split-KV partial blocks: both maps' softmax states, then
-// o = O1/l1 - lambda O2/l2, the optional head norm and the bf16 store.
+// o = O1/l1 - lambda O2/l2, the optional head norm and the bf16 store (out
+// with the given element strides, or contiguous).  If desc.status_dev holds a
+// non-zero status when the partial kernel has finished (one of its CTAs gave
+// up on a wait), every output element is NaN.
 diffattn_status launch_splitkv_combine(const diffattn_desc &desc, int64_t n_kv, int splits,
                                        const float *part, const float *lambda,
-                                       const float *norm_w, void *out, cudaStream_t stream);
+                                       const float *norm_w, void *out, cudaStream_t stream,
+                                       const diffattn_strides *out_strides = nullptr);
 
 // Key tiles that query tile qt (of N queries against n_kv keys) sees: all of
 // them, or under the causal mask those up to the one holding the position

@@ -1,12 +1,12 @@
 // diffattn_fwd_kv_noalloc: diffattn_fwd_kv on a fixed scratch area that the
 // library owns, for callers that cannot provide a workspace.  Nothing is
 // allocated: the scratch is a static device array of the module, and its
-// address is looked up once per device.
+// address is looked up on every call (a context reset can move the module, so
+// a cached address could go stale).
 #include <cuda_runtime.h>
 
 #include <cstddef>
 #include <cstdint>
-#include <mutex>
 
 #include "internal.h"
 
@@ -17,20 +17,13 @@ static_assert(kScratchBytes == (size_t{64} << 20), "64 MiB");
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-std::mutex g_setup_mutex;
-void *g_scratch_addr[64];  // per device, set once
-
-// Device address of g_scratch for the current device (nullptr on failure).
+// Device address of g_scratch in the current device's context (nullptr on
+// failure).  In host code g_scratch names a host-side stand-in, never the
+// device array, so the kernels only ever receive this looked-up address.
 void *scratch_address() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void *addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_scratch) != cudaSuccess) return nullptr;
-    g_scratch_addr[dev] = addr;
-  }
-  return g_scratch_addr[dev];
+  void *addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_scratch) != cudaSuccess) return nullptr;
+  return addr;
 }
 
 }  // namespace

@@ -104,6 +104,8 @@ struct CombineParams {
   const float *lambda;
   const float *norm_w;
   __nv_bfloat16 *out;
+  int64_t out_sb, out_sh, out_sn;  // element strides of out (batch, head, row)
+  const int32_t *status;           // the call's status word, or null
 };
 
 // Running merge of one map's split states: (M, L, acc) absorbs (m, l, o).
@@ -150,6 +152,9 @@ __global__ void __launch_bounds__(kCombineThreads)
   for (int c = 0; c < kColsPerThread; ++c)
     wv[c] = p.norm_w ? __ldg(p.norm_w + static_cast<int64_t>(h) * kValueCols + col0 + c) : 1.f;
   grid_dependency_wait();
+  // A partial CTA that gave up on a wait has not written its block: rather
+  // than merge stale scratch into a plausible-looking output, write NaN.
+  const bool failed = p.status != nullptr && *reinterpret_cast<const volatile int32_t *>(p.status) != 0;
 
   float M1 = -INFINITY, L1 = 0.f, M2 = -INFINITY, L2 = 0.f;
   float acc1[kColsPerThread], acc2[kColsPerThread];
@@ -213,8 +218,10 @@ __global__ void __launch_bounds__(kCombineThreads)
     __nv_bfloat162 x[kColsPerThread / 2];
 #pragma unroll
     for (int c = 0; c < kColsPerThread / 2; ++c)
-      x[c] = __floats2bfloat162_rn(ov[2 * c], ov[2 * c + 1]);
-    *reinterpret_cast<uint4 *>(p.out + (bh * p.N + q) * kValueCols + col0) =
+      x[c] = failed ? __floats2bfloat162_rn(NAN, NAN)
+                    : __floats2bfloat162_rn(ov[2 * c], ov[2 * c + 1]);
+    const int64_t b = bh / p.H;
+    *reinterpret_cast<uint4 *>(p.out + b * p.out_sb + h * p.out_sh + q * p.out_sn + col0) =
         *reinterpret_cast<const uint4 *>(x);
   }
 }
@@ -223,7 +230,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 diffattn_status launch_splitkv_combine(const diffattn_desc &desc, int64_t n_kv, int splits,
                                        const float *part, const float *lambda,
-                                       const float *norm_w, void *out, cudaStream_t stream) {
+                                       const float *norm_w, void *out, cudaStream_t stream,
+                                       const diffattn_strides *out_strides) {
   const int64_t BH = desc.B * desc.H;
   const int64_t n_qtiles = (desc.N + kTileRows - 1) / kTileRows;
   const int64_t n_ktiles = (n_kv + kTileKeys - 1) / kTileKeys;
@@ -246,6 +254,10 @@ diffattn_status launch_splitkv_combine(const diffattn_desc &desc, int64_t n_kv, 
   p.lambda = lambda;
   p.norm_w = norm_w;
   p.out = static_cast<__nv_bfloat16 *>(out);
+  p.out_sn = out_strides ? out_strides->n : kValueCols;
+  p.out_sh = out_strides ? out_strides->h : desc.N * kValueCols;
+  p.out_sb = out_strides ? out_strides->b : desc.H * desc.N * kValueCols;
+  p.status = desc.status_dev;
   // Programmatic dependent launch: the kernel may be scheduled while the
   // partial kernel drains; it waits for that grid before reading `part`.
   cudaLaunchConfig_t cfg = {};

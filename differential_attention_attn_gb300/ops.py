@@ -84,6 +84,10 @@ def load(path: str = LIB_PATH):
         lib.diffattn_fwd_strided.restype = ctypes.c_int
         lib.diffattn_fwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp,
                                              ctypes.POINTER(Strides), vp]
+        lib.diffattn_fwd_kv_strided.restype = ctypes.c_int
+        lib.diffattn_fwd_kv_strided.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
+                                                vp, ctypes.c_int, vp, ctypes.c_size_t,
+                                                ctypes.POINTER(Strides), vp]
         lib.diffattn_selftest_wait.restype = ctypes.c_int
         lib.diffattn_selftest_wait.argtypes = [vp, ctypes.c_int64, vp]
         lib.diffattn_headnorm.restype = ctypes.c_int
@@ -300,6 +304,50 @@ def fwd_kv(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True, norm_
     st = lib.diffattn_fwd_kv(ctypes.byref(desc), int(n_kv), _ptr(q1), _ptr(k1), _ptr(q2),
                              _ptr(k2), _ptr(v), _ptr(lam), _ptr(norm_w), _ptr(out), int(splits),
                              _ptr(workspace), ws_bytes, _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return out
+
+
+def fwd_kv_strided(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: bool = True,
+                   norm_w=None, eps: float = 1e-5, lambda_init: float = 0.0, splits: int = 0,
+                   workspace=None, out=None, status=None, stream=None, raw_status: bool = False):
+    """`diffattn_fwd_kv_strided`: `fwd_kv` (bf16, d = 64) on [B, H, rows, width]-shaped
+    views of any layout whose rows are contiguous (e.g. a [B, Nkv, H, d] cache seen
+    through permute(0, 2, 1, 3)); `out` may be such a view too (default: contiguous)."""
+    B, H, N, d = q1.shape
+    n_kv = k1.shape[2]
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=q1.device)
+    ts = [q1, k1, q2, k2, v, out]
+    shapes = [(B, H, N, d), (B, H, n_kv, d), (B, H, N, d), (B, H, n_kv, d),
+              (B, H, n_kv, 2 * d), (B, H, N, 2 * d)]
+    for t, shape in zip(ts, shapes):
+        if tuple(t.shape) != shape or t.dtype != q1.dtype or not t.is_cuda:
+            raise ValueError(f"expected a CUDA {q1.dtype} tensor of shape {shape}")
+        if t.stride(-1) != 1:
+            raise ValueError("rows must be contiguous (last stride 1)")
+    _cuda_contig([lam, norm_w])
+    arr = (Strides * 6)(*[Strides(t.stride(0), t.stride(1), t.stride(2)) for t in ts])
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
+                     lambda_init, status)
+    lib = load()
+    if workspace is None:
+        sp, nb = ctypes.c_int(0), ctypes.c_size_t(0)
+        st = lib.diffattn_fwd_kv_plan(ctypes.byref(desc), int(n_kv), int(splits),
+                                      ctypes.byref(sp), ctypes.byref(nb))
+        if st != OK:
+            if raw_status:
+                return st
+            _check(st)
+        if nb.value:
+            workspace = torch.empty(nb.value, dtype=torch.uint8, device=q1.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.diffattn_fwd_kv_strided(ctypes.byref(desc), int(n_kv), _ptr(q1), _ptr(k1),
+                                     _ptr(q2), _ptr(k2), _ptr(v), _ptr(lam), _ptr(norm_w),
+                                     _ptr(out), int(splits), _ptr(workspace), ws_bytes, arr,
+                                     _stream_handle(stream))
     if raw_status:
         return st
     _check(st)

@@ -95,7 +95,7 @@ typedef struct diffattn_desc {
  *
  * Arguments: desc as above; q1, k1, q2, k2 device [B, H, N, d]; v device
  * [B, H, N, 2d]; lambda device float32 [H] (any finite value, not clamped);
- * norm_w device float32 [H, 2d] or NULL (ones; only read when headnorm = 1);
+ * norm_w device float32 [H, 2d] or NULL (ones; read when headnorm is 1 or 2);
  * out device [B, H, N, 2d] in desc->dtype, fully overwritten; stream a
  * cudaStream_t or NULL.
  *
@@ -192,6 +192,24 @@ diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const v
                                 size_t workspace_bytes, void *stream);
 
 /*
+ * diffattn_fwd_kv_strided — diffattn_fwd_kv with caller-given strides, so that
+ * a key/value cache kept in another layout (for example [B, n_kv, H, d]) is
+ * read in place.  Same computation and output values as diffattn_fwd_kv on
+ * contiguous copies.
+ *
+ * strides[0..5] are those of q1, k1, q2, k2, v, out, in elements, with the
+ * rules of diffattn_fwd_strided (contiguous rows; every stride a positive
+ * multiple of 8 elements and below 2^39).  Domain: DIFFATTN_BF16, d == 64;
+ * other arguments, the workspace and the errors as for diffattn_fwd_kv.
+ */
+diffattn_status diffattn_fwd_kv_strided(const diffattn_desc *desc, int64_t n_kv,
+                                        const void *q1, const void *k1, const void *q2,
+                                        const void *k2, const void *v, const float *lambda,
+                                        const float *norm_w, void *out, int splits,
+                                        void *workspace, size_t workspace_bytes,
+                                        const diffattn_strides *strides, void *stream);
+
+/*
  * diffattn_fwd_kv_plan — the split count diffattn_fwd_kv runs for this
  * request (splits = 0: the library's choice for the current device, from its
  * SM count and a per-CTA cost model) and the workspace bytes it needs (0 when
@@ -271,9 +289,10 @@ diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const vo
  * apart from the workspace: the split-KV partial blocks go to a fixed
  * DIFFATTN_NOALLOC_SCRATCH_BYTES area that the library owns (a static device
  * array of its module; nothing is allocated).  Its device address is looked
- * up once per device with cudaGetSymbolAddress on the first call that needs
- * it; a failed lookup returns DIFFATTN_ERR_CUDA.  Nothing in the area has to
- * start at zero, so nothing is cleared.
+ * up with cudaGetSymbolAddress on every call that needs it (after a context
+ * reset the module may sit at another address, so none is kept between
+ * calls); a failed lookup returns DIFFATTN_ERR_CUDA.  Nothing in the area has
+ * to start at zero, so nothing is cleared.
  *
  * Errors: those of diffattn_fwd_kv and diffattn_fwd_kv_plan, plus
  * DIFFATTN_ERR_UNSUPPORTED when the planned workspace exceeds
@@ -282,9 +301,9 @@ diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const vo
  * Caveats: every call on a device shares the one scratch area, so calls
  * that overlap in time (different streams, or different host threads without
  * ordering) race on it and give undefined results; order them.  The first
- * call on each device performs the set-up (the symbol lookup, which can load
- * the module), so it must come before any CUDA stream capture that records
- * this entry point.
+ * call on each device performs the set-up (its symbol lookup can load the
+ * module), so it must come before any CUDA stream capture that records this
+ * entry point.
  */
 diffattn_status diffattn_fwd_kv_noalloc(const diffattn_desc *desc, int64_t n_kv,
                                         const void *q1, const void *k1, const void *q2,

@@ -15,12 +15,31 @@ def lib():
     return ops.load()
 
 
+EXPECTED_ENTRY_POINTS = {
+    "diffattn_fwd", "diffattn_fwd_strided", "diffattn_fwd_kv_plan", "diffattn_fwd_kv",
+    "diffattn_fwd_kv_strided",
+    "diffattn_fwd_kv_noalloc", "diffattn_train_sizes", "diffattn_fwd_train", "diffattn_bwd",
+    "diffattn_headnorm", "diffattn_selftest_wait", "diffattn_lambda_init", "diffattn_strerror",
+    "diffattn_version"}
+
+
 def test_exports_every_declared_symbol(lib):
     names = ops.declared_symbols()
-    assert set(names) == {"diffattn_fwd", "diffattn_headnorm", "diffattn_lambda_init",
-                          "diffattn_strerror", "diffattn_version"} or len(names) >= 5
+    assert set(names) == EXPECTED_ENTRY_POINTS
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/diffattn.h but not exported"
+
+
+def test_exports_nothing_undeclared():
+    """Every exported diffattn_* function is declared in the header (nm on the built
+    library; no compute call)."""
+    import subprocess
+    lib_path = libbuild.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines()
+                if ln.split() and ln.split()[-1].startswith("diffattn_") and " T " in ln}
+    assert exported == EXPECTED_ENTRY_POINTS
 
 
 def test_desc_layout_matches_header():

@@ -139,3 +139,17 @@ def test_kv_group_norm(splits):
     w = W.kv_cache(495, B=1, H=3, Nq=40, Nkv=1500, causal=True)
     w.headnorm = 2
     _cmp(harness.run_gpu_kv(w, splits=splits), harness.run_oracle_kv(w), f"group splits={splits}")
+
+
+def test_combine_reports_a_failed_partial_as_nan():
+    """If the status word already holds an error when the partial kernel finishes (as it
+    would after a CTA gave up on a wait), the combine writes NaN rather than merging
+    scratch into a plausible output.  The error is planted on the host: no wait runs out
+    and nothing faults."""
+    w = W.kv_cache(940, B=1, H=4, Nq=16, Nkv=4096, causal=True)
+    status = torch.full((1,), ops.ERR_TIMEOUT, dtype=torch.int32, device="cuda")
+    out = harness.run_gpu_kv(w, splits=4, status=status)
+    assert torch.isnan(out.float()).all()
+    status.zero_()
+    out = harness.run_gpu_kv(w, splits=4, status=status)
+    assert int(status.item()) == 0 and torch.isfinite(out.float()).all()

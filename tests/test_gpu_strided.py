@@ -87,3 +87,30 @@ def test_d128_bnhd_layout_matches_contiguous(N, causal, headnorm):
     oracle_out = harness.run_oracle(w)
     err = float(np.max(np.abs(out.double().cpu().numpy() - oracle_out)))
     assert err <= harness.bf16_tolerance(oracle_out)
+
+
+@pytest.mark.parametrize("Nq,Nkv,splits", [(1, 5000, 4), (16, 2000, 1), (200, 1000, 3)])
+def test_kv_cache_in_bnhd_layout(Nq, Nkv, splits):
+    """diffattn_fwd_kv_strided on a [B, Nkv, H, c] cache (and [B, Nq, H, c] queries and
+    output) equals diffattn_fwd_kv on contiguous copies bitwise, single pass and split."""
+    w = W.kv_cache(820 + Nq, B=2, H=3, Nq=Nq, Nkv=Nkv, causal=True)
+    dev, lam, kw = _args(w)
+    ref = ops.fwd_kv(*dev, lam, splits=splits, **kw)
+    views = [_bnhd_view(t) for t in dev]
+    out_store = torch.full((2, Nq, 3, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = out_store.permute(0, 2, 1, 3)
+    ops.fwd_kv_strided(*views, lam, splits=splits, out=out, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    ref64 = harness.run_oracle_kv(w)
+    assert float(np.max(np.abs(out.double().cpu().numpy() - ref64))) <= harness.bf16_tolerance(ref64)
+
+
+def test_kv_strided_rejects_bad_strides():
+    w = W.kv_cache(830, B=1, H=2, Nq=4, Nkv=300, causal=True)
+    dev, lam, kw = _args(w)
+    store = torch.zeros((1, 2, 300, 70), dtype=torch.bfloat16, device="cuda")
+    k1 = store[..., :64]  # row stride 70: not a multiple of 8 elements
+    st = ops.fwd_kv_strided(dev[0], k1, dev[2], dev[3], dev[4], lam, splits=1,
+                            raw_status=True, **kw)
+    assert st == ops.ERR_INVALID_ARG

@@ -60,6 +60,20 @@ def test_noalloc_repeated_call_is_stable_and_matches_oracle():
     assert err <= harness.bf16_tolerance(ref)
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal,headnorm", [(True, 2), (False, 1), (False, 2)])
+def test_noalloc_group_norm_and_non_causal_through_the_combine(causal, headnorm):
+    """The mean-subtracting norm and the non-causal mask with splits > 1 (so the
+    combine kernel runs), bitwise against diffattn_fwd_kv with a fresh workspace."""
+    w = W.kv_cache(903 + headnorm, B=2, H=3, Nq=8, Nkv=2500, causal=causal, headnorm=headnorm)
+    dev, lam, kw = _args(w)
+    got = ops.fwd_kv_noalloc(*dev, lam, splits=5, **kw)
+    torch.cuda.synchronize()
+    want = ops.fwd_kv(*dev, lam, splits=5, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+
+
 def test_noalloc_rejects_oversize_requests_before_launch():
     """A split count whose partial blocks exceed the 64 MiB scratch is refused on the host."""
     libbuild.build()
