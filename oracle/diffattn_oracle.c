@@ -393,7 +393,9 @@ int oracle_headnorm(int64_t R, int dv, int H, const double *x,
  *                     y  = o r g,  r = 1 / sqrt(mean(o^2) + eps),  g = w (1 - lambda_init)
  *   given dy (row i):
  *     norm:    do = r g dy - (r^3 / 2d) o sum_c(dy_c g_c o_c);   dw += dy o r (1 - lambda_init)
- *              (without the norm: do = dy)
+ *              (without the norm: do = dy; with the group form, headnorm = 2,
+ *              o above is the centred row o - mean(o), r is taken from it, and
+ *              do then loses its mean: do -= mean_c(do))
  *     lambda:  dlambda += -(do . o2)
  *     values:  dV[j] += (p1[j] - lambda p2[j]) do
  *     maps:    dp1[j] = do . v_j,  dp2[j] = -lambda do . v_j
@@ -429,21 +431,38 @@ static void bwd_head(int64_t N, int d, const double *q1, const double *k1,
             }
         for (int c = 0; c < dv_; ++c)
             o[c] = o1[c] - lam * o2[c];
-        /* norm backward */
+        /* norm backward.  The group form normalises the centred row o - mean(o)
+         * exactly as the RMS form normalises o, so the RMS formula applies to the
+         * centred row; the derivative of the centring then removes the mean of
+         * the result. */
         if (headnorm) {
+            double mu = 0.0;
+            if (headnorm == 2) {
+                for (int c = 0; c < dv_; ++c)
+                    mu += o[c];
+                mu /= (double)dv_;
+            }
             double ms = 0.0, t = 0.0;
             for (int c = 0; c < dv_; ++c)
-                ms += o[c] * o[c];
+                ms += (o[c] - mu) * (o[c] - mu);
             ms /= (double)dv_;
             const double r = 1.0 / sqrt(ms + eps);
             for (int c = 0; c < dv_; ++c) {
                 const double g = (w_head ? w_head[c] : 1.0) * (1.0 - lambda_init);
-                t += dyi[c] * g * o[c];
+                t += dyi[c] * g * (o[c] - mu);
             }
             for (int c = 0; c < dv_; ++c) {
                 const double g = (w_head ? w_head[c] : 1.0) * (1.0 - lambda_init);
-                dout[c] = r * g * dyi[c] - r * r * r / (double)dv_ * o[c] * t;
-                dw[c] += dyi[c] * o[c] * r * (1.0 - lambda_init);
+                dout[c] = r * g * dyi[c] - r * r * r / (double)dv_ * (o[c] - mu) * t;
+                dw[c] += dyi[c] * (o[c] - mu) * r * (1.0 - lambda_init);
+            }
+            if (headnorm == 2) {
+                double md = 0.0;
+                for (int c = 0; c < dv_; ++c)
+                    md += dout[c];
+                md /= (double)dv_;
+                for (int c = 0; c < dv_; ++c)
+                    dout[c] -= md;
             }
         } else {
             for (int c = 0; c < dv_; ++c)
@@ -484,8 +503,8 @@ int oracle_bwd(int B, int H, int64_t N, int d, const double *q1, const double *k
                const double *dy, double *dq1, double *dk1, double *dq2, double *dk2,
                double *dv, double *dlam, double *dw, int nthreads)
 {
-    if (B < 0 || H <= 0 || N < 0 || d <= 0 || headnorm < 0 || headnorm > 1)
-        return -1;  /* the backward covers the RMS form (headnorm = 1) only */
+    if (B < 0 || H <= 0 || N < 0 || d <= 0 || headnorm < 0 || headnorm > 2)
+        return -1;
     const int64_t BH = (int64_t)B * H;
     const int dv_ = 2 * d;
     const size_t nqk = (size_t)(BH * N * d), nv = (size_t)(BH * N * dv_);

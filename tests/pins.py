@@ -352,10 +352,11 @@ def _fd_grads(lib, tensors, lam, w, dy, causal, headnorm, eps, li, h=1e-6):
 
 def pin_bwd_finite_differences(lib):
     """Every gradient of the backward oracle matches central differences of the
-    forward oracle (loss sum(y * dy)), causal or not, with and without the norm."""
+    forward oracle (loss sum(y * dy)), causal or not, without the norm and with
+    either form of it (RMS, group)."""
     worst = 0.0
-    for seed, causal, headnorm in [(61, True, True), (62, False, True), (63, True, False),
-                                   (64, False, False)]:
+    for seed, causal, headnorm in [(61, True, 1), (62, False, 1), (63, True, 0),
+                                   (64, False, 0), (65, True, 2), (66, False, 2)]:
         rng, q1, k1, q2, k2, v = _rand(seed, 1, 2, 5, 3)
         lam = rng.uniform(-0.3, 1.2, size=2)
         w = rng.uniform(0.5, 1.5, size=(2, 6))

@@ -60,10 +60,16 @@ MUTANTS = [
      "dk1[j * d + c] += ds1 * q1i[c];"),
     ("bwd_dv_plus_lambda", "dv[j * dv_ + c] += (p1[j] - lam * p2[j]) * dout[c];",
      "dv[j * dv_ + c] += (p1[j] + lam * p2[j]) * dout[c];"),
-    ("bwd_norm_term_halved", "dout[c] = r * g * dyi[c] - r * r * r / (double)dv_ * o[c] * t;",
-     "dout[c] = r * g * dyi[c] - r * r * r / (double)(2 * dv_) * o[c] * t;"),
-    ("bwd_dw_missing_lambda_init", "dw[c] += dyi[c] * o[c] * r * (1.0 - lambda_init);",
-     "dw[c] += dyi[c] * o[c] * r;"),
+    ("bwd_norm_term_halved",
+     "dout[c] = r * g * dyi[c] - r * r * r / (double)dv_ * (o[c] - mu) * t;",
+     "dout[c] = r * g * dyi[c] - r * r * r / (double)(2 * dv_) * (o[c] - mu) * t;"),
+    ("bwd_dw_missing_lambda_init", "dw[c] += dyi[c] * (o[c] - mu) * r * (1.0 - lambda_init);",
+     "dw[c] += dyi[c] * (o[c] - mu) * r;"),
+    ("bwd_groupnorm_do_not_centred", "dout[c] -= md;", "dout[c] -= 0.0 * md;"),
+    ("bwd_groupnorm_mean_dropped", "                    mu += o[c];\n",
+     "                    mu += 0.0 * o[c];\n"),
+    ("bwd_groupnorm_dw_uncentred", "dw[c] += dyi[c] * (o[c] - mu) * r * (1.0 - lambda_init);",
+     "dw[c] += dyi[c] * o[c] * r * (1.0 - lambda_init);"),
     ("bwd_dlambda_of_map1", "*dlam -= do_o2;", "*dlam -= do_o1;"),
     ("groupnorm_variance_uncentred", "var += (o[c] - mu) * (o[c] - mu);", "var += o[c] * o[c];"),
     ("groupnorm_output_uncentred", "o[c] = (o[c] - mu) * rg * g * (1.0 - lambda_init);",
