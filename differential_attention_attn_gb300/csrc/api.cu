@@ -236,7 +236,6 @@ diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_by
   if (st != DIFFATTN_OK) return st;
   if (saved_bytes == nullptr || workspace_bytes == nullptr) return DIFFATTN_ERR_INVALID_ARG;
   if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
-  if (desc->headnorm == 2) return DIFFATTN_ERR_UNSUPPORTED;  // backward: RMS form only
   const int64_t BH = desc->B * desc->H;
   *saved_bytes = static_cast<size_t>(saved_floats(BH, desc->N)) * sizeof(float);
   *workspace_bytes = static_cast<size_t>(bwd_workspace_floats(BH, desc->N)) * sizeof(float);

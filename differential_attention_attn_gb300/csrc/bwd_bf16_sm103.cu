@@ -657,6 +657,12 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
       float o[4], dout[4];
       for (int j = 0; j < 4; ++j) o[j] = o1[j] - lam * o2[j];
       if (p.headnorm) {
+        // The group form (headnorm = 2) normalises the centred row as the RMS
+        // form normalises o; the centring's derivative then removes do's mean.
+        if (p.headnorm == 2) {
+          const float mu = warp_sum((o[0] + o[1]) + (o[2] + o[3])) * (1.f / DV);
+          for (int j = 0; j < 4; ++j) o[j] -= mu;
+        }
         float ms = 0.f, t = 0.f;
         for (int j = 0; j < 4; ++j) {
           ms = fmaf(o[j], o[j], ms);
@@ -669,6 +675,10 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
         for (int j = 0; j < 4; ++j) {
           dout[j] = r * g[j] * dy[j] - r3 * o[j] * t;
           acc_w[j] = fmaf(dy[j] * o[j], r * p.out_scale, acc_w[j]);
+        }
+        if (p.headnorm == 2) {
+          const float md = warp_sum((dout[0] + dout[1]) + (dout[2] + dout[3])) * (1.f / DV);
+          for (int j = 0; j < 4; ++j) dout[j] -= md;
         }
       } else {
         for (int j = 0; j < 4; ++j) dout[j] = dy[j];
@@ -829,7 +839,7 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   pp.H = static_cast<int32_t>(desc.H);
   pp.N = static_cast<int32_t>(N);
   pp.n_pad = static_cast<int32_t>(n_pad);
-  pp.headnorm = desc.headnorm ? 1 : 0;
+  pp.headnorm = desc.headnorm;  // 0, 1 (RMS) or 2 (group)
   pp.eps = desc.eps;
   pp.out_scale = 1.0f - desc.lambda_init;
   pp.lambda = lambda;

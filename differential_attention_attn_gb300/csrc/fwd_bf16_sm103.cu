@@ -334,7 +334,8 @@ __device__ __forceinline__ bool next_item(const Params &p, uint32_t r, Item &it)
 // kPartial: split-KV partial mode (a key range per CTA, partial softmax
 // states to p.part, no epilogue); otherwise the whole forward of a query tile.
 // kSave (with !kPartial): also store the activations the backward pass needs.
-// kGroup (with !kPartial): the head norm is the mean-subtracting form.
+// kGroup (with !kPartial): the head norm is the mean-subtracting form (with
+// or without kSave).
 // kFp8: q1, k1, q2, k2 are e4m3 (one byte per element, 64-byte
 // rows with 64-byte swizzle in the same shared-memory slots); S is computed by
 // kind::f8f6f4 MMAs, everything from P on is unchanged.
@@ -909,6 +910,7 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
     auto *k3 = diffattn_fwd_bf16_sm103_kernel<false, false, true, false>;
     auto *k4 = diffattn_fwd_bf16_sm103_kernel<false, false, false, true>;
     auto *k5 = diffattn_fwd_bf16_sm103_kernel<true, false, false, true>;
+    auto *k6 = diffattn_fwd_bf16_sm103_kernel<false, true, true, false>;
     if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
         cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -920,6 +922,8 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
         cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
         cudaFuncSetAttribute(k5, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(k6, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
     attr_set[dev].store(true, std::memory_order_release);
@@ -973,6 +977,9 @@ diffattn_status launch_fwd_bf16_sm103(const diffattn_desc &desc, int64_t n_kv, c
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else if (splits > 1)
     diffattn_fwd_bf16_sm103_kernel<true, false, false, false>
+        <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  else if (save != nullptr && desc.headnorm == 2)
+    diffattn_fwd_bf16_sm103_kernel<false, true, true, false>
         <<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else if (save != nullptr)
     diffattn_fwd_bf16_sm103_kernel<false, true, false, false>

@@ -228,14 +228,15 @@ diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, in
  * differential attention works"); the backward is its derivative by the
  * chain rule: with o_k = map_k V (k = 1, 2), o = o1 - lambda o2 and, with the
  * norm, y = o r g, r = 1/sqrt(mean(o^2) + eps), g = w (1 - lambda_init):
- *   do = r g dy - (r^3 / 2d) o sum_c(dy g o)  (do = dy without the norm)
+ *   do = r g dy - (r^3 / 2d) o sum_c(dy g o)  (do = dy without the norm;
+ *        with the group form o is the centred row and do then loses its mean)
  *   dw = sum_rows dy o r (1 - lambda_init);  dlambda = -sum_rows do . o2
  *   dV = map1^T do - lambda map2^T do;  dW = do V^T
  *   dS_1 = P_1 * (dW - do.o1),  dS_2 = -lambda P_2 * (dW - do.o2)  (per row)
  *   dQ_k = dS_k K_k / sqrt(d),  dK_k = dS_k^T Q_k / sqrt(d)
  *
  * Domain: DIFFATTN_BF16, d == 64, square attention (N queries = N keys),
- * causal or not, headnorm 0 or 1 (2 is DIFFATTN_ERR_UNSUPPORTED); an sm_103
+ * causal or not, headnorm 0, 1 or 2 (the group form: the page's GroupNorm); an sm_103
  * device.
  */
 
@@ -262,7 +263,7 @@ diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, co
  * and norm_w, the `saved` buffer of diffattn_fwd_train and dy (bf16
  * [B, H, N, 128]).  Outputs (all device, overwritten): dq1, dk1, dq2, dk2
  * bf16 [B, H, N, 64]; dv bf16 [B, H, N, 128]; dlambda fp32 [H]; dnorm_w fp32
- * [H, 128] (written only when headnorm = 1; may be NULL to skip it).
+ * [H, 128] (written when headnorm is 1 or 2; may be NULL to skip it).
  * workspace: caller-owned scratch of at least workspace_bytes from
  * diffattn_train_sizes, 256-byte aligned (its contents on entry do not
  * matter).  dq and dv are summed over key tiles with fp32 atomic adds, so

@@ -204,10 +204,14 @@ def test_bwd_validation_before_launch(lib):
 def test_headnorm_mode_validation(lib):
     d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, 3, 1e-5, 0.2)
     assert _call(lib, d) == ops.ERR_INVALID_ARG
+    # the group form is trainable: same buffer sizes as the RMS form
     g = ops.make_desc(1, 2, 256, 64, ops.BF16, True, 2, 1e-5, 0.2)
+    r = ops.make_desc(1, 2, 256, 64, ops.BF16, True, 1, 1e-5, 0.2)
     a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
-    assert lib.diffattn_train_sizes(ctypes.byref(g), ctypes.byref(a),
-                                    ctypes.byref(b)) == ops.ERR_UNSUPPORTED
+    a1, b1 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.diffattn_train_sizes(ctypes.byref(g), ctypes.byref(a), ctypes.byref(b)) == ops.OK
+    assert lib.diffattn_train_sizes(ctypes.byref(r), ctypes.byref(a1), ctypes.byref(b1)) == ops.OK
+    assert (a.value, b.value) == (a1.value, b1.value) and a.value > 0
 
 
 def test_strided_validation_before_launch(lib):

@@ -108,3 +108,18 @@ def test_bwd_status_clear_and_repeatable():
             assert torch.equal(a[k], b[k])
     for k in ("dq1", "dq2", "dv"):  # fp32 atomics: order may differ, values agree closely
         assert torch.allclose(a[k].float(), b[k].float(), rtol=2e-2, atol=1e-2)
+
+
+@pytest.mark.parametrize("N,causal", [(7, True), (200, True), (256, False), (384, True)])
+@pytest.mark.parametrize("lam", [0.8, -0.5])
+def test_bwd_group_norm(N, causal, lam):
+    """headnorm = 2 (the page's GroupNorm, mean-subtracting): every gradient, including
+    the norm weight's, against the oracle; the training forward's output equals the
+    plain forward's bitwise."""
+    w = W.custom(700 + N, B=2, H=2, N=N, d=64, causal=causal, headnorm=2, random_w=True,
+                 layer=5)
+    w.lam_offset = np.full(w.H, lam)
+    dy = _dy(w, N + 1)
+    out, g = _run(w, dy)
+    _cmp(g, _oracle(w, dy), f"group norm N={N} causal={causal} lambda={lam}")
+    assert torch.equal(out, harness.run_gpu(w))
