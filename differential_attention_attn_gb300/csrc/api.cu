@@ -82,8 +82,12 @@ diffattn_status plan_kv(const diffattn_desc *desc, int64_t n_kv, int splits, int
   if (st != DIFFATTN_OK) return st;
   if (n_kv < 0 || splits < 0 || splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
   if (desc->causal && n_kv < desc->N) return DIFFATTN_ERR_INVALID_ARG;
-  if ((desc->dtype != DIFFATTN_BF16 && desc->dtype != DIFFATTN_E4M3_QK) || desc->d != 64)
+  if (desc->dtype != DIFFATTN_BF16 && desc->dtype != DIFFATTN_E4M3_QK)
     return DIFFATTN_ERR_UNSUPPORTED;
+  if (desc->d != 64 && !(desc->d == 128 && desc->dtype == DIFFATTN_BF16))
+    return DIFFATTN_ERR_UNSUPPORTED;
+  // d = 128 runs its two-pass kernel over the whole key range (no split-KV).
+  if (desc->d == 128 && splits > 1) return DIFFATTN_ERR_UNSUPPORTED;
   if (desc->dtype == DIFFATTN_E4M3_QK && desc->headnorm == 2) return DIFFATTN_ERR_UNSUPPORTED;
   const int64_t BH = desc->B * desc->H;
   if (BH * desc->N == 0) {
@@ -94,6 +98,7 @@ diffattn_status plan_kv(const diffattn_desc *desc, int64_t n_kv, int splits, int
   if (n_kv == 0) return DIFFATTN_ERR_INVALID_ARG;  // a softmax over no keys
   const int64_t n_qtiles = (desc->N + kTileRows - 1) / kTileRows;
   const int64_t n_ktiles = (n_kv + kTileKeys - 1) / kTileKeys;
+  if (splits == 0 && desc->d == 128) splits = 1;
   if (splits == 0) {
     const int sms = sm_count();
     if (sms <= 0) return DIFFATTN_ERR_CUDA;
@@ -130,7 +135,7 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
       return DIFFATTN_ERR_INVALID_ARG;
     if ((st = check_sm103()) != DIFFATTN_OK) return st;
     if (desc->d == 128)
-      return launch_fwd_d128_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w, out, s);
+      return launch_fwd_d128_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out, s);
     return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out, s, 1,
                                  nullptr);
   }
@@ -159,7 +164,7 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
   if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
   if (desc->d == 128)
-    return launch_fwd_d128_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w, out,
+    return launch_fwd_d128_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
                                  static_cast<cudaStream_t>(stream), strides);
   return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
                                static_cast<cudaStream_t>(stream), 1, nullptr, nullptr, strides);
@@ -194,6 +199,8 @@ diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const v
     return DIFFATTN_ERR_INVALID_ARG;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (desc->d == 128)
+    return launch_fwd_d128_sm103(*desc, n_kv, q1, k1, q2, k2, v, lambda, norm_w, out, s);
   float *part = sp > 1 ? static_cast<float *>(workspace) : nullptr;
   st = launch_fwd_bf16_sm103(*desc, n_kv, q1, k1, q2, k2, v, lambda, norm_w, out, s, sp, part);
   if (st != DIFFATTN_OK || sp == 1) return st;
@@ -223,6 +230,8 @@ diffattn_status diffattn_fwd_kv_strided(const diffattn_desc *desc, int64_t n_kv,
   if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (desc->d == 128)
+    return launch_fwd_d128_sm103(*desc, n_kv, q1, k1, q2, k2, v, lambda, norm_w, out, s, strides);
   float *part = sp > 1 ? static_cast<float *>(workspace) : nullptr;
   st = launch_fwd_bf16_sm103(*desc, n_kv, q1, k1, q2, k2, v, lambda, norm_w, out, s, sp, part,
                              nullptr, strides);

@@ -91,6 +91,8 @@ constexpr uint64_t DRAIN_TIMEOUT_NS = 200000000ull;
 struct Params {
   int64_t BH;
   int32_t H, N, n_qtiles, n_ktiles, causal, headnorm;
+  int32_t N_kv;   // key/value rows per head
+  int32_t q_off;  // sequence position of query row 0 (N_kv - N): causal alignment
   float scale_log2, eps, out_scale;
   const float *lambda;
   const float *norm_w;
@@ -131,8 +133,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int h = static_cast<int>(bh32 % H32);
   const int b_idx = static_cast<int>(bh32 / H32);
   const int q0 = qt * BM;
-  // Key tiles this query tile sees: all, or up to the one holding its last row.
-  const int n_kv = p.causal ? min(p.n_ktiles, (q0 + BM - 1) / BN + 1) : p.n_ktiles;
+  // Key tiles this query tile sees: all, or up to the one holding the position
+  // of its last row (queries are the last N of N_kv positions).
+  const int n_kv = p.causal ? min(p.n_ktiles, (p.q_off + q0 + BM - 1) / BN + 1) : p.n_ktiles;
   const int T = 2 * n_kv;  // tiles over both passes
 
   if (threadIdx.x == 0) {
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = (warp % 4) * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const float sl2 = p.scale_log2;
-    const int qpos = q0 + r;
+    const int qpos = p.q_off + q0 + r;  // sequence position of this row
     float m = -INFINITY, l = 0.f;               // pass 1: statistics of map g + 1
     float m1 = 0.f, m2 = 0.f, c2 = 0.f;  // pass 2: log2-sum-exp of each map, lambda
     bool ok = true;
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool pass2 = t >= n_kv;
       const int kv0 = (pass2 ? t - n_kv : t) * BN;
       // Key column c of the tile is visible to this row iff c <= lim.
-      const int lim = p.causal ? (qpos - kv0) : (p.N - 1 - kv0);
+      const int lim = p.causal ? (qpos - kv0) : (p.N_kv - 1 - kv0);
       const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
       if (!pass2) {
         // Online statistics over four 32-column chunks.  As in the d = 64
@@ -528,28 +531,31 @@ CUresult encode_map(CUtensorMap *map, const void *base, uint64_t width, uint64_t
 
 }  // namespace
 
-diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
-                                      const void *q2, const void *k2, const void *v,
-                                      const float *lambda, const float *norm_w, void *out,
-                                      cudaStream_t stream, const diffattn_strides *strides) {
+diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
+                                      const void *k1, const void *q2, const void *k2,
+                                      const void *v, const float *lambda, const float *norm_w,
+                                      void *out, cudaStream_t stream,
+                                      const diffattn_strides *strides) {
   const int64_t BH = desc.B * desc.H, N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
-  const int64_t n_ktiles = (N + BN - 1) / BN;
-  if (BH * n_qtiles > INT32_MAX || N > INT32_MAX / 2 || desc.B > INT32_MAX ||
-      desc.H > INT32_MAX)
+  const int64_t n_ktiles = (n_kv + BN - 1) / BN;
+  if (BH * n_qtiles > INT32_MAX || N > INT32_MAX / 2 || n_kv > INT32_MAX / 2 ||
+      desc.B > INT32_MAX || desc.H > INT32_MAX)
     return DIFFATTN_ERR_UNSUPPORTED;
-  // Element strides of q1, k1, q2, k2, v, out: given, or contiguous [B, H, N, width].
+  // Element strides of q1, k1, q2, k2, v, out: given, or contiguous [B, H, rows, width].
   diffattn_strides st[6];
   for (int i = 0; i < 6; ++i) {
     const int64_t width = (i >= 4) ? DV : HD;
-    st[i] = strides ? strides[i] : diffattn_strides{desc.H * N * width, N * width, width};
+    const int64_t rows = (i == 0 || i == 2 || i == 5) ? N : n_kv;
+    st[i] = strides ? strides[i] : diffattn_strides{desc.H * rows * width, rows * width, width};
   }
   CUtensorMap maps[5];
   const void *bases[5] = {q1, k1, q2, k2, v};
   for (int i = 0; i < 5; ++i) {
     const uint64_t width = (i == 4) ? DV : HD;
     const uint32_t rows = 128;
-    if (encode_map(&maps[i], bases[i], width, static_cast<uint64_t>(N),
+    const int64_t n_rows = (i == 0 || i == 2) ? N : n_kv;
+    if (encode_map(&maps[i], bases[i], width, static_cast<uint64_t>(n_rows),
                    static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B), rows, st[i]) !=
         CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
@@ -569,6 +575,8 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1,
   p.BH = BH;
   p.H = static_cast<int32_t>(desc.H);
   p.N = static_cast<int32_t>(N);
+  p.N_kv = static_cast<int32_t>(n_kv);
+  p.q_off = static_cast<int32_t>(n_kv - N);
   p.n_qtiles = static_cast<int32_t>(n_qtiles);
   p.n_ktiles = static_cast<int32_t>(n_ktiles);
   p.causal = desc.causal ? 1 : 0;

@@ -77,13 +77,14 @@ __host__ __device__ inline int64_t key_tiles_seen(int64_t qt, int64_t N, int64_t
 int auto_splits(int64_t BH, int64_t N, int64_t n_kv, bool causal, int sm_count);
 
 // Fused bf16 forward for d = 128 (value width 256): two passes per query tile
-// (statistics, then one normalised accumulator); [B, H, N, width] with the
-// element strides of q1, k1, q2, k2, v, out given (rows contiguous), or
-// contiguous when strides is null.
-diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
-                                      const void *q2, const void *k2, const void *v,
-                                      const float *lambda, const float *norm_w, void *out,
-                                      cudaStream_t stream,
+// (statistics, then one normalised accumulator) of N queries against n_kv
+// keys (causal: the queries are the last N positions); [B, H, rows, width]
+// with the element strides of q1, k1, q2, k2, v, out given (rows contiguous),
+// or contiguous when strides is null.
+diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
+                                      const void *k1, const void *q2, const void *k2,
+                                      const void *v, const float *lambda, const float *norm_w,
+                                      void *out, cudaStream_t stream,
                                       const diffattn_strides *strides = nullptr);
 
 // Bounded-wait self-test (selftest.cu).

@@ -106,7 +106,8 @@ typedef struct diffattn_desc {
  *     otherwise).  Runs a fused tcgen05/TMEM/TMA kernel (for d == 128 a
  *     two-pass one: row statistics, then a single normalised accumulator);
  *     needs an sm_103 device.  diffattn_fwd_strided takes both head widths;
- *     the other entry points take d == 64 only.
+ *     so does the key/value-cache entry (diffattn_fwd_kv, single pass);
+ *     training takes d == 64 only.
  *   - DIFFATTN_F32: 1 <= d <= 128, N <= 4096.  Plain CUDA-core kernel
  *     (accurate expf, fp32 accumulation).
  *   - DIFFATTN_E4M3_QK: d == 64, headnorm 0 or 1: the d == 64 kernel with the
@@ -164,9 +165,11 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
  * merges them, forms map1 - lambda map2 and applies the head norm.  This
  * fills the GPU when B * H * ceil(N / 128) is small against the SM count.
  *
- * Arguments: q1, q2 device bf16 [B, H, N, 64]; k1, k2 device bf16
- * [B, H, n_kv, 64]; v device bf16 [B, H, n_kv, 128]; out device bf16
- * [B, H, N, 128], fully overwritten; lambda and norm_w as for diffattn_fwd.
+ * Arguments: q1, q2 device bf16 [B, H, N, d]; k1, k2 device bf16
+ * [B, H, n_kv, d]; v device bf16 [B, H, n_kv, 2d]; out device bf16
+ * [B, H, N, 2d], fully overwritten; lambda and norm_w as for diffattn_fwd;
+ * d = 64, or d = 128 (which runs the two-pass d = 128 kernel over the whole
+ * key range: splits 0 and 1 only).
  * With dtype DIFFATTN_E4M3_QK, q1, k1, q2, k2 are e4m3 (one byte each, same
  * shapes) and v, out stay bf16, as for diffattn_fwd.
  * splits: 0 lets the library choose (diffattn_fwd_kv_plan reports the
@@ -181,8 +184,9 @@ diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, 
  * Errors: DIFFATTN_ERR_INVALID_ARG for a negative n_kv, causal with
  * n_kv < N, n_kv = 0 with queries present, splits outside 0..256, a missing
  * or short workspace, or misaligned buffers; DIFFATTN_ERR_UNSUPPORTED unless
- * d == 64 and dtype is DIFFATTN_BF16, or DIFFATTN_E4M3_QK with headnorm 0 or 1,
- * or on a non-sm_103 device.
+ * dtype is DIFFATTN_BF16 with d == 64, DIFFATTN_BF16 with d == 128 and splits
+ * 0 or 1, or DIFFATTN_E4M3_QK with d == 64 and headnorm 0 or 1; and on a
+ * non-sm_103 device.
  * B * H * N == 0 returns DIFFATTN_OK without launching anything.
  */
 diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const void *q1,
@@ -199,8 +203,9 @@ diffattn_status diffattn_fwd_kv(const diffattn_desc *desc, int64_t n_kv, const v
  *
  * strides[0..5] are those of q1, k1, q2, k2, v, out, in elements, with the
  * rules of diffattn_fwd_strided (contiguous rows; every stride a positive
- * multiple of 8 elements and below 2^39).  Domain: DIFFATTN_BF16, d == 64;
- * other arguments, the workspace and the errors as for diffattn_fwd_kv.
+ * multiple of 8 elements and below 2^39).  Domain: DIFFATTN_BF16, d == 64 or
+ * d == 128 (splits 0 or 1); other arguments, the workspace and the errors as
+ * for diffattn_fwd_kv.
  */
 diffattn_status diffattn_fwd_kv_strided(const diffattn_desc *desc, int64_t n_kv,
                                         const void *q1, const void *k1, const void *q2,

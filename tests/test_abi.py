@@ -159,7 +159,13 @@ def test_kv_validation(lib):
     f32 = ops.make_desc(1, 4, 64, 8, ops.F32, True, True, 1e-5, 0.2)
     assert _plan(lib, f32, 64, 1)[0] == ops.ERR_UNSUPPORTED
     wide = ops.make_desc(1, 4, 64, 128, ops.BF16, True, True, 1e-5, 0.2)
-    assert _plan(lib, wide, 64, 1)[0] == ops.ERR_UNSUPPORTED
+    assert _plan(lib, wide, 64, 1)[:2] == (ops.OK, 1)             # d = 128: single pass
+    assert _plan(lib, wide, 4096, 0)[:2] == (ops.OK, 1)           # the library picks 1
+    assert _plan(lib, wide, 4096, 2)[0] == ops.ERR_UNSUPPORTED    # no split-KV at d = 128
+    wide8 = ops.make_desc(1, 4, 64, 128, ops.E4M3_QK, True, True, 1e-5, 0.2)
+    assert _plan(lib, wide8, 64, 1)[0] == ops.ERR_UNSUPPORTED
+    odd = ops.make_desc(1, 4, 64, 96, ops.BF16, True, True, 1e-5, 0.2)
+    assert _plan(lib, odd, 64, 1)[0] == ops.ERR_UNSUPPORTED
     assert lib.diffattn_fwd_kv_plan(ctypes.byref(d), 512, 1, None, None) == ops.ERR_INVALID_ARG
     # split launches need a large enough, aligned workspace (checked before any launch)
     assert _call_kv(lib, d, 512, 2, ws=0) == ops.ERR_INVALID_ARG

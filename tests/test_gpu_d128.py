@@ -48,3 +48,28 @@ def test_d128_long_sampled():
     bh, ri = harness.sample_rows(w, 48, full_heads=(1,))
     got = gpu.view(-1, w.N, 2 * w.d)[torch.from_numpy(bh).cuda(), torch.from_numpy(ri).cuda()]
     _cmp(got, harness.run_oracle_rows(w, bh, ri), "d128 N=4096 sampled")
+
+
+@pytest.mark.parametrize("Nq,Nkv,causal", [(1, 4000, True), (16, 1000, True), (200, 700, True),
+                                           (130, 130, True), (40, 300, False)])
+@pytest.mark.parametrize("headnorm", [1, 2])
+def test_d128_kv_cache(Nq, Nkv, causal, headnorm):
+    """diffattn_fwd_kv with d = 128: queries at the last Nq of Nkv positions (single
+    pass), against the oracle's key/value-cache form."""
+    w = W.kv_cache(950 + Nq, B=2, H=2, Nq=Nq, Nkv=Nkv, d=128, causal=causal, headnorm=headnorm)
+    _cmp(harness.run_gpu_kv(w, splits=0), harness.run_oracle_kv(w), f"d128 kv {Nq}/{Nkv}")
+
+
+def test_d128_kv_square_is_the_plain_forward():
+    w = W.kv_cache(960, B=1, H=3, Nq=300, Nkv=300, d=128, causal=True)
+    a = harness.run_gpu_kv(w, splits=1)
+    b = harness.run_gpu(w)
+    assert torch.equal(a, b)
+
+
+def test_d128_kv_refuses_splits():
+    from differential_attention_attn_gb300 import ops
+    w = W.kv_cache(961, B=1, H=2, Nq=4, Nkv=1000, d=128, causal=True)
+    st = harness.run_gpu_kv(w, splits=2, raw_status=True)
+    assert st == ops.ERR_UNSUPPORTED
+    assert ops.fwd_kv_plan(1, 2, 4, 1000, causal=True, splits=0, d=128)[0] == 1
