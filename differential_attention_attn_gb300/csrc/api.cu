@@ -319,6 +319,7 @@ const char *diffattn_strerror(diffattn_status status) {
     case DIFFATTN_ERR_UNSUPPORTED: return "unsupported configuration";
     case DIFFATTN_ERR_CUDA: return "CUDA error";
     case DIFFATTN_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case DIFFATTN_ERR_BOUNDS: return "kernel bounds check failed (debug build)";
   }
   return "unknown status";
 }

@@ -39,6 +39,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "debug_check.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -519,7 +520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           transpose8_chunks(ch, lane);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            if (row0 + j < p.N)
+            if (row0 + j < p.N &&
+                dbg_ok(row0 + j >= 0 && 32 * half + 4 * (lane & 7) + 4 <= HD, p.status, 40))
               red_add_v4(col_base + static_cast<int64_t>(row0 + j) * HD + 32 * half,
                          __uint_as_float(ch[j].x), __uint_as_float(ch[j].y),
                          __uint_as_float(ch[j].z), __uint_as_float(ch[j].w));
@@ -554,7 +556,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         transpose8_chunks(ch, lane);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (krow0 + j < p.N)
+          if (krow0 + j < p.N &&
+              dbg_ok(krow0 + j >= 0 && 32 * bk + 4 * (lane & 7) + 4 <= DV, p.status, 41))
             red_add_v4(dv_col + static_cast<int64_t>(krow0 + j) * DV + 32 * bk,
                        __uint_as_float(ch[j].x), __uint_as_float(ch[j].y),
                        __uint_as_float(ch[j].z), __uint_as_float(ch[j].w));
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 8 * (lane & 7);
 #pragma unroll
         for (int j2 = 0; j2 < 8; ++j2) {
-          if (krow0 + j2 < p.N)
+          if (krow0 + j2 < p.N && dbg_ok(krow0 + j2 >= 0 && 8 * (lane & 7) + 8 <= HD, p.status, 42))
             *reinterpret_cast<uint4 *>(dk_col + static_cast<int64_t>(krow0 + j2) * HD) = pkt[j2];
         }
       }
@@ -702,7 +705,7 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
       d1 = warp_sum(d1);
       d2 = warp_sum(d2);
     }
-    if (lane == 0) {  // c_k D_k: c_1 = 1, c_2 = -lambda
+    if (lane == 0 && dbg_ok(i < p.n_pad && bh < p.BH, nullptr, 43)) {  // c_k D_k: c_1 = 1, c_2 = -lambda
       p.dvec[bh * p.n_pad + i] = d1;
       p.dvec[(p.BH + bh) * p.n_pad + i] = -lam * d2;
     }

@@ -76,6 +76,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "debug_check.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -430,6 +431,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // The previous item's Q is dead once its last Q K^T MMAs completed.
           if (r > 0 && !(ok = mbar_wait(&ctrl->q_empty, (r - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
             break;
+          if (!dbg_ok(it.q0 >= 0 && it.q0 < p.N && it.h >= 0 && it.h < p.H &&
+                          it.bh >= 0 && it.bh < p.BH, p.status, 1))
+            break;
           mbar_arrive_expect_tx(&ctrl->q_full, 2 * QK_LOAD_BYTES);
           tma_load_4d(smem + OFF_Q1, &tm_q1, &ctrl->q_full, 0, it.q0, it.h, it.b);
           tma_load_4d(smem + OFF_Q2, &tm_q2, &ctrl->q_full, 0, it.q0, it.h, it.b);
@@ -442,6 +446,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             uint8_t *st = smem + OFF_STAGES + s * STAGE_BYTES;
             const int32_t y = (it.kv_lo + j) * BN;
+            if (!dbg_ok(s < STAGES && y >= 0 && y < p.n_ktiles * BN, p.status, 2)) {
+              ok = false;
+              break;
+            }
             mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * QK_LOAD_BYTES);
             tma_load_4d(st + STAGE_K1, &tm_k1, &ctrl->k_full[s], 0, y, it.h, it.b);
             tma_load_4d(st + STAGE_K2, &tm_k2, &ctrl->k_full[s], 0, y, it.h, it.b);
@@ -495,6 +503,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kk = 0; kk < 2; ++kk)
               umma_e4m3_ss_warp(tmem + tm_s(k), a + 2 * kk, b + 2 * kk, IDESC_QK8, kk > 0);
           } else {
+            if (!dbg_ok(s < STAGES && tmem_cols_ok(tmem + tm_s(k), BN, tmem, TMEM_COLS), p.status,
+                        3))
+              return;
             const uint32_t a = dq[k], b = dk[k] + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
@@ -504,6 +515,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // O_k += P_k V; 16 keys = 2048 bytes of V.  P_k's keys 0-63 are packed over
         // S_k columns 0-31 and keys 64-127 over columns 64-95.
         auto pv = [&](int k, int s, bool accumulate) {
+          if (!dbg_ok(s < STAGES && tmem_cols_ok(tmem + tm_o(k), DV, tmem, TMEM_COLS) &&
+                          tmem_cols_ok(tmem + tm_s(k), BN, tmem, TMEM_COLS),
+                      p.status, 4))
+            return;
           const uint32_t b = dvb + (static_cast<uint32_t>(s) * STAGE_BYTES >> 4);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
@@ -602,6 +617,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after_sync();
         const int lim = lim0 - j * BN;
         const bool masked = __any_sync(0xffffffffu, lim < BN - 1);
+        // This thread's S columns (two threads per lane: 64 apart) and its P.
+        if (!dbg_ok_warp(tmem_range_ok(t_s, BN, tmem, TMEM_COLS, warp, 16) &&
+                             tmem_range_ok(t_o, DV, tmem, TMEM_COLS, warp, 16),
+                         p.status, 5)) {
+          ok = false;
+          break;
+        }
         uint32_t pk[BN / 4];
         float tile_sum = 0.f;
         // Steady state: exponentials against the current reference maximum; a
@@ -667,6 +689,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (ok) ok = mbar_wait(&ctrl->o_done, ri & 1, abort_flag, WAIT_TIMEOUT_NS);
       const float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // both halves
       const float inv = 1.f / l_row;
+      if (!dbg_ok(r >= 0 && r < BM && (!w_mine || quarter * 32 + lane < DV), p.status, 6))
+        ok = false;
       if (!kPartial) {
         // Published by the barrier below.  Every thread finished reading the
         // previous item's exchange before this item's o_done could complete
@@ -683,7 +707,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // column 64 further), as accumulated against the reference maximum, then that
         // maximum and the running sum.
         float *blk = p.part + static_cast<int64_t>(blockIdx.x) * PART_FLOATS + k * PART_MAP_FLOATS;
-        const bool real = it.q0 + r < p.N;
+        const bool real = dbg_ok(key0 + DV / 2 <= DV && r < BM, p.status, 7) && it.q0 + r < p.N;
 #pragma unroll 1
         for (int c0 = 0; c0 < DV / 2; c0 += 32) {
           uint32_t v[32];
@@ -705,7 +729,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // (8 rows of one key half) so that every store writes four 128-byte row
         // segments.
         const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BM;
-        if (hc == 0) p.save_lse[(k * p.BH + it.bh) * n_pad + it.q0 + r] = m_run + __log2f(l_row);
+        if (hc == 0 && dbg_ok(it.q0 + r < n_pad && it.bh < p.BH, p.status, 8))
+          p.save_lse[(k * p.BH + it.bh) * n_pad + it.q0 + r] = m_run + __log2f(l_row);
         const int row0 = it.q0 + r - (lane & 7);  // the 8-lane group's first row
         float *so = p.save_o + (k * p.BH + it.bh) * static_cast<int64_t>(p.N) * DV + key0 +
                     4 * (lane & 7);
@@ -723,7 +748,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           transpose8_chunks(ch, lane);
 #pragma unroll
           for (int jr = 0; jr < 8; ++jr) {
-            if (row0 + jr < p.N)
+            if (row0 + jr < p.N &&
+                dbg_ok(row0 + jr >= 0 && key0 + c0 + 4 * (lane & 7) + 4 <= DV, p.status, 9))
               *reinterpret_cast<uint4 *>(so + static_cast<int64_t>(row0 + jr) * DV + c0) = ch[jr];
           }
         }
@@ -733,6 +759,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // This thread's 32 value columns: 64 hc + 32 k .. + 31, read from O1 and O2
       // through the two-threads-per-lane shape.
       const int col0 = key0 + 32 * k;
+      if (!dbg_ok_warp(tmem_range_ok(tmem + lane_addr + tm_o(0) + 32 * k, 96, tmem, TMEM_COLS,
+                                     warp, 16) &&
+                           tmem_range_ok(tmem + lane_addr + tm_o(1) + 32 * k, 96, tmem,
+                                         TMEM_COLS, warp, 16),
+                       p.status, 10))
+        break;
       float o[32];
       float ss = 0.f;
       {
@@ -805,7 +837,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __nv_bfloat16 *obase = p.out + it.b * p.out_sb + it.h * p.out_sh + col0 + 8 * (lane & 3);
 #pragma unroll
       for (int jr = 0; jr < 4; ++jr) {
-        if (row0 + jr < p.N)
+        if (row0 + jr < p.N &&
+            dbg_ok(row0 + jr >= 0 && col0 + 8 * (lane & 3) + 8 <= DV && it.b * p.H + it.h < p.BH,
+                   p.status, 11))
           *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row0 + jr) * p.out_sn) = pkt[jr];
       }
       // The next item writes xch and w_row only after its o_done, which needs

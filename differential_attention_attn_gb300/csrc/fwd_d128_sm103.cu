@@ -43,6 +43,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "debug_check.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -482,7 +483,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         transpose8_chunks(pkt, lane);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (row0 + j < p.N)
+          if (row0 + j < p.N && dbg_ok(row0 + j >= 0 && c64 + 8 * (lane & 7) + 8 <= DV, p.status, 50))
             *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(row0 + j) * p.out_sn + c64) =
                 pkt[j];
         }

@@ -22,6 +22,7 @@
 #include <functional>
 #include <vector>
 
+#include "debug_check.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -214,7 +215,9 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
     for (int c = 0; c < kColsPerThread; ++c) ov[c] *= rr * wv[c];
   }
-  if (real) {
+  if (real && dbg_ok(q >= 0 && col0 + kColsPerThread <= kValueCols &&
+                         item < p.BH * p.n_qtiles && used <= p.splits,
+                     const_cast<int32_t *>(p.status), 30)) {
     __nv_bfloat162 x[kColsPerThread / 2];
 #pragma unroll
     for (int c = 0; c < kColsPerThread / 2; ++c)

@@ -7,6 +7,7 @@ library has not been built, the first call raises; there is no fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -18,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdiffattn.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "diffattn.h")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = 0, 1, 2, 3, 4, 5
 BF16, F32, E4M3_QK = 0, 1, 2
 _DTYPE_CODE = {torch.bfloat16: BF16, torch.float32: F32}
 
@@ -57,49 +58,67 @@ def load(path: str = LIB_PATH):
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is missing: build it with "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
-        lib = ctypes.CDLL(path)
-        vp, fp = ctypes.c_void_p, ctypes.c_void_p
-        dp = ctypes.POINTER(Desc)
-        lib.diffattn_fwd.restype = ctypes.c_int
-        lib.diffattn_fwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp]
-        lib.diffattn_fwd_kv.restype = ctypes.c_int
-        lib.diffattn_fwd_kv.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp, vp,
-                                        ctypes.c_int, vp, ctypes.c_size_t, vp]
-        lib.diffattn_fwd_kv_plan.restype = ctypes.c_int
-        lib.diffattn_fwd_kv_plan.argtypes = [dp, ctypes.c_int64, ctypes.c_int,
-                                             ctypes.POINTER(ctypes.c_int),
-                                             ctypes.POINTER(ctypes.c_size_t)]
-        lib.diffattn_fwd_kv_noalloc.restype = ctypes.c_int
-        lib.diffattn_fwd_kv_noalloc.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
-                                                vp, ctypes.c_int, vp]
-        lib.diffattn_train_sizes.restype = ctypes.c_int
-        lib.diffattn_train_sizes.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t),
-                                             ctypes.POINTER(ctypes.c_size_t)]
-        lib.diffattn_fwd_train.restype = ctypes.c_int
-        lib.diffattn_fwd_train.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp,
-                                           ctypes.c_size_t, vp]
-        lib.diffattn_bwd.restype = ctypes.c_int
-        lib.diffattn_bwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp, vp,
-                                     fp, fp, vp, ctypes.c_size_t, vp]
-        lib.diffattn_fwd_strided.restype = ctypes.c_int
-        lib.diffattn_fwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp,
-                                             ctypes.POINTER(Strides), vp]
-        lib.diffattn_fwd_kv_strided.restype = ctypes.c_int
-        lib.diffattn_fwd_kv_strided.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
-                                                vp, ctypes.c_int, vp, ctypes.c_size_t,
-                                                ctypes.POINTER(Strides), vp]
-        lib.diffattn_selftest_wait.restype = ctypes.c_int
-        lib.diffattn_selftest_wait.argtypes = [vp, ctypes.c_int64, vp]
-        lib.diffattn_headnorm.restype = ctypes.c_int
-        lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
-        lib.diffattn_lambda_init.restype = ctypes.c_double
-        lib.diffattn_lambda_init.argtypes = [ctypes.c_int]
-        lib.diffattn_strerror.restype = ctypes.c_char_p
-        lib.diffattn_strerror.argtypes = [ctypes.c_int]
-        lib.diffattn_version.restype = ctypes.c_int
-        lib.diffattn_version.argtypes = []
-        _lib = lib
-        return lib
+        _lib = bind(ctypes.CDLL(path))
+        return _lib
+
+
+@contextlib.contextmanager
+def using(lib):
+    """Route this module's calls to another bound library (e.g. the
+    bounds-checked debug build) for the duration of a `with` block."""
+    global _lib
+    with _lock:
+        prev, _lib = _lib, lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def bind(lib):
+    """Declare the C signatures of include/diffattn.h on a loaded library."""
+    vp, fp = ctypes.c_void_p, ctypes.c_void_p
+    dp = ctypes.POINTER(Desc)
+    lib.diffattn_fwd.restype = ctypes.c_int
+    lib.diffattn_fwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp]
+    lib.diffattn_fwd_kv.restype = ctypes.c_int
+    lib.diffattn_fwd_kv.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp, vp,
+                                    ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.diffattn_fwd_kv_plan.restype = ctypes.c_int
+    lib.diffattn_fwd_kv_plan.argtypes = [dp, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.diffattn_fwd_kv_noalloc.restype = ctypes.c_int
+    lib.diffattn_fwd_kv_noalloc.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
+                                            vp, ctypes.c_int, vp]
+    lib.diffattn_train_sizes.restype = ctypes.c_int
+    lib.diffattn_train_sizes.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t),
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.diffattn_fwd_train.restype = ctypes.c_int
+    lib.diffattn_fwd_train.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp,
+                                       ctypes.c_size_t, vp]
+    lib.diffattn_bwd.restype = ctypes.c_int
+    lib.diffattn_bwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp, vp,
+                                 fp, fp, vp, ctypes.c_size_t, vp]
+    lib.diffattn_fwd_strided.restype = ctypes.c_int
+    lib.diffattn_fwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp,
+                                         ctypes.POINTER(Strides), vp]
+    lib.diffattn_fwd_kv_strided.restype = ctypes.c_int
+    lib.diffattn_fwd_kv_strided.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
+                                            vp, ctypes.c_int, vp, ctypes.c_size_t,
+                                            ctypes.POINTER(Strides), vp]
+    lib.diffattn_selftest_wait.restype = ctypes.c_int
+    lib.diffattn_selftest_wait.argtypes = [vp, ctypes.c_int64, vp]
+    lib.diffattn_headnorm.restype = ctypes.c_int
+    lib.diffattn_headnorm.argtypes = [dp, fp, fp, vp, vp]
+    lib.diffattn_lambda_init.restype = ctypes.c_double
+    lib.diffattn_lambda_init.argtypes = [ctypes.c_int]
+    lib.diffattn_strerror.restype = ctypes.c_char_p
+    lib.diffattn_strerror.argtypes = [ctypes.c_int]
+    lib.diffattn_version.restype = ctypes.c_int
+    lib.diffattn_version.argtypes = []
+    return lib
 
 
 def declared_symbols(header: str = HEADER_PATH) -> list[str]:

@@ -55,7 +55,11 @@ typedef enum diffattn_status {
     DIFFATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned buffer, bad dtype */
     DIFFATTN_ERR_UNSUPPORTED = 2, /* valid request outside the implemented domain */
     DIFFATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
-    DIFFATTN_ERR_TIMEOUT = 4      /* written to status_dev by a kernel whose wait ran out */
+    DIFFATTN_ERR_TIMEOUT = 4,     /* written to status_dev by a kernel whose wait ran out */
+    DIFFATTN_ERR_BOUNDS = 5       /* debug build only (compiled with DIFFATTN_DEBUG): a
+                                     kernel's bounds check failed; status_dev holds
+                                     5 | (site << 8) of the first failing check, and the
+                                     checked access was skipped */
 } diffattn_status;
 
 typedef enum diffattn_dtype {

@@ -264,3 +264,13 @@ def test_strided_domain_takes_both_head_widths(lib):
         st = lib.diffattn_fwd_strided(ctypes.byref(desc), f, f, f, f, f, f, None, misaligned,
                                       arr, None)
         assert st == (ops.ERR_INVALID_ARG if ok else ops.ERR_UNSUPPORTED), (d_half, st)
+
+
+def test_debug_build_exports_the_same_entry_points():
+    """The bounds-checked variant (DIFFATTN_DEBUG) builds and exports the same C ABI;
+    its strerror knows the bounds status (host-only, no GPU)."""
+    path = libbuild.build(debug=True)
+    dbg = ops.bind(ctypes.CDLL(path))
+    for n in EXPECTED_ENTRY_POINTS:
+        assert hasattr(dbg, n)
+    assert dbg.diffattn_strerror(ops.ERR_BOUNDS).decode() == "kernel bounds check failed (debug build)"
