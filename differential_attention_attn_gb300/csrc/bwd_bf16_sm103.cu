@@ -27,9 +27,10 @@
 //   3. diffattn_bwd_finish_kernel: fp32 accumulators -> bf16 gradients.
 //
 // Roles in kernel 2 (512 threads): warp 0 TMA producer; warp 1 TMEM
-// allocator and single MMA-issuing thread; warps 4-15 three warpgroups
-// (thread = key row) sharing the P^T / dS^T work of each tile by 16-query
-// chunks, the one with fewer chunks then draining dQ (thread = query row).
+// allocator and MMA issuer (the converged warp, one elected lane issuing);
+// warps 4-15 three warpgroups (thread = key row) sharing the P^T / dS^T work
+// of each tile by 16-query chunks in three published steps, the one with
+// fewer chunks also draining dQ (thread = query row).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -68,7 +69,7 @@ struct Ctrl {
   uint64_t qd_full[2];
   uint64_t qd_empty[2];
   uint64_t s_full;
-  uint64_t ds_ready;
+  uint64_t ds_ready[3];  // the three chunk steps of a tile
   uint64_t ds_free[2];
   uint64_t dq_full;
   uint64_t dq_free;
@@ -262,7 +263,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&ctrl->qd_empty[s], 1);
     }
     mbar_init(&ctrl->s_full, 1);
-    mbar_init(&ctrl->ds_ready, 384);
+    mbar_init(&ctrl->ds_ready[0], 384);
+    mbar_init(&ctrl->ds_ready[1], 384);
+    mbar_init(&ctrl->ds_ready[2], 256);
     mbar_init(&ctrl->ds_free[0], 1);
     mbar_init(&ctrl->ds_free[1], 1);
     mbar_init(&ctrl->dq_full, 1);
@@ -320,107 +323,110 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);   // S^T = K Q^T
-      constexpr uint32_t ID_W = idesc_ab(BK, BQ, false, false);   // dW^T = V dO^T
-      constexpr uint32_t ID_DV = idesc_ab(BK, DV, false, true);   // dV += P^T dO
-      constexpr uint32_t ID_DK = idesc_ab(BK, HD, false, true);   // dK += dS^T Q
-      constexpr uint32_t ID_DQ = idesc_ab(BQ, HD, true, true);    // dQ = dS K
-      const uint32_t s_k = smem_u32(smem + OFF_K), s_v = smem_u32(smem + OFF_V);
-      const uint32_t s_ds = smem_u32(smem + OFF_DS);
-      // K-major views (rows of 64 bf16): advance 32 bytes per 16 elements.
-      const uint64_t d_k_kmaj = smem_desc_sw128(s_k, 16, 1024);
-      const uint64_t d_v_kmaj = smem_desc_sw128(s_v, 16, 1024);
-      // MN-major views (64-wide blocks TILE64 apart): advance 2048 bytes per 16 rows.
-      const uint64_t d_k_mn = smem_desc_sw128(s_k, TILE64, 1024);
-      const uint64_t d_ds_mn = smem_desc_sw128(s_ds, TILE64, 1024);
-      // Adds a byte offset to a descriptor's start address.
-      auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-      auto stage_desc = [&](int st, bool k_major, bool is_do) {
-        const uint32_t base = is_do ? smem_u32(smem + OFF_DO + st * 2 * TILE64)
-                                    : smem_u32(smem + OFF_Q + st * TILE64);
-        return k_major ? smem_desc_sw128(base, 16, 1024) : smem_desc_sw128(base, TILE64, 1024);
-      };
-      // S^T = K Q^T (K = 64) and dW^T = V dO^T (K = 128: two 64-column boxes) of
-      // the query tile held in stage st.
-      auto issue_s_w = [&](int st) {
-        const uint64_t d_q = stage_desc(st, true, false), d_do = stage_desc(st, true, true);
+    // The whole warp walks the loop, so every operand is warp-uniform; one
+    // elected lane issues each MMA and commit (the same lane throughout).
+    constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);   // S^T = K Q^T
+    constexpr uint32_t ID_W = idesc_ab(BK, BQ, false, false);   // dW^T = V dO^T
+    constexpr uint32_t ID_DV = idesc_ab(BK, DV, false, true);   // dV += P^T dO
+    constexpr uint32_t ID_DK = idesc_ab(BK, HD, false, true);   // dK += dS^T Q
+    constexpr uint32_t ID_DQ = idesc_ab(BQ, HD, true, true);    // dQ = dS K
+    const uint32_t s_k = smem_u32(smem + OFF_K), s_v = smem_u32(smem + OFF_V);
+    const uint32_t s_ds = smem_u32(smem + OFF_DS);
+    // Every operand is a base tile plus a byte offset below 256 KB, so advancing
+    // it adds offset >> 4 to the start-address field of the descriptor's low
+    // word; all of them share the high word (stride offset 1024, version,
+    // 128-byte swizzle).
+    auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
+    const uint32_t dhi = static_cast<uint32_t>(smem_desc_sw128(s_k, 16, 1024) >> 32);
+    // K-major views (rows of 64 bf16): advance 32 bytes per 16 elements.
+    const uint32_t d_k_kmaj = lo(smem_desc_sw128(s_k, 16, 1024));
+    const uint32_t d_v_kmaj = lo(smem_desc_sw128(s_v, 16, 1024));
+    // MN-major views (64-wide blocks TILE64 apart): advance 2048 bytes per 16 rows.
+    const uint32_t d_k_mn = lo(smem_desc_sw128(s_k, TILE64, 1024));
+    const uint32_t d_ds_mn = lo(smem_desc_sw128(s_ds, TILE64, 1024));
+    auto stage_desc = [&](int st, bool k_major, bool is_do) {
+      const uint32_t base = is_do ? smem_u32(smem + OFF_DO + st * 2 * TILE64)
+                                  : smem_u32(smem + OFF_Q + st * TILE64);
+      return lo(k_major ? smem_desc_sw128(base, 16, 1024) : smem_desc_sw128(base, TILE64, 1024));
+    };
+    // S^T = K Q^T (K = 64) and dW^T = V dO^T (K = 128: two 64-column boxes) of
+    // the query tile held in stage st.
+    auto issue_s_w = [&](int st) {
+      const uint32_t d_q = stage_desc(st, true, false), d_do = stage_desc(st, true, true);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss(tmem + TM_S, adv(d_k_kmaj, 32 * kk), adv(d_q, 32 * kk), ID_S, kk > 0);
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16_ss_lo_warp(tmem + TM_S, d_k_kmaj + 2 * kk, d_q + 2 * kk, dhi, ID_S, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * TILE64 + 32 * (kk & 3);
-          umma_bf16_ss(tmem + TM_W, adv(d_v_kmaj, off), adv(d_do, off), ID_W, kk > 0);
-        }
-        umma_commit(&ctrl->s_full);
-      };
-      // Order per query tile i: dV_i and dK_i (A operands from TMEM), dQ_i
-      // (from shared memory), then S and dW of tile i+1.  Issuing tile i+1's S
-      // and dW before dQ_i lets its P^T / dS^T work overlap dQ_i, but measured
-      // slower: that work then shares shared-memory bandwidth with the SS MMA.
-      bool ok = mbar_wait(&ctrl->kv_full, 0, abort_flag, WAIT_TIMEOUT_NS) &&
-                mbar_wait(&ctrl->qd_full[0], 0, abort_flag, WAIT_TIMEOUT_NS);
-      tc_fence_after_sync();
-      if (ok) issue_s_w(0);
-      for (int it = 0; ok && it < n_q; ++it) {
-        const int s = it & 1;  // Q / dO stage and dS^T buffer of tile it
-        if (!(ok = mbar_wait(&ctrl->ds_ready, it & 1, abort_flag, WAIT_TIMEOUT_NS))) break;
-        tc_fence_after_sync();
-        // dV += P^T dO (c applied at the end): A = packed P^T in TMEM (queries
-        // 16c .. 16c+15 at columns 16c .. 16c+7), B = dO MN-major (K = queries).
-        const uint64_t d_do_mn = stage_desc(s, false, true);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t pcol = 16 * kk;  // chunk kk's packed columns
-          umma_bf16_ts(tmem + TM_DV, tmem + TM_S + pcol, adv(d_do_mn, 2048 * kk), ID_DV,
-                       (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        // dK += dS^T Q: A = packed dS^T in TMEM over the dW^T columns (same column
-        // map as P^T), B = Q MN-major (N = 64).
-        const uint64_t d_q_mn = stage_desc(s, false, false);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t pcol = 16 * kk;  // chunk kk's packed columns
-          umma_bf16_ts(tmem + TM_DK, tmem + TM_W + pcol, adv(d_q_mn, 2048 * kk), ID_DK,
-                       (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        const uint64_t d_ds_m = adv(d_ds_mn, s * DS_BYTES);
-        // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (K = keys).
-        if (it > 0 && !(ok = mbar_wait(&ctrl->dq_free, (it - 1) & 1, abort_flag,
-                                       WAIT_TIMEOUT_NS)))
-          break;
+      for (int kk = 0; kk < DV / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * TILE64 + 32 * (kk & 3)) >> 4;
+        umma_bf16_ss_lo_warp(tmem + TM_W, d_v_kmaj + off, d_do + off, dhi, ID_W, kk > 0);
+      }
+      umma_commit_warp(&ctrl->s_full);
+    };
+    // The 16 queries of chunk c (the K slice of both products): dV += P^T dO,
+    // A = packed P^T over S^T columns 16c .. 16c+7, B = dO MN-major; dK +=
+    // dS^T Q, A = packed dS^T over dW^T columns 16c .. 16c+7, B = Q MN-major.
+    auto issue_dv_dk = [&](int st, int c, uint32_t acc) {
+      const uint32_t off = (2048u * c) >> 4;
+      umma_bf16_ts_lo_warp(tmem + TM_DV, tmem + TM_S + 16 * c, stage_desc(st, false, true) + off,
+                           dhi, ID_DV, acc);
+      umma_bf16_ts_lo_warp(tmem + TM_DK, tmem + TM_W + 16 * c,
+                           stage_desc(st, false, false) + off, dhi, ID_DK, acc);
+    };
+    auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, WAIT_TIMEOUT_NS));
+    };
+    // Order per query tile i: dV_i and dK_i chunk by chunk as the P^T / dS^T
+    // warps publish them (three steps), then S^T and dW^T of tile i+1 (over
+    // the packed P^T_i and dS^T_i, after the MMAs that read them), then dQ_i,
+    // which runs while the warps start on tile i+1.
+    bool ok = wait_all(&ctrl->kv_full, 0) && wait_all(&ctrl->qd_full[0], 0);
+    tc_fence_after_sync();
+    if (ok) issue_s_w(0);
+    for (int it = 0; ok && it < n_q; ++it) {
+      const int s = it & 1;  // Q / dO stage and dS^T buffer of tile it
+      for (int step = 0; ok && step < 3; ++step) {
+        if (!(ok = wait_all(&ctrl->ds_ready[step], it & 1))) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_bf16_ss(tmem + TM_DQ, adv(d_ds_m, 2048 * kk), adv(d_k_mn, 2048 * kk), ID_DQ,
-                       kk > 0);
-        umma_commit(&ctrl->dq_full);
-        umma_commit(&ctrl->qd_empty[s]);
-        umma_commit(&ctrl->ds_free[s]);
-        if (it + 1 < n_q) {
-          const int s1 = (it + 1) & 1;
-          if (!(ok = mbar_wait(&ctrl->qd_full[s1], ((it + 1) >> 1) & 1, abort_flag,
-                               WAIT_TIMEOUT_NS)))
-            break;
-          tc_fence_after_sync();
-          issue_s_w(s1);  // overwrites P^T_i and dS^T_i after dV_i, dK_i (in-order)
+        for (int j = 0; j < 3; ++j) {
+          const int c = 3 * step + j;
+          if (c < BQ / 16) issue_dv_dk(s, c, (it > 0 || c > 0) ? 1u : 0u);
         }
       }
-      if (ok) umma_commit(&ctrl->acc_done);
-      umma_commit(&ctrl->drain);
-      drain_wait(&ctrl->drain, 0);
+      if (!ok) break;
+      umma_commit_warp(&ctrl->qd_empty[s]);  // the last reads of Q_i and dO_i
+      if (it + 1 < n_q) {
+        const int s1 = s ^ 1;
+        if (!(ok = wait_all(&ctrl->qd_full[s1], ((it + 1) >> 1) & 1))) break;
+        tc_fence_after_sync();
+        issue_s_w(s1);
+      }
+      // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (K = keys).
+      if (it > 0 && !(ok = wait_all(&ctrl->dq_free, (it - 1) & 1))) break;
+      tc_fence_after_sync();
+      const uint32_t d_ds = d_ds_mn + ((s * DS_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        umma_bf16_ss_lo_warp(tmem + TM_DQ, d_ds + 128 * kk, d_k_mn + 128 * kk, dhi, ID_DQ, kk > 0);
+      umma_commit_warp(&ctrl->dq_full);
+      umma_commit_warp(&ctrl->ds_free[s]);
     }
+    if (ok) umma_commit_warp(&ctrl->acc_done);
+    umma_commit_warp(&ctrl->drain);
+    drain_wait(&ctrl->drain, 0);
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- P^T, dS^T, dQ drain
-    // Three warpgroups share the eight 16-query chunks of a tile: group g takes
-    // chunks [c_lo, c_hi) = [0, 3), [3, 6), [6, 8).  Chunk c leaves its packed
+    // Three warpgroups share the eight 16-query chunks of a tile in three
+    // steps: in step t group g takes chunk 3t + g (step 2 has chunks 6 and 7,
+    // for groups 0 and 1), and each step is published as soon as it is done so
+    // that its dV and dK MMAs overlap the next step.  Chunk c leaves its packed
     // P^T over S^T columns 16c .. 16c+7 and its packed dS^T over dW^T columns
-    // 16c .. 16c+7 (both already read), and dS^T in shared memory for dQ.
-    // Group 2 (two chunks) then drains dQ while the next tile's S^T and dW^T run.
+    // 16c .. 16c+7 (both already read, by the same thread), and dS^T in shared
+    // memory for dQ.  Group 2, with one chunk fewer, drains dQ of the previous
+    // tile after its second step.
     const int g = (warp - 4) / 4;
-    const int c_lo = 3 * g, c_hi = (g == 2) ? 8 : 3 * g + 3;
     const int kr = (warp % 4) * 32 + lane;  // key row (dQ: query row) = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + TM_S;
@@ -431,12 +437,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool key_ok = kpos < p.N;
     const bool key_tile_ragged = k0 + BK > p.N;
     float *dq_base = p.dq_acc + (map * p.BH + bh) * static_cast<int64_t>(p.N) * HD;
+    // dQ of query tile t into the fp32 accumulator (thread = query row).
+    auto drain_dq = [&](int t) {
+      bool okd = mbar_wait(&ctrl->dq_full, t & 1, abort_flag, WAIT_TIMEOUT_NS);
+      okd = __all_sync(0xffffffffu, okd);
+      if (!okd) return false;
+      tc_fence_after_sync();
+      uint32_t a[32], b[32];
+      tmem_ld_x32_nowait(tmem + lane_addr + TM_DQ, a);
+      tmem_ld_x32_nowait(tmem + lane_addr + TM_DQ + 32, b);
+      tmem_ld_wait_x32(a);
+      tmem_ld_wait_x32(b);
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->dq_free);
+      // dQ rows, transposed across each 8-lane group so that every vector
+      // reduction covers four 128-byte row segments (one row per lane made
+      // each instruction touch 32 rows).
+      const int q0 = (qt_first + t) * BQ;
+      const int row0 = q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
+      float *col_base = dq_base + 4 * (lane & 7);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t(&src)[32] = half ? b : a;
+        uint4 ch[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          ch[v] = make_uint4(__float_as_uint(__uint_as_float(src[4 * v]) * p.scale),
+                             __float_as_uint(__uint_as_float(src[4 * v + 1]) * p.scale),
+                             __float_as_uint(__uint_as_float(src[4 * v + 2]) * p.scale),
+                             __float_as_uint(__uint_as_float(src[4 * v + 3]) * p.scale));
+        transpose8_chunks(ch, lane);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (row0 + j < p.N &&
+              dbg_ok(row0 + j >= 0 && 32 * half + 4 * (lane & 7) + 4 <= HD, p.status, 40))
+            red_add_v4(col_base + static_cast<int64_t>(row0 + j) * HD + 32 * half,
+                       __uint_as_float(ch[j].x), __uint_as_float(ch[j].y),
+                       __uint_as_float(ch[j].z), __uint_as_float(ch[j].w));
+        }
+      }
+      return true;
+    };
+    // Packed P^T and dS^T in tensor memory and dS^T in shared memory visible
+    // to the MMAs, then step `step` of this thread is published.
+    auto publish = [&](int step) {
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->ds_ready[step]);
+    };
     bool ok = true;
     for (int it = 0; it < n_q; ++it) {
       const int s = it & 1;
       const int q0 = (qt_first + it) * BQ;
       ok = mbar_wait(&ctrl->s_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
-      // dS^T buffer s was last read by the dK / dQ MMAs of tile it - 2.
+      // dS^T buffer s was last read by the dQ MMAs of tile it - 2.
       if (ok && it >= 2)
         ok = mbar_wait(&ctrl->ds_free[s], ((it >> 1) - 1) & 1, abort_flag, WAIT_TIMEOUT_NS);
       ok = __all_sync(0xffffffffu, ok);
@@ -466,69 +521,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *reinterpret_cast<uint4 *>(sub + sw128(kr, (c & 3) * 2 + j)) = v4;
         }
       };
-      // Loads of the third chunk overlap the work on the second.
+      // Loads of each step's chunk overlap the work on the one before.
+      const int c_a = g, c_b = g + 3, c_c = g + 6;
+      const bool third = c_c < BQ / 16;  // uniform per warp
       uint32_t xa[16], wa[16], xb[16], wb[16];
-      tmem_ld16(t_s + 16 * c_lo, xa);
-      tmem_ld16(t_w + 16 * c_lo, wa);
-      tmem_ld16(t_s + 16 * (c_lo + 1), xb);
-      tmem_ld16(t_w + 16 * (c_lo + 1), wb);
+      tmem_ld16(t_s + 16 * c_a, xa);
+      tmem_ld16(t_w + 16 * c_a, wa);
+      tmem_ld16(t_s + 16 * c_b, xb);
+      tmem_ld16(t_w + 16 * c_b, wb);
       tmem_wait16x4(xa, wa, xb, wb);
-      work(xa, wa, c_lo);
-      const bool third = c_lo + 2 < c_hi;  // uniform per warp
+      work(xa, wa, c_a);
+      publish(0);
       if (third) {
-        tmem_ld16(t_s + 16 * (c_lo + 2), xa);
-        tmem_ld16(t_w + 16 * (c_lo + 2), wa);
+        tmem_ld16(t_s + 16 * c_c, xa);
+        tmem_ld16(t_w + 16 * c_c, wa);
       }
-      work(xb, wb, c_lo + 1);
+      work(xb, wb, c_b);
+      publish(1);
       if (third) {
         tmem_wait16x4(xa, wa, xb, wb);
-        work(xa, wa, c_lo + 2);
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before_sync();
-      mbar_arrive(&ctrl->ds_ready);
-      if (g == 2) {
-        // dQ of this tile into the fp32 accumulator, by the group with the
-        // fewest chunks, while the next tile's S^T and dW^T run.
-        ok = mbar_wait(&ctrl->dq_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after_sync();
-        uint32_t a[32], b[32];
-        tmem_ld_x32_nowait(tmem + lane_addr + TM_DQ, a);
-        tmem_ld_x32_nowait(tmem + lane_addr + TM_DQ + 32, b);
-        tmem_ld_wait_x32(a);
-        tmem_ld_wait_x32(b);
-        tc_fence_before_sync();
-        mbar_arrive(&ctrl->dq_free);
-        // dQ rows, transposed across each 8-lane group so that every vector
-        // reduction covers four 128-byte row segments (one row per lane made
-        // each instruction touch 32 rows).
-        const int row0 = q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
-        float *col_base = dq_base + 4 * (lane & 7);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t(&src)[32] = half ? b : a;
-          uint4 ch[8];
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            ch[v] = make_uint4(__float_as_uint(__uint_as_float(src[4 * v]) * p.scale),
-                               __float_as_uint(__uint_as_float(src[4 * v + 1]) * p.scale),
-                               __float_as_uint(__uint_as_float(src[4 * v + 2]) * p.scale),
-                               __float_as_uint(__uint_as_float(src[4 * v + 3]) * p.scale));
-          transpose8_chunks(ch, lane);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (row0 + j < p.N &&
-                dbg_ok(row0 + j >= 0 && 32 * half + 4 * (lane & 7) + 4 <= HD, p.status, 40))
-              red_add_v4(col_base + static_cast<int64_t>(row0 + j) * HD + 32 * half,
-                         __uint_as_float(ch[j].x), __uint_as_float(ch[j].y),
-                         __uint_as_float(ch[j].z), __uint_as_float(ch[j].w));
-          }
-        }
+        work(xa, wa, c_c);
+        publish(2);
+      } else if (it > 0 && !(ok = drain_dq(it - 1))) {
+        break;
       }
     }
+    if (ok && g == 2) ok = drain_dq(n_q - 1);
     // ---------------------------------------------------------------- dV, dK out
     if (ok) ok = mbar_wait(&ctrl->acc_done, 0, abort_flag, WAIT_TIMEOUT_NS);
     // Warp-uniform decision: the TMEM loads below are warp-collective.
