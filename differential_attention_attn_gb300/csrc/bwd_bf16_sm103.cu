@@ -84,6 +84,16 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(SMEM_BYTES + 1024 < (1u << 18), "descriptor start addresses must stay below 256 KB");
 
 constexpr uint32_t TM_S = 0, TM_W = 128, TM_DV = 256, TM_DK = 384, TM_DQ = 448;
+// Packed (2 bf16 per column) P^T and dS^T of 16-query chunk c.  P^T goes
+// over the first half of the chunk's S^T columns; dS^T over the first half of
+// its dW^T columns for chunks 0-5, and over the second half of its S^T columns
+// for chunks 6 and 7, so that dW^T of the next tile can be written while
+// chunks 6 and 7 are computed.  Either way a thread overwrites only columns of
+// its own lane that it has already read.
+__host__ __device__ constexpr uint32_t tm_p(int c) { return TM_S + 16 * c; }
+__host__ __device__ constexpr uint32_t tm_ds(int c) {
+  return c < 6 ? TM_W + 16 * c : TM_S + 16 * c + 8;
+}
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_TIMEOUT_NS = 200000000ull;
 
@@ -351,38 +361,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     // S^T = K Q^T (K = 64) and dW^T = V dO^T (K = 128: two 64-column boxes) of
     // the query tile held in stage st.
-    auto issue_s_w = [&](int st) {
-      const uint32_t d_q = stage_desc(st, true, false), d_do = stage_desc(st, true, true);
+    auto issue_s = [&](int st) {
+      const uint32_t d_q = stage_desc(st, true, false);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
         umma_bf16_ss_lo_warp(tmem + TM_S, d_k_kmaj + 2 * kk, d_q + 2 * kk, dhi, ID_S, kk > 0);
+    };
+    auto issue_w = [&](int st) {
+      const uint32_t d_do = stage_desc(st, true, true);
 #pragma unroll
       for (int kk = 0; kk < DV / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * TILE64 + 32 * (kk & 3)) >> 4;
         umma_bf16_ss_lo_warp(tmem + TM_W, d_v_kmaj + off, d_do + off, dhi, ID_W, kk > 0);
       }
-      umma_commit_warp(&ctrl->s_full);
     };
     // The 16 queries of chunk c (the K slice of both products): dV += P^T dO,
-    // A = packed P^T over S^T columns 16c .. 16c+7, B = dO MN-major; dK +=
-    // dS^T Q, A = packed dS^T over dW^T columns 16c .. 16c+7, B = Q MN-major.
+    // A = packed P^T, B = dO MN-major; dK += dS^T Q, A = packed dS^T, B = Q
+    // MN-major.  The packed operands sit at tm_p(c) and tm_ds(c).
     auto issue_dv_dk = [&](int st, int c, uint32_t acc) {
       const uint32_t off = (2048u * c) >> 4;
-      umma_bf16_ts_lo_warp(tmem + TM_DV, tmem + TM_S + 16 * c, stage_desc(st, false, true) + off,
-                           dhi, ID_DV, acc);
-      umma_bf16_ts_lo_warp(tmem + TM_DK, tmem + TM_W + 16 * c,
-                           stage_desc(st, false, false) + off, dhi, ID_DK, acc);
+      umma_bf16_ts_lo_warp(tmem + TM_DV, tmem + tm_p(c), stage_desc(st, false, true) + off, dhi,
+                           ID_DV, acc);
+      umma_bf16_ts_lo_warp(tmem + TM_DK, tmem + tm_ds(c), stage_desc(st, false, false) + off,
+                           dhi, ID_DK, acc);
     };
     auto wait_all = [&](uint64_t *bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, WAIT_TIMEOUT_NS));
     };
     // Order per query tile i: dV_i and dK_i chunk by chunk as the P^T / dS^T
-    // warps publish them (three steps), then S^T and dW^T of tile i+1 (over
-    // the packed P^T_i and dS^T_i, after the MMAs that read them), then dQ_i,
-    // which runs while the warps start on tile i+1.
+    // warps publish them (three steps).  Step 1 also means that every dW^T_i
+    // column has been read and that the packed dS^T in the dW^T columns is
+    // consumed by the MMAs issued so far, so dW^T of tile i+1 follows the
+    // chunks of step 1 while the warps compute step 2; S^T of tile i+1 follows
+    // the chunks of step 2; then dQ_i, which runs while the warps start on
+    // tile i+1.
     bool ok = wait_all(&ctrl->kv_full, 0) && wait_all(&ctrl->qd_full[0], 0);
     tc_fence_after_sync();
-    if (ok) issue_s_w(0);
+    if (ok) {
+      issue_w(0);
+      issue_s(0);
+      umma_commit_warp(&ctrl->s_full);
+    }
     for (int it = 0; ok && it < n_q; ++it) {
       const int s = it & 1;  // Q / dO stage and dS^T buffer of tile it
       for (int step = 0; ok && step < 3; ++step) {
@@ -393,15 +412,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int c = 3 * step + j;
           if (c < BQ / 16) issue_dv_dk(s, c, (it > 0 || c > 0) ? 1u : 0u);
         }
+        if (it + 1 < n_q) {
+          const int s1 = s ^ 1;
+          if (step == 1) {
+            if (!(ok = wait_all(&ctrl->qd_full[s1], ((it + 1) >> 1) & 1))) break;
+            tc_fence_after_sync();
+            issue_w(s1);
+          } else if (step == 2) {
+            issue_s(s1);
+            umma_commit_warp(&ctrl->s_full);
+          }
+        }
       }
       if (!ok) break;
       umma_commit_warp(&ctrl->qd_empty[s]);  // the last reads of Q_i and dO_i
-      if (it + 1 < n_q) {
-        const int s1 = s ^ 1;
-        if (!(ok = wait_all(&ctrl->qd_full[s1], ((it + 1) >> 1) & 1))) break;
-        tc_fence_after_sync();
-        issue_s_w(s1);
-      }
       // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (K = keys).
       if (it > 0 && !(ok = wait_all(&ctrl->dq_free, (it - 1) & 1))) break;
       tc_fence_after_sync();
@@ -421,16 +445,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Three warpgroups share the eight 16-query chunks of a tile in three
     // steps: in step t group g takes chunk 3t + g (step 2 has chunks 6 and 7,
     // for groups 0 and 1), and each step is published as soon as it is done so
-    // that its dV and dK MMAs overlap the next step.  Chunk c leaves its packed
-    // P^T over S^T columns 16c .. 16c+7 and its packed dS^T over dW^T columns
-    // 16c .. 16c+7 (both already read, by the same thread), and dS^T in shared
-    // memory for dQ.  Group 2, with one chunk fewer, drains dQ of the previous
+    // that its dV and dK MMAs overlap the next step.  Chunk c leaves packed
+    // P^T and dS^T at tm_p(c) and tm_ds(c), and dS^T in shared memory for dQ.
+    // Step 1 is published only once the step-2 chunk's S^T and dW^T are in
+    // registers.  Group 2, with one chunk fewer, drains dQ of the previous
     // tile after its second step.
     const int g = (warp - 4) / 4;
     const int kr = (warp % 4) * 32 + lane;  // key row (dQ: query row) = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t t_s = tmem + lane_addr + TM_S;
-    const uint32_t t_w = tmem + lane_addr + TM_W;
+    const uint32_t t_lane = tmem + lane_addr;
+    const uint32_t t_s = t_lane + TM_S;
+    const uint32_t t_w = t_lane + TM_W;
     const float coef = map ? -p.lambda[h] : 1.f;
     const float sl2 = p.scale_log2;
     const int kpos = k0 + kr;
@@ -512,8 +537,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bwd_chunk<true, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
         else
           bwd_chunk<false, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
-        tmem_st8(t_s + c0, pk);
-        tmem_st8(t_w + c0, dk);
+        tmem_st8(t_lane + tm_p(c), pk);
+        tmem_st8(t_lane + tm_ds(c), dk);
         uint8_t *sub = ds_buf + (c >> 2) * TILE64;  // 64-query half of the dS^T tile
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -537,9 +562,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld16(t_w + 16 * c_c, wa);
       }
       work(xb, wb, c_b);
+      if (third) tmem_wait16x4(xa, wa, xb, wb);
       publish(1);
       if (third) {
-        tmem_wait16x4(xa, wa, xb, wb);
         work(xa, wa, c_c);
         publish(2);
       } else if (it > 0 && !(ok = drain_dq(it - 1))) {
