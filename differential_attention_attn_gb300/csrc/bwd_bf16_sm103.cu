@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include <cmath>
@@ -66,6 +67,7 @@ constexpr uint32_t OFF_CTRL = OFF_VEC + 2 * VEC_BYTES;
 
 struct Ctrl {
   uint64_t kv_full;
+  uint64_t kv_empty;
   uint64_t qd_full[2];
   uint64_t qd_empty[2];
   uint64_t s_full;
@@ -74,6 +76,7 @@ struct Ctrl {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t acc_done;
+  uint64_t acc_free;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -100,6 +103,7 @@ constexpr uint64_t DRAIN_TIMEOUT_NS = 200000000ull;
 struct BwdParams {
   int64_t BH;
   int32_t H, N, n_qtiles, n_ktiles, causal;
+  int64_t n_items;  // 2 * BH * n_ktiles
   float scale_log2;  // log2(e) / sqrt(d)
   float scale;       // 1 / sqrt(d)
   const float *lambda;
@@ -235,7 +239,42 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&x)[W], const uint32_t
   }
 }
 
+// One work item: a (128-key tile, head, map) of the backward.  Items are
+// numbered heaviest first (under the causal mask key tile 0 sees every query
+// tile): item j is key tile j / (2 BH), head (j / 2) % BH, map j % 2.
+struct Item {
+  int map, kt, h, k0, qt_first, n_q;
+  int64_t bh;
+};
+
+__device__ __forceinline__ Item item_at(const BwdParams &p, int64_t j) {
+  Item w;
+  w.map = static_cast<int>(j & 1);
+  w.kt = static_cast<int>((j >> 1) / p.BH);
+  w.bh = (j >> 1) % p.BH;
+  w.h = static_cast<int>(w.bh % p.H);
+  w.k0 = w.kt * BK;
+  w.qt_first = p.causal ? w.kt : 0;
+  w.n_q = p.n_qtiles - w.qt_first;
+  return w;
+}
+
+// The r-th item of this CTA: items are dealt to the persistent CTAs in rounds
+// of gridDim.x, in alternating direction (so that the CTA that got the
+// lightest item of one round gets the heaviest of the next).
+__device__ __forceinline__ bool next_item(const BwdParams &p, int r, Item &w) {
+  const int64_t G = gridDim.x;
+  const int64_t c = (r & 1) ? (G - 1 - blockIdx.x) : blockIdx.x;
+  const int64_t j = static_cast<int64_t>(r) * G + c;
+  if (j >= p.n_items) return false;
+  w = item_at(p, j);
+  return true;
+}
+
 // ---------------------------------------------------------------- kernel 2
+// Persistent: one CTA per SM walks its items; every role counts barrier
+// phases by tile over all of its items (qd_*, s_full, ds_*, dq_*) or by item
+// (kv_full, kv_empty, acc_done, acc_free).
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     diffattn_bwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
                                    const __grid_constant__ CUtensorMap tm_k1,
@@ -250,24 +289,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int *abort_flag = &ctrl->abort;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-
-  // Heaviest key tiles first (under the causal mask key tile 0 sees every query tile).
-  const int map = static_cast<int>(blockIdx.x & 1);
-  const int64_t item = blockIdx.x >> 1;
-  const int kt = static_cast<int>(item / p.BH);
-  const int64_t bh = item % p.BH;
-  const int h = static_cast<int>(bh % p.H);
-  const int k0 = kt * BK;
-  const int qt_first = p.causal ? kt : 0;
-  const int n_q = p.n_qtiles - qt_first;
   const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BQ;
-  const float *lse_g = p.lse + (map * p.BH + bh) * n_pad;
-  const float *dvec_g = p.dvec + (map * p.BH + bh) * n_pad;
-  const CUtensorMap *tm_q = map ? &tm_q2 : &tm_q1;
-  const CUtensorMap *tm_k = map ? &tm_k2 : &tm_k1;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->kv_full, 1);
+    mbar_init(&ctrl->kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->qd_full[s], 1);
       mbar_init(&ctrl->qd_empty[s], 1);
@@ -281,13 +307,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(&ctrl->dq_full, 1);
     mbar_init(&ctrl->dq_free, 128);
     mbar_init(&ctrl->acc_done, 1);
+    mbar_init(&ctrl->acc_free, 384);
     mbar_init(&ctrl->drain, 1);
     ctrl->abort = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(tm_q);
-    tma_prefetch_desc(tm_k);
+    tma_prefetch_desc(&tm_q1);
+    tma_prefetch_desc(&tm_k1);
+    tma_prefetch_desc(&tm_q2);
+    tma_prefetch_desc(&tm_k2);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
   }
@@ -304,29 +333,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t issued[2] = {0, 0};
-      mbar_arrive_expect_tx(&ctrl->kv_full, 3 * TILE64);
-      tma_load_3d(smem + OFF_K, tm_k, &ctrl->kv_full, 0, k0, static_cast<int32_t>(bh));
-      tma_load_3d(smem + OFF_V, &tm_v, &ctrl->kv_full, 0, k0, static_cast<int32_t>(bh));
-      tma_load_3d(smem + OFF_V + TILE64, &tm_v, &ctrl->kv_full, HD, k0,
-                  static_cast<int32_t>(bh));
-      for (int it = 0; it < n_q; ++it) {
-        const int s = it & 1;
-        const uint32_t u = static_cast<uint32_t>(it >> 1);
-        if (u > 0 && !mbar_wait(&ctrl->qd_empty[s], (u - 1) & 1, abort_flag, WAIT_TIMEOUT_NS))
+      uint32_t T = 0;  // tiles loaded so far, over all items
+      int kv_issued = 0;
+      Item w;
+      bool ok = true;
+      for (int r = 0; ok && next_item(p, r, w); ++r) {
+        const CUtensorMap *tm_q = w.map ? &tm_q2 : &tm_q1;
+        const CUtensorMap *tm_k = w.map ? &tm_k2 : &tm_k1;
+        const float *lse_g = p.lse + (w.map * p.BH + w.bh) * n_pad;
+        const float *dvec_g = p.dvec + (w.map * p.BH + w.bh) * n_pad;
+        const int32_t bh32 = static_cast<int32_t>(w.bh);
+        // K and V of the previous item are read until its last MMAs complete.
+        if (r > 0 && !(ok = mbar_wait(&ctrl->kv_empty, (r - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
           break;
-        const int q0 = (qt_first + it) * BQ;
-        uint64_t *bar = &ctrl->qd_full[s];
-        mbar_arrive_expect_tx(bar, 3 * TILE64 + VEC_BYTES);
-        tma_load_3d(smem + OFF_Q + s * TILE64, tm_q, bar, 0, q0, static_cast<int32_t>(bh));
-        uint8_t *dst = smem + OFF_DO + s * 2 * TILE64;
-        tma_load_3d(dst, &tm_do, bar, 0, q0, static_cast<int32_t>(bh));
-        tma_load_3d(dst + TILE64, &tm_do, bar, HD, q0, static_cast<int32_t>(bh));
-        float *vec = reinterpret_cast<float *>(smem + OFF_VEC + s * VEC_BYTES);
-        bulk_g2s(vec, lse_g + q0, BQ * 4, bar);
-        bulk_g2s(vec + BQ, dvec_g + q0, BQ * 4, bar);
-        issued[s] = u + 1;
+        mbar_arrive_expect_tx(&ctrl->kv_full, 3 * TILE64);
+        tma_load_3d(smem + OFF_K, tm_k, &ctrl->kv_full, 0, w.k0, bh32);
+        tma_load_3d(smem + OFF_V, &tm_v, &ctrl->kv_full, 0, w.k0, bh32);
+        tma_load_3d(smem + OFF_V + TILE64, &tm_v, &ctrl->kv_full, HD, w.k0, bh32);
+        kv_issued = r + 1;
+        for (int it = 0; it < w.n_q; ++it, ++T) {
+          const int s = T & 1;
+          const uint32_t u = T >> 1;
+          if (u > 0 && !(ok = mbar_wait(&ctrl->qd_empty[s], (u - 1) & 1, abort_flag,
+                                        WAIT_TIMEOUT_NS)))
+            break;
+          const int q0 = (w.qt_first + it) * BQ;
+          uint64_t *bar = &ctrl->qd_full[s];
+          mbar_arrive_expect_tx(bar, 3 * TILE64 + VEC_BYTES);
+          tma_load_3d(smem + OFF_Q + s * TILE64, tm_q, bar, 0, q0, bh32);
+          uint8_t *dst = smem + OFF_DO + s * 2 * TILE64;
+          tma_load_3d(dst, &tm_do, bar, 0, q0, bh32);
+          tma_load_3d(dst + TILE64, &tm_do, bar, HD, q0, bh32);
+          float *vec = reinterpret_cast<float *>(smem + OFF_VEC + s * VEC_BYTES);
+          bulk_g2s(vec, lse_g + q0, BQ * 4, bar);
+          bulk_g2s(vec + BQ, dvec_g + q0, BQ * 4, bar);
+          issued[s] = u + 1;
+        }
       }
-      drain_wait(&ctrl->kv_full, 0);
+      // Loads still in flight land before the CTA exits.
+      if (kv_issued > 0) drain_wait(&ctrl->kv_full, (kv_issued - 1) & 1);
       for (int s = 0; s < 2; ++s)
         if (issued[s] > 0) drain_wait(&ctrl->qd_full[s], (issued[s] - 1) & 1);
     }
@@ -388,55 +433,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto wait_all = [&](uint64_t *bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, WAIT_TIMEOUT_NS));
     };
-    // Order per query tile i: dV_i and dK_i chunk by chunk as the P^T / dS^T
-    // warps publish them (three steps).  Step 1 also means that every dW^T_i
-    // column has been read and that the packed dS^T in the dW^T columns is
-    // consumed by the MMAs issued so far, so dW^T of tile i+1 follows the
-    // chunks of step 1 while the warps compute step 2; S^T of tile i+1 follows
-    // the chunks of step 2; then dQ_i, which runs while the warps start on
-    // tile i+1.
-    bool ok = wait_all(&ctrl->kv_full, 0) && wait_all(&ctrl->qd_full[0], 0);
-    tc_fence_after_sync();
-    if (ok) {
-      issue_w(0);
-      issue_s(0);
+    // Order per query tile i of an item: dV_i and dK_i chunk by chunk as the
+    // P^T / dS^T warps publish them (three steps).  Step 1 also means that
+    // every dW^T_i column has been read and that the packed dS^T in the dW^T
+    // columns is consumed by the MMAs issued so far, so dW^T of tile i+1
+    // follows the chunks of step 1 while the warps compute step 2; S^T of tile
+    // i+1 follows the chunks of step 2; then dQ_i, which runs while the warps
+    // start on tile i+1.  The first tile of an item waits for the item's K
+    // and V, which replace the previous item's once its last MMAs are done.
+    bool ok = true;
+    uint32_t T = 0;  // tiles processed so far, over all items
+    Item w;
+    for (int r = 0; ok && next_item(p, r, w); ++r) {
+      if (!(ok = wait_all(&ctrl->kv_full, r & 1) && wait_all(&ctrl->qd_full[T & 1], (T >> 1) & 1)))
+        break;
+      tc_fence_after_sync();
+      issue_w(T & 1);
+      issue_s(T & 1);
       umma_commit_warp(&ctrl->s_full);
-    }
-    for (int it = 0; ok && it < n_q; ++it) {
-      const int s = it & 1;  // Q / dO stage and dS^T buffer of tile it
-      for (int step = 0; ok && step < 3; ++step) {
-        if (!(ok = wait_all(&ctrl->ds_ready[step], it & 1))) break;
-        tc_fence_after_sync();
+      // The item's first dV and dK MMAs overwrite the accumulators that the
+      // previous item's epilogue reads.
+      if (r > 0 && !(ok = wait_all(&ctrl->acc_free, (r - 1) & 1))) break;
+      for (int it = 0; ok && it < w.n_q; ++it, ++T) {
+        const int s = T & 1;  // Q / dO stage and dS^T buffer of tile T
+        for (int step = 0; ok && step < 3; ++step) {
+          if (!(ok = wait_all(&ctrl->ds_ready[step], T & 1))) break;
+          tc_fence_after_sync();
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const int c = 3 * step + j;
-          if (c < BQ / 16) issue_dv_dk(s, c, (it > 0 || c > 0) ? 1u : 0u);
-        }
-        if (it + 1 < n_q) {
-          const int s1 = s ^ 1;
-          if (step == 1) {
-            if (!(ok = wait_all(&ctrl->qd_full[s1], ((it + 1) >> 1) & 1))) break;
-            tc_fence_after_sync();
-            issue_w(s1);
-          } else if (step == 2) {
-            issue_s(s1);
-            umma_commit_warp(&ctrl->s_full);
+          for (int j = 0; j < 3; ++j) {
+            const int c = 3 * step + j;
+            if (c < BQ / 16) issue_dv_dk(s, c, (it > 0 || c > 0) ? 1u : 0u);
+          }
+          if (it + 1 < w.n_q) {
+            const int s1 = s ^ 1;
+            if (step == 1) {
+              if (!(ok = wait_all(&ctrl->qd_full[s1], ((T + 1) >> 1) & 1))) break;
+              tc_fence_after_sync();
+              issue_w(s1);
+            } else if (step == 2) {
+              issue_s(s1);
+              umma_commit_warp(&ctrl->s_full);
+            }
           }
         }
+        if (!ok) break;
+        umma_commit_warp(&ctrl->qd_empty[s]);  // the last reads of Q_i and dO_i
+        // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (K = keys).
+        if (T > 0 && !(ok = wait_all(&ctrl->dq_free, (T - 1) & 1))) break;
+        tc_fence_after_sync();
+        const uint32_t d_ds = d_ds_mn + ((s * DS_BYTES) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_bf16_ss_lo_warp(tmem + TM_DQ, d_ds + 128 * kk, d_k_mn + 128 * kk, dhi, ID_DQ,
+                               kk > 0);
+        umma_commit_warp(&ctrl->dq_full);
+        umma_commit_warp(&ctrl->ds_free[s]);
       }
       if (!ok) break;
-      umma_commit_warp(&ctrl->qd_empty[s]);  // the last reads of Q_i and dO_i
-      // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (K = keys).
-      if (it > 0 && !(ok = wait_all(&ctrl->dq_free, (it - 1) & 1))) break;
-      tc_fence_after_sync();
-      const uint32_t d_ds = d_ds_mn + ((s * DS_BYTES) >> 4);
-#pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk)
-        umma_bf16_ss_lo_warp(tmem + TM_DQ, d_ds + 128 * kk, d_k_mn + 128 * kk, dhi, ID_DQ, kk > 0);
-      umma_commit_warp(&ctrl->dq_full);
-      umma_commit_warp(&ctrl->ds_free[s]);
+      umma_commit_warp(&ctrl->acc_done);  // dV and dK of the item are complete
+      umma_commit_warp(&ctrl->kv_empty);  // K and V of the item are no longer read
     }
-    if (ok) umma_commit_warp(&ctrl->acc_done);
     umma_commit_warp(&ctrl->drain);
     drain_wait(&ctrl->drain, 0);
     __syncwarp();
@@ -449,21 +505,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // P^T and dS^T at tm_p(c) and tm_ds(c), and dS^T in shared memory for dQ.
     // Step 1 is published only once the step-2 chunk's S^T and dW^T are in
     // registers.  Group 2, with one chunk fewer, drains dQ of the previous
-    // tile after its second step.
+    // tile (which may belong to the previous item) after its second step.
+    // After an item's last tile, every group takes part in its dV / dK
+    // epilogue.
     const int g = (warp - 4) / 4;
     const int kr = (warp % 4) * 32 + lane;  // key row (dQ: query row) = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t t_lane = tmem + lane_addr;
     const uint32_t t_s = t_lane + TM_S;
     const uint32_t t_w = t_lane + TM_W;
-    const float coef = map ? -p.lambda[h] : 1.f;
     const float sl2 = p.scale_log2;
-    const int kpos = k0 + kr;
-    const bool key_ok = kpos < p.N;
-    const bool key_tile_ragged = k0 + BK > p.N;
-    float *dq_base = p.dq_acc + (map * p.BH + bh) * static_cast<int64_t>(p.N) * HD;
-    // dQ of query tile t into the fp32 accumulator (thread = query row).
-    auto drain_dq = [&](int t) {
+    // dQ of tile t (query tile q0 of head bh, map `map`) into the fp32
+    // accumulator (thread = query row).
+    auto drain_dq = [&](uint32_t t, int map, int64_t bh, int q0) {
       bool okd = mbar_wait(&ctrl->dq_full, t & 1, abort_flag, WAIT_TIMEOUT_NS);
       okd = __all_sync(0xffffffffu, okd);
       if (!okd) return false;
@@ -478,7 +532,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // dQ rows, transposed across each 8-lane group so that every vector
       // reduction covers four 128-byte row segments (one row per lane made
       // each instruction touch 32 rows).
-      const int q0 = (qt_first + t) * BQ;
+      float *dq_base = p.dq_acc + (map * p.BH + bh) * static_cast<int64_t>(p.N) * HD;
       const int row0 = q0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first row
       float *col_base = dq_base + 4 * (lane & 7);
 #pragma unroll
@@ -512,83 +566,102 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_arrive(&ctrl->ds_ready[step]);
     };
     bool ok = true;
-    for (int it = 0; it < n_q; ++it) {
-      const int s = it & 1;
-      const int q0 = (qt_first + it) * BQ;
-      ok = mbar_wait(&ctrl->s_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
-      // dS^T buffer s was last read by the dQ MMAs of tile it - 2.
-      if (ok && it >= 2)
-        ok = mbar_wait(&ctrl->ds_free[s], ((it >> 1) - 1) & 1, abort_flag, WAIT_TIMEOUT_NS);
-      ok = __all_sync(0xffffffffu, ok);
+    uint32_t T = 0;  // tiles processed so far, over all items
+    int prev_map = 0, prev_q0 = 0;  // the previous tile, whose dQ group 2 drains
+    int64_t prev_bh = 0;
+    Item w;
+    for (int r = 0; ok && next_item(p, r, w); ++r) {
+      const float coef = w.map ? -p.lambda[w.h] : 1.f;
+      const int kpos = w.k0 + kr;
+      const bool key_ok = kpos < p.N;
+      const bool key_tile_ragged = w.k0 + BK > p.N;
+      for (int it = 0; it < w.n_q; ++it, ++T) {
+        const int s = T & 1;
+        const int q0 = (w.qt_first + it) * BQ;
+        ok = mbar_wait(&ctrl->s_full, T & 1, abort_flag, WAIT_TIMEOUT_NS);
+        // dS^T buffer s was last read by the dQ MMAs of tile T - 2.
+        if (ok && T >= 2)
+          ok = mbar_wait(&ctrl->ds_free[s], ((T >> 1) - 1) & 1, abort_flag, WAIT_TIMEOUT_NS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        uint8_t *ds_buf = smem + OFF_DS + s * DS_BYTES;
+        const float *vec = reinterpret_cast<const float *>(smem + OFF_VEC + s * VEC_BYTES);
+        const float *lse = vec;
+        const float *cd = vec + BQ;
+        // Query column c of the tile (query q0 + c) is visible iff lo <= c < hi.
+        const int lo = p.causal ? (kpos - q0) : 0;
+        const int hi = key_ok ? (p.N - q0) : 0;
+        const bool masked = key_tile_ragged || q0 + BQ > p.N || (p.causal && q0 == w.k0);
+        auto work = [&](const uint32_t (&x)[16], const uint32_t (&wv)[16], int c) {
+          const int c0 = 16 * c;
+          uint32_t pk[8], dk[8];
+          if (masked)
+            bwd_chunk<true, 16>(x, wv, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
+          else
+            bwd_chunk<false, 16>(x, wv, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
+          tmem_st8(t_lane + tm_p(c), pk);
+          tmem_st8(t_lane + tm_ds(c), dk);
+          uint8_t *sub = ds_buf + (c >> 2) * TILE64;  // 64-query half of the dS^T tile
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint4 v4 = make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+            *reinterpret_cast<uint4 *>(sub + sw128(kr, (c & 3) * 2 + j)) = v4;
+          }
+        };
+        // Loads of each step's chunk overlap the work on the one before.
+        const int c_a = g, c_b = g + 3, c_c = g + 6;
+        const bool third = c_c < BQ / 16;  // uniform per warp
+        uint32_t xa[16], wa[16], xb[16], wb[16];
+        tmem_ld16(t_s + 16 * c_a, xa);
+        tmem_ld16(t_w + 16 * c_a, wa);
+        tmem_ld16(t_s + 16 * c_b, xb);
+        tmem_ld16(t_w + 16 * c_b, wb);
+        tmem_wait16x4(xa, wa, xb, wb);
+        work(xa, wa, c_a);
+        publish(0);
+        if (third) {
+          tmem_ld16(t_s + 16 * c_c, xa);
+          tmem_ld16(t_w + 16 * c_c, wa);
+        }
+        work(xb, wb, c_b);
+        if (third) tmem_wait16x4(xa, wa, xb, wb);
+        publish(1);
+        if (third) {
+          work(xa, wa, c_c);
+          publish(2);
+        } else if (T > 0 && !(ok = drain_dq(T - 1, prev_map, prev_bh, prev_q0))) {
+          break;
+        }
+        prev_map = w.map;
+        prev_bh = w.bh;
+        prev_q0 = q0;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------------- dV, dK out
+      ok = mbar_wait(&ctrl->acc_done, r & 1, abort_flag, WAIT_TIMEOUT_NS);
+      // Warp-uniform decision: the TMEM loads below are warp-collective.
+      ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
       if (!ok) break;
       tc_fence_after_sync();
-      uint8_t *ds_buf = smem + OFF_DS + s * DS_BYTES;
-      const float *vec = reinterpret_cast<const float *>(smem + OFF_VEC + s * VEC_BYTES);
-      const float *lse = vec;
-      const float *cd = vec + BQ;
-      // Query column c of the tile (query q0 + c) is visible iff lo <= c < hi.
-      const int lo = p.causal ? (kpos - q0) : 0;
-      const int hi = key_ok ? (p.N - q0) : 0;
-      const bool masked = key_tile_ragged || q0 + BQ > p.N || (p.causal && q0 == k0);
-      auto work = [&](const uint32_t (&x)[16], const uint32_t (&w)[16], int c) {
-        const int c0 = 16 * c;
-        uint32_t pk[8], dk[8];
-        if (masked)
-          bwd_chunk<true, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
-        else
-          bwd_chunk<false, 16>(x, w, lse, cd, c0, sl2, coef, lo, hi, pk, dk);
-        tmem_st8(t_lane + tm_p(c), pk);
-        tmem_st8(t_lane + tm_ds(c), dk);
-        uint8_t *sub = ds_buf + (c >> 2) * TILE64;  // 64-query half of the dS^T tile
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint4 v4 = make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
-          *reinterpret_cast<uint4 *>(sub + sw128(kr, (c & 3) * 2 + j)) = v4;
-        }
-      };
-      // Loads of each step's chunk overlap the work on the one before.
-      const int c_a = g, c_b = g + 3, c_c = g + 6;
-      const bool third = c_c < BQ / 16;  // uniform per warp
-      uint32_t xa[16], wa[16], xb[16], wb[16];
-      tmem_ld16(t_s + 16 * c_a, xa);
-      tmem_ld16(t_w + 16 * c_a, wa);
-      tmem_ld16(t_s + 16 * c_b, xb);
-      tmem_ld16(t_w + 16 * c_b, wb);
-      tmem_wait16x4(xa, wa, xb, wb);
-      work(xa, wa, c_a);
-      publish(0);
-      if (third) {
-        tmem_ld16(t_s + 16 * c_c, xa);
-        tmem_ld16(t_w + 16 * c_c, wa);
-      }
-      work(xb, wb, c_b);
-      if (third) tmem_wait16x4(xa, wa, xb, wb);
-      publish(1);
-      if (third) {
-        work(xa, wa, c_c);
-        publish(2);
-      } else if (it > 0 && !(ok = drain_dq(it - 1))) {
-        break;
-      }
-    }
-    if (ok && g == 2) ok = drain_dq(n_q - 1);
-    // ---------------------------------------------------------------- dV, dK out
-    if (ok) ok = mbar_wait(&ctrl->acc_done, 0, abort_flag, WAIT_TIMEOUT_NS);
-    // Warp-uniform decision: the TMEM loads below are warp-collective.
-    ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
-    if (ok) {
-      tc_fence_after_sync();
-      // dV times c (both maps add into the fp32 accumulator), in 32-column
-      // blocks (group 0: blocks 0-1, group 1: block 2, group 2: block 3), each
-      // transposed across 8-lane groups so that every vector reduction covers
-      // four 128-byte row segments.
-      const int blk_lo = g == 0 ? 0 : g + 1, blk_hi = g == 0 ? 2 : g + 2;
-      const int krow0 = k0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first key row
-      float *dv_col = p.dv_acc + bh * static_cast<int64_t>(p.N) * DV + 4 * (lane & 7);
-#pragma unroll 1
-      for (int bk = blk_lo; bk < blk_hi; ++bk) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_addr + TM_DV + 32 * bk, v);  // warp-collective
+      // Every accumulator column this warp handles is read into registers
+      // before the next item's MMAs may overwrite them: dV 32-column blocks
+      // (group 0: blocks 0-1, group 1: block 2, group 2: block 3) and dK
+      // 32-column halves (group 1: columns 0-31, group 2: columns 32-63).
+      uint32_t va[32], vb[32];
+      const int blk_a = g == 0 ? 0 : g + 1;
+      tmem_ld_x32_nowait(tmem + lane_addr + TM_DV + 32 * blk_a, va);
+      tmem_ld_x32_nowait(tmem + lane_addr + (g == 0 ? TM_DV + 32 : TM_DK + 32 * (g - 1)), vb);
+      tmem_ld_wait_x32(va);
+      tmem_ld_wait_x32(vb);
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->acc_free);
+      // dV times c (both maps add into the fp32 accumulator), each 32-column
+      // block transposed across 8-lane groups so that every vector reduction
+      // covers four 128-byte row segments.
+      const int krow0 = w.k0 + (warp % 4) * 32 + (lane & ~7);  // the 8-lane group's first key row
+      float *dv_col = p.dv_acc + w.bh * static_cast<int64_t>(p.N) * DV + 4 * (lane & 7);
+      auto store_dv = [&](const uint32_t (&v)[32], int bk) {
         uint4 ch[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -605,39 +678,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        __uint_as_float(ch[j].x), __uint_as_float(ch[j].y),
                        __uint_as_float(ch[j].z), __uint_as_float(ch[j].w));
         }
-      }
-      // dK (64 columns, by group 1), scaled by 1/sqrt(d), stored once as bf16:
-      // packed, transposed across 8-lane groups, four 128-byte row segments per
-      // store instruction.
-      if (g == 1) {
-        uint4 pkt[8];
+      };
+      store_dv(va, blk_a);
+      if (g == 0) store_dv(vb, 1);
+      // dK (groups 1 and 2, 32 columns each), scaled by 1/sqrt(d), stored
+      // once as bf16: packed, transposed across 4-lane groups, eight 64-byte
+      // row segments per store instruction.
+      if (g >= 1) {
+        uint4 pkt[4];
 #pragma unroll
-        for (int c32 = 0; c32 < HD; c32 += 32) {
-          uint32_t v[32];
-          tmem_ld_x32(tmem + lane_addr + TM_DK + c32, v);  // warp-collective
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 &pk = pkt[c32 / 8 + q];
-            pk.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * p.scale,
-                               __uint_as_float(v[8 * q + 1]) * p.scale);
-            pk.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * p.scale,
-                               __uint_as_float(v[8 * q + 3]) * p.scale);
-            pk.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * p.scale,
-                               __uint_as_float(v[8 * q + 5]) * p.scale);
-            pk.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * p.scale,
-                               __uint_as_float(v[8 * q + 7]) * p.scale);
-          }
+        for (int q = 0; q < 4; ++q) {
+          uint4 &pk = pkt[q];
+          pk.x = pack_bf16x2(__uint_as_float(vb[8 * q + 0]) * p.scale,
+                             __uint_as_float(vb[8 * q + 1]) * p.scale);
+          pk.y = pack_bf16x2(__uint_as_float(vb[8 * q + 2]) * p.scale,
+                             __uint_as_float(vb[8 * q + 3]) * p.scale);
+          pk.z = pack_bf16x2(__uint_as_float(vb[8 * q + 4]) * p.scale,
+                             __uint_as_float(vb[8 * q + 5]) * p.scale);
+          pk.w = pack_bf16x2(__uint_as_float(vb[8 * q + 6]) * p.scale,
+                             __uint_as_float(vb[8 * q + 7]) * p.scale);
         }
-        transpose8_chunks(pkt, lane);
-        __nv_bfloat16 *dk_col = (map ? p.dk2 : p.dk1) + bh * static_cast<int64_t>(p.N) * HD +
-                                8 * (lane & 7);
+        transpose4_chunks(pkt, lane);
+        const int krow4 = w.k0 + (warp % 4) * 32 + (lane & ~3);  // the 4-lane group's first key row
+        const int dcol = 32 * (g - 1) + 8 * (lane & 3);
+        __nv_bfloat16 *dk_col = (w.map ? p.dk2 : p.dk1) + w.bh * static_cast<int64_t>(p.N) * HD + dcol;
 #pragma unroll
-        for (int j2 = 0; j2 < 8; ++j2) {
-          if (krow0 + j2 < p.N && dbg_ok(krow0 + j2 >= 0 && 8 * (lane & 7) + 8 <= HD, p.status, 42))
-            *reinterpret_cast<uint4 *>(dk_col + static_cast<int64_t>(krow0 + j2) * HD) = pkt[j2];
+        for (int j2 = 0; j2 < 4; ++j2) {
+          if (krow4 + j2 < p.N && dbg_ok(krow4 + j2 >= 0 && dcol + 8 <= HD, p.status, 42))
+            *reinterpret_cast<uint4 *>(dk_col + static_cast<int64_t>(krow4 + j2) * HD) = pkt[j2];
         }
       }
     }
+    // dQ of the last tile.
+    if (ok && g == 2 && T > 0) drain_dq(T - 1, prev_map, prev_bh, prev_q0);
   }
 
   tc_fence_before_sync();
@@ -937,15 +1010,16 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   p.dq_acc = dq_acc;
   p.dv_acc = dv_acc;
   p.status = desc.status_dev;
-  dim3 grid(static_cast<unsigned>(BH * n_qtiles * 2));
+  p.n_items = 2 * BH * n_qtiles;
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  dim3 grid(static_cast<unsigned>(std::min<int64_t>(p.n_items, sms)));
   diffattn_bwd_bf16_sm103_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
       maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
   if (cudaGetLastError() != cudaSuccess) return DIFFATTN_ERR_CUDA;
 
   // 3. bf16 gradients
   const int64_t n_q4 = BH * N * HD / 4, n_v4 = BH * N * DV / 4;
-  int sms = 148;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   diffattn_bwd_finish_kernel<<<4 * sms, 256, 0, stream>>>(
       dq_acc, dv_acc, static_cast<__nv_bfloat16 *>(dq1), static_cast<__nv_bfloat16 *>(dq2),
       static_cast<__nv_bfloat16 *>(dv), n_q4, n_v4);

@@ -80,12 +80,28 @@ def test_bwd_lambda_and_norm(lam, headnorm):
 
 
 def test_bwd_larger_many_items():
-    """More (head, key tile, map) work items than SMs: B=2, H=4, N=1024 (every row)."""
+    """Eight key tiles per head, 128 work items: B=2, H=4, N=1024 (every row)."""
     w = W.custom(23, B=2, H=4, N=1024, d=64, causal=True, headnorm=True, random_w=True,
                  layer=8)
     dy = _dy(w, 23)
     _, g = _run(w, dy)
     _cmp(g, _oracle(w, dy), "B2H4N1024")
+
+
+@pytest.mark.parametrize("B,H,N,causal", [(8, 16, 384, True), (4, 16, 256, False),
+                                          (2, 8, 1408, True), (5, 8, 333, True)])
+def test_bwd_several_items_per_cta(B, H, N, causal):
+    """More (key tile, head, map) work items than a GB300 has SMs (152), so the
+    persistent gradient kernel walks several items per CTA: accumulators handed
+    from one item's epilogue to the next item's MMAs, K and V reloaded, and the
+    last dQ tile of one item drained during the next.  Items of different
+    lengths (causal) and ragged key tiles (N = 333, 1408) meet in one CTA."""
+    assert 2 * B * H * -(-N // 128) > 152
+    w = W.custom(900 + N, B=B, H=H, N=N, d=64, causal=causal, headnorm=True, random_w=True,
+                 layer=5)
+    dy = _dy(w, 900 + N)
+    _, g = _run(w, dy)
+    _cmp(g, _oracle(w, dy), f"B{B}H{H}N{N} causal={causal}")
 
 
 def test_fwd_train_output_is_the_forward():
