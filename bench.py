@@ -439,8 +439,9 @@ def run_decode(args):
                    "dv": 2 * d, "causal": True, "headnorm": True, "splits": splits,
                    "workspace_bytes": ws_bytes,
                    "bytes_convention": "k1, k2, v of the cache once + q1, q2 in + out",
-                   "l2": f"rotating {n_sets} caches of {set_bytes / 1e6:.1f} MB "
-                         f"(> {L2_BYTES / 1e6:.0f} MB L2)",
+                   "l2": f"rotating {n_sets} caches of {set_bytes / 1e6:.1f} MB: a step's set was last "
+                         f"used {(n_sets - 1) * set_bytes / 1e6:.0f} MB of other sets earlier "
+                         f"(L2 {L2_BYTES / 1e6:.0f} MB)",
                    "parallelism": f"weak x{world} (one full workload per rank)"},
         "roofline": {"bound": "hbm", "achieved": nbytes / (launch_ms * 1e-3) / 1e9,
                      "peak": peak, "unit": "GB/s",
@@ -565,8 +566,9 @@ def run_bwd(args):
                    "causal": True, "headnorm": True,
                    "flops_convention": "20*d per visible pair (S1, S2, dW, dV, dQ, dK), "
                                        "B*H*N^2/2 pairs",
-                   "l2": f"rotating {n_sets} sets of {set_bytes / 1e6:.1f} MB "
-                         f"(> {L2_BYTES / 1e6:.0f} MB L2)",
+                   "l2": f"rotating {n_sets} sets of {set_bytes / 1e6:.1f} MB: a step's set was last "
+                         f"used {(n_sets - 1) * set_bytes / 1e6:.0f} MB of other sets earlier "
+                         f"(L2 {L2_BYTES / 1e6:.0f} MB)",
                    "parallelism": f"weak x{world} (one full workload per rank)"},
         "roofline": {"bound": "tensor", "achieved": flops_step / (launch_ms * 1e-3) / 1e12,
                      "peak": peak, "unit": UNIT,
@@ -757,8 +759,9 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "N": N, "d": d, "dv": 2 * d,
                    "causal": True, "headnorm": True,
                    "flops_convention": "8*d per visible pair, B*H*N^2/2 pairs",
-                   "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
-                         f"(> {L2_BYTES / 1e6:.0f} MB L2)",
+                   "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB: a step's set was last "
+                         f"used {(n_sets - 1) * set_bytes / 1e6:.0f} MB of other sets earlier "
+                         f"(L2 {L2_BYTES / 1e6:.0f} MB)",
                    "parallelism": par},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
