@@ -118,6 +118,20 @@ diffattn_status plan_kv(const diffattn_desc *desc, int64_t n_kv, int splits, int
 
 extern "C" {
 
+namespace {
+// The shapes and dtypes diffattn_fwd runs (desc already checked).
+diffattn_status fwd_domain(const diffattn_desc &d) {
+  if (d.dtype == DIFFATTN_BF16 || d.dtype == DIFFATTN_E4M3_QK) {
+    if (d.d != 64 && d.d != 128) return DIFFATTN_ERR_UNSUPPORTED;
+    if (d.dtype == DIFFATTN_E4M3_QK && (d.d != 64 || d.headnorm == 2))
+      return DIFFATTN_ERR_UNSUPPORTED;
+    return check_sm103();
+  }
+  if (d.d > kF32MaxD || d.N > kF32MaxN) return DIFFATTN_ERR_UNSUPPORTED;
+  return DIFFATTN_OK;
+}
+}  // namespace
+
 diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const void *k1,
                              const void *q2, const void *k2, const void *v, const float *lambda,
                              const float *norm_w, void *out, void *stream) {
@@ -144,6 +158,63 @@ diffattn_status diffattn_fwd(const diffattn_desc *desc, const void *q1, const vo
                         static_cast<const float *>(q2), static_cast<const float *>(k2),
                         static_cast<const float *>(v), lambda, norm_w, static_cast<float *>(out),
                         s);
+}
+
+namespace {
+// Byte sizes of a forward's tensors: each q/k half, v and out.
+struct FwdBytes {
+  size_t qk, v, out;
+};
+FwdBytes fwd_bytes(const diffattn_desc &d) {
+  const size_t n = static_cast<size_t>(d.B) * static_cast<size_t>(d.H) * static_cast<size_t>(d.N);
+  const size_t wide = n * 2 * static_cast<size_t>(d.d);
+  const size_t qk_elem = d.dtype == DIFFATTN_F32 ? 4 : d.dtype == DIFFATTN_E4M3_QK ? 1 : 2;
+  const size_t vo_elem = d.dtype == DIFFATTN_F32 ? 4 : 2;
+  return {n * static_cast<size_t>(d.d) * qk_elem, wide * vo_elem, wide * vo_elem};
+}
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+diffattn_status diffattn_fwd_host_staging_bytes(const diffattn_desc *desc, size_t *bytes) {
+  diffattn_status st = check_desc(desc);
+  if (st != DIFFATTN_OK) return st;
+  if (bytes == nullptr) return DIFFATTN_ERR_INVALID_ARG;
+  const FwdBytes b = fwd_bytes(*desc);
+  *bytes = 4 * round256(b.qk) + round256(b.v) + round256(b.out);
+  return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd_host(const diffattn_desc *desc, const void *q1, const void *k1,
+                                  const void *q2, const void *k2, const void *v,
+                                  const float *lambda, const float *norm_w, void *out_host,
+                                  void *staging, size_t staging_bytes, void *stream) {
+  size_t need = 0;
+  diffattn_status st = diffattn_fwd_host_staging_bytes(desc, &need);
+  if (st != DIFFATTN_OK) return st;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out_host) return DIFFATTN_ERR_INVALID_ARG;
+  if (staging == nullptr || (reinterpret_cast<uintptr_t>(staging) & 255u) != 0 ||
+      staging_bytes < need)
+    return DIFFATTN_ERR_INVALID_ARG;
+  if ((st = fwd_domain(*desc)) != DIFFATTN_OK) return st;  // before any copy is queued
+  const FwdBytes b = fwd_bytes(*desc);
+  uint8_t *base = static_cast<uint8_t *>(staging);
+  uint8_t *dev[6];
+  const size_t sizes[6] = {b.qk, b.qk, b.qk, b.qk, b.v, b.out};
+  for (int i = 0; i < 6; ++i) {
+    dev[i] = base;
+    base += round256(sizes[i]);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void *src[5] = {q1, k1, q2, k2, v};
+  for (int i = 0; i < 5; ++i)
+    if (cudaMemcpyAsync(dev[i], src[i], sizes[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return DIFFATTN_ERR_CUDA;
+  st = diffattn_fwd(desc, dev[0], dev[1], dev[2], dev[3], dev[4], lambda, norm_w, dev[5], stream);
+  if (st != DIFFATTN_OK) return st;
+  if (cudaMemcpyAsync(out_host, dev[5], b.out, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DIFFATTN_ERR_CUDA;
+  return DIFFATTN_OK;
 }
 
 diffattn_status diffattn_fwd_strided(const diffattn_desc *desc, const void *q1, const void *k1,

@@ -101,6 +101,11 @@ def bind(lib):
     lib.diffattn_bwd.restype = ctypes.c_int
     lib.diffattn_bwd.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp, vp,
                                  fp, fp, vp, ctypes.c_size_t, vp]
+    lib.diffattn_fwd_host.restype = ctypes.c_int
+    lib.diffattn_fwd_host.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp, ctypes.c_size_t,
+                                      vp]
+    lib.diffattn_fwd_host_staging_bytes.restype = ctypes.c_int
+    lib.diffattn_fwd_host_staging_bytes.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
     lib.diffattn_fwd_strided.restype = ctypes.c_int
     lib.diffattn_fwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp,
                                          ctypes.POINTER(Strides), vp]
@@ -194,6 +199,55 @@ def fwd(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm_w=None,
     desc = make_desc(B, H, N, d, _DTYPE_CODE[dtype], causal, headnorm, eps, lambda_init, status)
     st = load().diffattn_fwd(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v),
                              _ptr(lam), _ptr(norm_w), _ptr(out), _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return out
+
+
+def fwd_host_staging_bytes(B, H, N, d, dtype=torch.bfloat16) -> int:
+    """`diffattn_fwd_host_staging_bytes`: device staging bytes `fwd_host` needs."""
+    desc = make_desc(B, H, N, d, _DTYPE_CODE[dtype], True, 1, 1e-5, 0.0)
+    n = ctypes.c_size_t(0)
+    _check(load().diffattn_fwd_host_staging_bytes(ctypes.byref(desc), ctypes.byref(n)))
+    return n.value
+
+
+def fwd_host(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm_w=None,
+             eps: float = 1e-5, lambda_init: float = 0.0, out=None, staging=None, status=None,
+             stream=None, raw_status: bool = False):
+    """`diffattn_fwd_host`: the forward with q1, k1, q2, k2, v and out in host memory.
+
+    q1, k1, q2, k2, v: contiguous CPU tensors (bf16 or fp32; pinned keeps the copies
+    asynchronous); lam (float32 [H]) and norm_w stay CUDA tensors; staging: a CUDA
+    uint8 tensor of at least fwd_host_staging_bytes(...) bytes (allocated when not
+    given).  Returns the CPU `out` [B, H, N, 2d], filled once `stream` reaches the
+    end of the call.
+    """
+    B, H, N, d = q1.shape
+    dtype = q1.dtype
+    if dtype not in _DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {dtype}")
+    for name, t, shape in (("q1", q1, (B, H, N, d)), ("k1", k1, (B, H, N, d)),
+                           ("q2", q2, (B, H, N, d)), ("k2", k2, (B, H, N, d)),
+                           ("v", v, (B, H, N, 2 * d))):
+        if tuple(t.shape) != shape or t.dtype != dtype or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU {shape} {dtype} tensor")
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=dtype).pin_memory()
+    if out.is_cuda or not out.is_contiguous() or tuple(out.shape) != (B, H, N, 2 * d):
+        raise ValueError("out must be a contiguous CPU [B, H, N, 2d] tensor")
+    if not lam.is_cuda or lam.dtype != torch.float32 or lam.numel() != H:
+        raise ValueError("lam must be a CUDA float32 [H] tensor")
+    need = fwd_host_staging_bytes(B, H, N, d, dtype)
+    if staging is None:
+        staging = torch.empty(need, dtype=torch.uint8, device=lam.device)
+    if not staging.is_cuda or staging.numel() < need:
+        raise ValueError(f"staging must be a CUDA uint8 tensor of at least {need} bytes")
+    desc = make_desc(B, H, N, d, _DTYPE_CODE[dtype], causal, headnorm, eps, lambda_init, status)
+    st = load().diffattn_fwd_host(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2),
+                                  _ptr(v), _ptr(lam), _ptr(norm_w), _ptr(out), _ptr(staging),
+                                  staging.numel(), _stream_handle(stream))
     if raw_status:
         return st
     _check(st)

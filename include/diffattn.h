@@ -136,6 +136,33 @@ typedef struct diffattn_strides {
 } diffattn_strides;
 
 /*
+ * diffattn_fwd_host — diffattn_fwd with its inputs and its output in host
+ * memory: the call a host program makes when the tensors live on the CPU side.
+ * Same computation, domain and errors as diffattn_fwd ("Differential
+ * Transformer", "How differential attention works").
+ *
+ * Arguments as diffattn_fwd except: q1, k1, q2, k2, v (same shapes and dtypes)
+ * and out_host ([B, H, N, 2d] in the output dtype) are HOST pointers;
+ * page-locked memory keeps the copies asynchronous, pageable memory works with
+ * the copies synchronising as cudaMemcpyAsync does.  lambda and norm_w stay
+ * device pointers.  staging: a device buffer, 256-byte aligned, of at least
+ * diffattn_fwd_host_staging_bytes(desc) bytes, owned by the caller; it holds
+ * the five inputs and the output (each region rounded up to 256 bytes) and must
+ * not be used by another call still in flight.  On `stream`, in order: one
+ * host-to-device cudaMemcpyAsync per input, diffattn_fwd on the staged
+ * tensors, one device-to-host cudaMemcpyAsync of the output; nothing is
+ * allocated.  A NULL, misaligned or short staging buffer is
+ * DIFFATTN_ERR_INVALID_ARG; a failed copy is DIFFATTN_ERR_CUDA.
+ */
+diffattn_status diffattn_fwd_host(const diffattn_desc *desc, const void *q1, const void *k1,
+                                  const void *q2, const void *k2, const void *v,
+                                  const float *lambda, const float *norm_w, void *out_host,
+                                  void *staging, size_t staging_bytes, void *stream);
+
+/* Bytes of the staging buffer diffattn_fwd_host needs for desc (host-only). */
+diffattn_status diffattn_fwd_host_staging_bytes(const diffattn_desc *desc, size_t *bytes);
+
+/*
  * diffattn_fwd_strided — diffattn_fwd with caller-given strides, so that
  * q1, k1, q2, k2, v and out may be views of other layouts (for example
  * [B, N, H, d] storage, strides {N*H*d, d, H*d}) without copies.  Same

@@ -16,7 +16,8 @@ def lib():
 
 
 EXPECTED_ENTRY_POINTS = {
-    "diffattn_fwd", "diffattn_fwd_strided", "diffattn_fwd_kv_plan", "diffattn_fwd_kv",
+    "diffattn_fwd", "diffattn_fwd_host", "diffattn_fwd_host_staging_bytes",
+    "diffattn_fwd_strided", "diffattn_fwd_kv_plan", "diffattn_fwd_kv",
     "diffattn_fwd_kv_strided",
     "diffattn_fwd_kv_noalloc", "diffattn_train_sizes", "diffattn_fwd_train", "diffattn_bwd",
     "diffattn_headnorm", "diffattn_selftest_wait", "diffattn_lambda_init", "diffattn_strerror",
@@ -274,3 +275,36 @@ def test_debug_build_exports_the_same_entry_points():
     for n in EXPECTED_ENTRY_POINTS:
         assert hasattr(dbg, n)
     assert dbg.diffattn_strerror(ops.ERR_BOUNDS).decode() == "kernel bounds check failed (debug build)"
+
+
+def test_fwd_host_staging_and_validation(lib):
+    """diffattn_fwd_host: staging size (five inputs and the output, each rounded up
+    to 256 bytes) and argument checks that return before any copy is queued."""
+    B, H, N = 2, 3, 300
+    d = ops.make_desc(B, H, N, 64, ops.BF16, True, True, 1e-5, 0.2)
+    n = ctypes.c_size_t(0)
+    assert lib.diffattn_fwd_host_staging_bytes(ctypes.byref(d), ctypes.byref(n)) == ops.OK
+    r = lambda x: (x + 255) // 256 * 256
+    qk, wide = B * H * N * 64 * 2, B * H * N * 128 * 2
+    assert n.value == 4 * r(qk) + 2 * r(wide)
+    f32 = ops.make_desc(1, 1, 6, 8, ops.F32, False, False, 1e-5, 0.2)
+    assert lib.diffattn_fwd_host_staging_bytes(ctypes.byref(f32), ctypes.byref(n)) == ops.OK
+    assert n.value == 4 * r(6 * 8 * 4) + 2 * r(6 * 16 * 4)
+    assert lib.diffattn_fwd_host_staging_bytes(ctypes.byref(d), None) == ops.ERR_INVALID_ARG
+    assert lib.diffattn_fwd_host_staging_bytes(None, ctypes.byref(n)) == ops.ERR_INVALID_ARG
+    need = 4 * r(qk) + 2 * r(wide)
+    f = ctypes.c_void_p(FAKE)
+    args = [f] * 5 + [f, None, f]
+    # NULL, misaligned, short staging
+    assert lib.diffattn_fwd_host(ctypes.byref(d), *args, None, need, None) == ops.ERR_INVALID_ARG
+    assert lib.diffattn_fwd_host(ctypes.byref(d), *args, ctypes.c_void_p(FAKE + 16), need,
+                                 None) == ops.ERR_INVALID_ARG
+    assert lib.diffattn_fwd_host(ctypes.byref(d), *args, f, need - 1, None) == ops.ERR_INVALID_ARG
+    # NULL host input or output
+    assert lib.diffattn_fwd_host(ctypes.byref(d), None, *args[1:], f, need,
+                                 None) == ops.ERR_INVALID_ARG
+    assert lib.diffattn_fwd_host(ctypes.byref(d), *args[:7], None, f, need,
+                                 None) == ops.ERR_INVALID_ARG
+    # empty problem: nothing to do
+    e = ops.make_desc(0, 3, 300, 64, ops.BF16, True, True, 1e-5, 0.2)
+    assert lib.diffattn_fwd_host(ctypes.byref(e), *args, None, 0, None) == ops.OK
