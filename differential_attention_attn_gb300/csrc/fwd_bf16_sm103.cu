@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             b + 128 * kk, dhi, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
         };
         auto wait_all = [&](uint64_t *bar, uint32_t parity) {
-          return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, WAIT_TIMEOUT_NS));
+          return mbar_wait_warp(bar, parity, abort_flag, WAIT_TIMEOUT_NS);
         };
         bool ok = true;
         uint32_t g = 0;  // key tiles processed so far
@@ -611,8 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float l_run = 0.f;        // this half row's running sum of exp2(x - m_run)
       bool ok = true;
       for (int j = 0; j < n_kv; ++j, ++g) {
-        ok = mbar_wait(&ctrl->s_full[k], g & 1, abort_flag, WAIT_TIMEOUT_NS);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = mbar_wait_warp(&ctrl->s_full[k], g & 1, abort_flag, WAIT_TIMEOUT_NS);
         if (!ok) break;
         tc_fence_after_sync();
         const int lim = lim0 - j * BN;
@@ -686,7 +685,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
 
       // -------------------------------------------------------------- epilogue
-      if (ok) ok = mbar_wait(&ctrl->o_done, ri & 1, abort_flag, WAIT_TIMEOUT_NS);
+      if (ok) ok = mbar_wait_warp(&ctrl->o_done, ri & 1, abort_flag, WAIT_TIMEOUT_NS);
       const float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);  // both halves
       const float inv = 1.f / l_row;
       if (!dbg_ok(r >= 0 && r < BM && (!w_mine || quarter * 32 + lane < DV), p.status, 6))

@@ -102,6 +102,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// The same wait by a whole converged warp, with a warp-uniform result.  A
+// phase that has already completed costs one try_wait and one vote (the
+// bounded helper's early return otherwise makes the warp diverge and
+// reconverge around it).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               uint64_t timeout_ns) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(smem_u32(bar), parity))) return true;
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, timeout_ns));
+}
+
 // ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor): 3-D tiled load into shared memory, completion
 // counted in bytes on an mbarrier.  The x coordinate must be a multiple of 8
