@@ -63,10 +63,11 @@ int sm_count() {
   return n;
 }
 
-// Strides of q1, k1, q2, k2, v, out: positive multiples of 8 elements (16
-// bytes, the tensor-copy rule) below 2^39.
-diffattn_status check_strides(const diffattn_strides *strides) {
-  for (int i = 0; i < 6; ++i) {
+// Strides (q1, k1, q2, k2, v, out for the forward entries; the backward's
+// eleven): positive multiples of 8 elements (16 bytes, the tensor-copy rule)
+// below 2^39.
+diffattn_status check_strides(const diffattn_strides *strides, int count = 6) {
+  for (int i = 0; i < count; ++i) {
     const int64_t s3[3] = {strides[i].b, strides[i].h, strides[i].n};
     for (int64_t x : s3)
       if (x <= 0 || (x & 7) != 0 || x >= (int64_t{1} << 39)) return DIFFATTN_ERR_INVALID_ARG;
@@ -340,12 +341,15 @@ diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, co
                                static_cast<float *>(saved));
 }
 
-diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
-                             const void *q2, const void *k2, const void *v, const float *lambda,
-                             const float *norm_w, const void *saved, const void *dy, void *dq1,
-                             void *dk1, void *dq2, void *dk2, void *dv, float *dlambda,
-                             float *dnorm_w, void *workspace, size_t workspace_bytes,
-                             void *stream) {
+namespace {
+
+// diffattn_bwd and diffattn_bwd_strided (strides == nullptr: contiguous).
+diffattn_status bwd_common(const diffattn_desc *desc, const void *q1, const void *k1,
+                           const void *q2, const void *k2, const void *v, const float *lambda,
+                           const float *norm_w, const void *saved, const void *dy, void *dq1,
+                           void *dk1, void *dq2, void *dk2, void *dv, float *dlambda,
+                           float *dnorm_w, void *workspace, size_t workspace_bytes,
+                           const diffattn_strides *strides, void *stream) {
   size_t saved_need = 0, ws_need = 0;
   diffattn_status st = diffattn_train_sizes(desc, &saved_need, &ws_need);
   if (st != DIFFATTN_OK) return st;
@@ -355,11 +359,62 @@ diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const vo
     if (q == nullptr || !aligned16(q)) return DIFFATTN_ERR_INVALID_ARG;
   if (!lambda || !dlambda || workspace_bytes < ws_need) return DIFFATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DIFFATTN_ERR_INVALID_ARG;
+  if (strides != nullptr && (st = check_strides(strides, kBwdStrides)) != DIFFATTN_OK) return st;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
   return launch_bwd_bf16_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w,
                                static_cast<const float *>(saved), dy, dq1, dk1, dq2, dk2, dv,
                                dlambda, dnorm_w, static_cast<float *>(workspace),
-                               static_cast<cudaStream_t>(stream));
+                               static_cast<cudaStream_t>(stream), strides);
+}
+
+}  // namespace
+
+diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
+                             const void *q2, const void *k2, const void *v, const float *lambda,
+                             const float *norm_w, const void *saved, const void *dy, void *dq1,
+                             void *dk1, void *dq2, void *dk2, void *dv, float *dlambda,
+                             float *dnorm_w, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+  return bwd_common(desc, q1, k1, q2, k2, v, lambda, norm_w, saved, dy, dq1, dk1, dq2, dk2, dv,
+                    dlambda, dnorm_w, workspace, workspace_bytes, nullptr, stream);
+}
+
+diffattn_status diffattn_bwd_strided(const diffattn_desc *desc, const void *q1, const void *k1,
+                                     const void *q2, const void *k2, const void *v,
+                                     const float *lambda, const float *norm_w,
+                                     const void *saved, const void *dy, void *dq1, void *dk1,
+                                     void *dq2, void *dk2, void *dv, float *dlambda,
+                                     float *dnorm_w, void *workspace, size_t workspace_bytes,
+                                     const diffattn_strides *strides, void *stream) {
+  if (strides == nullptr) {
+    const diffattn_status st = check_desc(desc);
+    return st != DIFFATTN_OK ? st : DIFFATTN_ERR_INVALID_ARG;
+  }
+  return bwd_common(desc, q1, k1, q2, k2, v, lambda, norm_w, saved, dy, dq1, dk1, dq2, dk2, dv,
+                    dlambda, dnorm_w, workspace, workspace_bytes, strides, stream);
+}
+
+diffattn_status diffattn_fwd_train_strided(const diffattn_desc *desc, const void *q1,
+                                           const void *k1, const void *q2, const void *k2,
+                                           const void *v, const float *lambda,
+                                           const float *norm_w, void *out, void *saved,
+                                           size_t saved_bytes, const diffattn_strides *strides,
+                                           void *stream) {
+  size_t need = 0, ws = 0;
+  diffattn_status st = diffattn_train_sizes(desc, &need, &ws);
+  if (st != DIFFATTN_OK) return st;
+  if (strides == nullptr) return DIFFATTN_ERR_INVALID_ARG;
+  if (desc->B * desc->H * desc->N == 0) return DIFFATTN_OK;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !lambda || !out || !saved) return DIFFATTN_ERR_INVALID_ARG;
+  if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+      !aligned16(out) || !aligned16(saved) || saved_bytes < need)
+    return DIFFATTN_ERR_INVALID_ARG;
+  if ((st = check_strides(strides)) != DIFFATTN_OK) return st;
+  if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
+  if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
+                               static_cast<cudaStream_t>(stream), 1, nullptr,
+                               static_cast<float *>(saved), strides);
 }
 
 diffattn_status diffattn_headnorm(const diffattn_desc *desc, const float *x, const float *norm_w,

@@ -109,7 +109,8 @@ struct BwdParams {
   const float *lambda;
   const float *lse;   // [2][BH][n_pad] log2-sum-exp from the forward
   const float *dvec;  // [2][BH][n_pad] c_k D_k
-  __nv_bfloat16 *dk1, *dk2;  // [BH][N][64]
+  __nv_bfloat16 *dk1, *dk2;  // [B, H, N, 64] views
+  int64_t dk_sb[2], dk_sh[2], dk_sn[2];  // their element strides (batch, head, row)
   float *dq_acc;             // [2][BH][N][64], zeroed
   float *dv_acc;             // [BH][N][128], zeroed
   int32_t *status;
@@ -274,7 +275,10 @@ __device__ __forceinline__ bool next_item(const BwdParams &p, int r, Item &w) {
 // ---------------------------------------------------------------- kernel 2
 // Persistent: one CTA per SM walks its items; every role counts barrier
 // phases by tile over all of its items (qd_*, s_full, ds_*, dq_*) or by item
-// (kv_full, kv_empty, acc_done, acc_free).
+// (kv_full, kv_empty, acc_done, acc_free).  kStridedDk: dk1 and dk2 are
+// written through their strides (a separate instantiation: the 64-bit stride
+// arithmetic costs the contiguous epilogue registers it does not have).
+template <bool kStridedDk>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     diffattn_bwd_bf16_sm103_kernel(const __grid_constant__ CUtensorMap tm_q1,
                                    const __grid_constant__ CUtensorMap tm_k1,
@@ -342,14 +346,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap *tm_k = w.map ? &tm_k2 : &tm_k1;
         const float *lse_g = p.lse + (w.map * p.BH + w.bh) * n_pad;
         const float *dvec_g = p.dvec + (w.map * p.BH + w.bh) * n_pad;
-        const int32_t bh32 = static_cast<int32_t>(w.bh);
+        // batch index (b * H + h = bh < 2^31)
+        const int wb = static_cast<int>(static_cast<uint32_t>(w.bh) / static_cast<uint32_t>(p.H));
         // K and V of the previous item are read until its last MMAs complete.
         if (r > 0 && !(ok = mbar_wait(&ctrl->kv_empty, (r - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
           break;
         mbar_arrive_expect_tx(&ctrl->kv_full, 3 * TILE64);
-        tma_load_3d(smem + OFF_K, tm_k, &ctrl->kv_full, 0, w.k0, bh32);
-        tma_load_3d(smem + OFF_V, &tm_v, &ctrl->kv_full, 0, w.k0, bh32);
-        tma_load_3d(smem + OFF_V + TILE64, &tm_v, &ctrl->kv_full, HD, w.k0, bh32);
+        tma_load_4d(smem + OFF_K, tm_k, &ctrl->kv_full, 0, w.k0, w.h, wb);
+        tma_load_4d(smem + OFF_V, &tm_v, &ctrl->kv_full, 0, w.k0, w.h, wb);
+        tma_load_4d(smem + OFF_V + TILE64, &tm_v, &ctrl->kv_full, HD, w.k0, w.h, wb);
         kv_issued = r + 1;
         for (int it = 0; it < w.n_q; ++it, ++T) {
           const int s = T & 1;
@@ -360,10 +365,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int q0 = (w.qt_first + it) * BQ;
           uint64_t *bar = &ctrl->qd_full[s];
           mbar_arrive_expect_tx(bar, 3 * TILE64 + VEC_BYTES);
-          tma_load_3d(smem + OFF_Q + s * TILE64, tm_q, bar, 0, q0, bh32);
+          tma_load_4d(smem + OFF_Q + s * TILE64, tm_q, bar, 0, q0, w.h, wb);
           uint8_t *dst = smem + OFF_DO + s * 2 * TILE64;
-          tma_load_3d(dst, &tm_do, bar, 0, q0, bh32);
-          tma_load_3d(dst + TILE64, &tm_do, bar, HD, q0, bh32);
+          tma_load_4d(dst, &tm_do, bar, 0, q0, w.h, wb);
+          tma_load_4d(dst + TILE64, &tm_do, bar, HD, q0, w.h, wb);
           float *vec = reinterpret_cast<float *>(smem + OFF_VEC + s * VEC_BYTES);
           bulk_g2s(vec, lse_g + q0, BQ * 4, bar);
           bulk_g2s(vec + BQ, dvec_g + q0, BQ * 4, bar);
@@ -701,11 +706,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         transpose4_chunks(pkt, lane);
         const int krow4 = w.k0 + (warp % 4) * 32 + (lane & ~3);  // the 4-lane group's first key row
         const int dcol = 32 * (g - 1) + 8 * (lane & 3);
-        __nv_bfloat16 *dk_col = (w.map ? p.dk2 : p.dk1) + w.bh * static_cast<int64_t>(p.N) * HD + dcol;
+        __nv_bfloat16 *dk_col;
+        int64_t sn;
+        if (kStridedDk) {
+          const uint32_t wb = static_cast<uint32_t>(w.bh) / static_cast<uint32_t>(p.H);
+          const int64_t sb = w.map ? p.dk_sb[1] : p.dk_sb[0];
+          const int64_t sh = w.map ? p.dk_sh[1] : p.dk_sh[0];
+          sn = w.map ? p.dk_sn[1] : p.dk_sn[0];
+          dk_col = (w.map ? p.dk2 : p.dk1) + wb * sb + w.h * sh + dcol;
+        } else {
+          sn = HD;
+          dk_col = (w.map ? p.dk2 : p.dk1) + w.bh * static_cast<int64_t>(p.N) * HD + dcol;
+        }
 #pragma unroll
         for (int j2 = 0; j2 < 4; ++j2) {
           if (krow4 + j2 < p.N && dbg_ok(krow4 + j2 >= 0 && dcol + 8 <= HD, p.status, 42))
-            *reinterpret_cast<uint4 *>(dk_col + static_cast<int64_t>(krow4 + j2) * HD) = pkt[j2];
+            *reinterpret_cast<uint4 *>(dk_col + (krow4 + j2) * sn) = pkt[j2];
         }
       }
     }
@@ -729,7 +745,8 @@ struct PreParams {
   int32_t H, N, n_pad, headnorm;
   float eps, out_scale;  // out_scale = 1 - lambda_init
   const float *lambda, *norm_w;
-  const __nv_bfloat16 *dy;  // [BH][N][128]
+  const __nv_bfloat16 *dy;  // [B, H, N, 128] view
+  int64_t dy_sb, dy_sh, dy_sn;  // its element strides (batch, head, row)
   const float *o_n;         // [2][BH][N][128] normalised map outputs
   __nv_bfloat16 *dout;      // [BH][N][128]
   float *dvec;              // [2][BH][n_pad] c_k D_k
@@ -766,7 +783,8 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
     float d1 = 0.f, d2 = 0.f;
     if (i < p.N) {
       const int64_t row = (bh * p.N + i) * DV + c;
-      const uint2 yb = *reinterpret_cast<const uint2 *>(p.dy + row);
+      const uint2 yb = *reinterpret_cast<const uint2 *>(p.dy + (bh / p.H) * p.dy_sb +
+                                                        h * p.dy_sh + i * p.dy_sn + c);
       const float2 y01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&yb.x));
       const float2 y23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&yb.y));
       const float dy[4] = {y01.x, y01.y, y23.x, y23.y};
@@ -844,11 +862,19 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
 // ---------------------------------------------------------------- kernel 3
 // fp32 accumulators -> bf16: dq_acc [2][BH][N][64] -> dq1, dq2; dv_acc -> dv.
 // Each thread has FINISH_UNROLL 16-byte loads in flight before it stores (one
-// at a time left the copy well short of the memory bandwidth).
+// at a time left the copy well short of the memory bandwidth).  kStrided: the
+// three destinations are [B, H, N, width] views with the element strides in
+// `fs` (dq1, dq2, dv), each 4-element group placed by its (batch, head, row).
 constexpr int FINISH_UNROLL = 4;
+struct FinishStrides {
+  int64_t sb[3], sh[3], sn[3];
+  int64_t H, N;
+};
+template <bool kStrided>
 __global__ void diffattn_bwd_finish_kernel(const float *dq_acc, const float *dv_acc,
                                            __nv_bfloat16 *dq1, __nv_bfloat16 *dq2,
-                                           __nv_bfloat16 *dv, int64_t n_q4, int64_t n_v4) {
+                                           __nv_bfloat16 *dv, int64_t n_q4, int64_t n_v4,
+                                           const FinishStrides fs) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t total = 2 * n_q4 + n_v4;
   auto src_of = [&](int64_t i, int64_t &j) -> const float4 * {
@@ -872,13 +898,25 @@ __global__ void diffattn_bwd_finish_kernel(const float *dq_acc, const float *dv_
       if (i >= total) continue;
       __nv_bfloat16 *dst;
       int64_t j;
-      if (i < n_q4) { dst = dq1; j = i; }
-      else if (i < 2 * n_q4) { dst = dq2; j = i - n_q4; }
-      else { dst = dv; j = i - 2 * n_q4; }
+      int t;
+      if (i < n_q4) { dst = dq1; j = i; t = 0; }
+      else if (i < 2 * n_q4) { dst = dq2; j = i - n_q4; t = 1; }
+      else { dst = dv; j = i - 2 * n_q4; t = 2; }
       uint2 o;
       o.x = pack_bf16x2(v[u].x, v[u].y);
       o.y = pack_bf16x2(v[u].z, v[u].w);
-      reinterpret_cast<uint2 *>(dst)[j] = o;
+      if (kStrided) {
+        const int64_t width4 = t == 2 ? DV / 4 : HD / 4;  // 4-element groups per row
+        const int64_t row = j / width4, col = 4 * (j - row * width4);
+        const int64_t bh = row / fs.N, n = row - bh * fs.N;
+        const int64_t b = bh / fs.H, h = bh - b * fs.H;
+        const int64_t sb = t == 0 ? fs.sb[0] : t == 1 ? fs.sb[1] : fs.sb[2];
+        const int64_t sh = t == 0 ? fs.sh[0] : t == 1 ? fs.sh[1] : fs.sh[2];
+        const int64_t sn = t == 0 ? fs.sn[0] : t == 1 ? fs.sn[1] : fs.sn[2];
+        *reinterpret_cast<uint2 *>(dst + b * sb + h * sh + n * sn + col) = o;
+      } else {
+        reinterpret_cast<uint2 *>(dst)[j] = o;
+      }
     }
   }
 }
@@ -893,8 +931,10 @@ using EncodeTiledFnB = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32
                                     CUtensorMapSwizzle, CUtensorMapL2promotion,
                                     CUtensorMapFloatOOBfill);
 
+// 4-D view {inner, rows, H, B} of a bf16 tensor with element strides st (rows
+// contiguous); 128-row x 64-column boxes with 128-byte swizzle.
 static CUresult encode_map_b(CUtensorMap *map, const void *base, uint64_t inner, uint64_t n,
-                             uint64_t bh) {
+                             uint64_t H, uint64_t B, const diffattn_strides &st) {
   static EncodeTiledFnB fn = [] {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -905,11 +945,12 @@ static CUresult encode_map_b(CUtensorMap *map, const void *base, uint64_t inner,
     return reinterpret_cast<EncodeTiledFnB>(ptr);
   }();
   if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
-  cuuint64_t dims[3] = {inner, n, bh};
-  cuuint64_t strides[2] = {inner * 2, inner * 2 * n};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+  cuuint64_t dims[4] = {inner, n, H, B};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                           static_cast<cuuint64_t>(st.b) * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
@@ -927,8 +968,16 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
                                       const float *lambda, const float *norm_w,
                                       const float *saved, const void *dy, void *dq1, void *dk1,
                                       void *dq2, void *dk2, void *dv, float *dlambda,
-                                      float *dnorm_w, float *workspace, cudaStream_t stream) {
+                                      float *dnorm_w, float *workspace, cudaStream_t stream,
+                                      const diffattn_strides *strides) {
   const int64_t BH = desc.B * desc.H, N = desc.N;
+  // Element strides of q1, k1, q2, k2, v, dy, dq1, dk1, dq2, dk2, dv: given, or
+  // contiguous [B, H, N, width].
+  diffattn_strides st[kBwdStrides];
+  for (int i = 0; i < kBwdStrides; ++i) {
+    const int64_t width = (i == 4 || i == 5 || i == 10) ? DV : HD;
+    st[i] = strides ? strides[i] : diffattn_strides{desc.H * N * width, N * width, width};
+  }
   const int64_t n_qtiles = (N + BQ - 1) / BQ;
   const int64_t n_pad = n_qtiles * BQ;
   if (BH * n_qtiles * 2 > INT32_MAX || N > INT32_MAX / 2) return DIFFATTN_ERR_UNSUPPORTED;
@@ -964,6 +1013,9 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   pp.lambda = lambda;
   pp.norm_w = norm_w;
   pp.dy = static_cast<const __nv_bfloat16 *>(dy);
+  pp.dy_sb = st[5].b;
+  pp.dy_sh = st[5].h;
+  pp.dy_sn = st[5].n;
   pp.o_n = o_n;
   pp.dout = dout;
   pp.dvec = dvec;
@@ -976,10 +1028,12 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   // 2. fused gradient kernel
   CUtensorMap maps[6];
   const void *bases[6] = {q1, k1, q2, k2, v, dout};
+  const diffattn_strides dout_st{desc.H * N * DV, N * DV, DV};  // the workspace's dO
   for (int i = 0; i < 6; ++i) {
     const uint64_t inner = (i >= 4) ? DV : HD;
     if (encode_map_b(&maps[i], bases[i], inner, static_cast<uint64_t>(N),
-                     static_cast<uint64_t>(BH)) != CUDA_SUCCESS)
+                     static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B),
+                     i == 5 ? dout_st : st[i]) != CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
   static std::atomic<bool> attr_set[64];  // per device (concurrent callers may both set)
@@ -987,7 +1041,10 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(diffattn_bwd_bf16_sm103_kernel,
+    if (cudaFuncSetAttribute(diffattn_bwd_bf16_sm103_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(diffattn_bwd_bf16_sm103_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES)) != cudaSuccess)
       return DIFFATTN_ERR_CUDA;
@@ -1007,6 +1064,11 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   p.dvec = dvec;
   p.dk1 = static_cast<__nv_bfloat16 *>(dk1);
   p.dk2 = static_cast<__nv_bfloat16 *>(dk2);
+  for (int m = 0; m < 2; ++m) {  // dk1: strides[7], dk2: strides[9]
+    p.dk_sb[m] = st[7 + 2 * m].b;
+    p.dk_sh[m] = st[7 + 2 * m].h;
+    p.dk_sn[m] = st[7 + 2 * m].n;
+  }
   p.dq_acc = dq_acc;
   p.dv_acc = dv_acc;
   p.status = desc.status_dev;
@@ -1014,15 +1076,33 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
   int sms = 148;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   dim3 grid(static_cast<unsigned>(std::min<int64_t>(p.n_items, sms)));
-  diffattn_bwd_bf16_sm103_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  if (strides != nullptr)
+    diffattn_bwd_bf16_sm103_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  else
+    diffattn_bwd_bf16_sm103_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
   if (cudaGetLastError() != cudaSuccess) return DIFFATTN_ERR_CUDA;
 
   // 3. bf16 gradients
   const int64_t n_q4 = BH * N * HD / 4, n_v4 = BH * N * DV / 4;
-  diffattn_bwd_finish_kernel<<<4 * sms, 256, 0, stream>>>(
-      dq_acc, dv_acc, static_cast<__nv_bfloat16 *>(dq1), static_cast<__nv_bfloat16 *>(dq2),
-      static_cast<__nv_bfloat16 *>(dv), n_q4, n_v4);
+  FinishStrides fs;
+  const int dst_idx[3] = {6, 8, 10};  // dq1, dq2, dv
+  for (int t = 0; t < 3; ++t) {
+    fs.sb[t] = st[dst_idx[t]].b;
+    fs.sh[t] = st[dst_idx[t]].h;
+    fs.sn[t] = st[dst_idx[t]].n;
+  }
+  fs.H = desc.H;
+  fs.N = N;
+  if (strides != nullptr)
+    diffattn_bwd_finish_kernel<true><<<4 * sms, 256, 0, stream>>>(
+        dq_acc, dv_acc, static_cast<__nv_bfloat16 *>(dq1), static_cast<__nv_bfloat16 *>(dq2),
+        static_cast<__nv_bfloat16 *>(dv), n_q4, n_v4, fs);
+  else
+    diffattn_bwd_finish_kernel<false><<<4 * sms, 256, 0, stream>>>(
+        dq_acc, dv_acc, static_cast<__nv_bfloat16 *>(dq1), static_cast<__nv_bfloat16 *>(dq2),
+        static_cast<__nv_bfloat16 *>(dv), n_q4, n_v4, fs);
   return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 

@@ -50,7 +50,11 @@ diffattn_status launch_bwd_bf16_sm103(const diffattn_desc &desc, const void *q1,
                                       const float *lambda, const float *norm_w,
                                       const float *saved, const void *dy, void *dq1, void *dk1,
                                       void *dq2, void *dk2, void *dv, float *dlambda,
-                                      float *dnorm_w, float *workspace, cudaStream_t stream);
+                                      float *dnorm_w, float *workspace, cudaStream_t stream,
+                                      const diffattn_strides *strides = nullptr);
+// Element strides the strided backward takes: q1, k1, q2, k2, v, dy, dq1, dk1,
+// dq2, dk2, dv.
+constexpr int kBwdStrides = 11;
 
 // Merge of the split-KV partial blocks: both maps' softmax states, then
 // o = O1/l1 - lambda O2/l2, the optional head norm and the bf16 store (out

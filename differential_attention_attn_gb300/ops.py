@@ -109,6 +109,13 @@ def bind(lib):
     lib.diffattn_fwd_strided.restype = ctypes.c_int
     lib.diffattn_fwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp,
                                          ctypes.POINTER(Strides), vp]
+    lib.diffattn_fwd_train_strided.restype = ctypes.c_int
+    lib.diffattn_fwd_train_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp,
+                                               ctypes.c_size_t, ctypes.POINTER(Strides), vp]
+    lib.diffattn_bwd_strided.restype = ctypes.c_int
+    lib.diffattn_bwd_strided.argtypes = [dp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp,
+                                         vp, fp, fp, vp, ctypes.c_size_t,
+                                         ctypes.POINTER(Strides), vp]
     lib.diffattn_fwd_kv_strided.restype = ctypes.c_int
     lib.diffattn_fwd_kv_strided.argtypes = [dp, ctypes.c_int64, vp, vp, vp, vp, vp, fp, fp,
                                             vp, ctypes.c_int, vp, ctypes.c_size_t,
@@ -287,14 +294,8 @@ def fwd_strided(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm
     if out is None:
         out = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=q1.device)
     ts = [q1, k1, q2, k2, v, out]
-    shapes = [(B, H, N, d)] * 4 + [(B, H, N, 2 * d)] * 2
-    for t, shape in zip(ts, shapes):
-        if tuple(t.shape) != shape or t.dtype != q1.dtype or not t.is_cuda:
-            raise ValueError(f"expected a CUDA {q1.dtype} tensor of shape {shape}")
-        if t.stride(-1) != 1:
-            raise ValueError("rows must be contiguous (last stride 1)")
+    arr = _view_strides(ts, [(B, H, N, d)] * 4 + [(B, H, N, 2 * d)] * 2, q1.dtype)
     _cuda_contig([lam, norm_w])
-    arr = (Strides * 6)(*[Strides(t.stride(0), t.stride(1), t.stride(2)) for t in ts])
     desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
                      lambda_init, status)
     st = load().diffattn_fwd_strided(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2),
@@ -304,6 +305,17 @@ def fwd_strided(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1, norm
         return st
     _check(st)
     return out
+
+
+def _view_strides(ts, shapes, dtype):
+    """Checks [B, H, rows, width]-shaped CUDA views with contiguous rows and
+    returns their (batch, head, row) element strides as a Strides array."""
+    for t, shape in zip(ts, shapes):
+        if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_cuda:
+            raise ValueError(f"expected a CUDA {dtype} tensor of shape {tuple(shape)}")
+        if t.stride(-1) != 1:
+            raise ValueError("rows must be contiguous (last stride 1)")
+    return (Strides * len(ts))(*[Strides(t.stride(0), t.stride(1), t.stride(2)) for t in ts])
 
 
 def fwd_kv_plan(B, H, N, n_kv, *, causal: bool, splits: int = 0, d: int = 64,
@@ -503,6 +515,69 @@ def bwd(q1, k1, q2, k2, v, lam, saved, dy, *, causal: bool, headnorm: bool = Tru
                              _ptr(grads["dv"]), _ptr(grads["dlam"]), _ptr(grads["dw"]),
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream_handle(stream))
+    if raw_status:
+        return st
+    _check(st)
+    return grads
+
+
+def fwd_train_strided(q1, k1, q2, k2, v, lam, *, causal: bool, headnorm: int = 1,
+                      norm_w=None, eps: float = 1e-5, lambda_init: float = 0.0, out=None,
+                      saved=None, status=None, stream=None):
+    """`diffattn_fwd_train_strided`: fwd_train on [B, H, N, d]-shaped views with
+    contiguous rows (`out` may be such a view too; default contiguous).
+    Returns (out, saved)."""
+    B, H, N, d = q1.shape
+    saved_bytes, _ = train_sizes(B, H, N, d=d)
+    if out is None:
+        out = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=q1.device)
+    if saved is None:
+        saved = torch.empty(saved_bytes, dtype=torch.uint8, device=q1.device)
+    ts = [q1, k1, q2, k2, v, out]
+    arr = _view_strides(ts, [(B, H, N, d)] * 4 + [(B, H, N, 2 * d)] * 2, q1.dtype)
+    _cuda_contig([lam, norm_w, saved])
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
+                     lambda_init, status)
+    _check(load().diffattn_fwd_train_strided(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2),
+                                             _ptr(k2), _ptr(v), _ptr(lam), _ptr(norm_w),
+                                             _ptr(out), _ptr(saved),
+                                             saved.numel() * saved.element_size(), arr,
+                                             _stream_handle(stream)))
+    return out, saved
+
+
+def bwd_strided(q1, k1, q2, k2, v, lam, saved, dy, *, causal: bool, headnorm: int = 1,
+                norm_w=None, eps: float = 1e-5, lambda_init: float = 0.0, workspace=None,
+                grads=None, status=None, stream=None, raw_status: bool = False):
+    """`diffattn_bwd_strided`: bwd on [B, H, N, .]-shaped views with contiguous rows;
+    `grads` (dq1, dk1, dq2, dk2, dv views, plus dlam and dw) defaults to contiguous
+    tensors.  Returns the grads dict as bwd does."""
+    B, H, N, d = q1.shape
+    _, ws_bytes = train_sizes(B, H, N, d=d)
+    dev = q1.device
+    if grads is None:
+        grads = {k: torch.empty((B, H, N, d), dtype=q1.dtype, device=dev)
+                 for k in ("dq1", "dk1", "dq2", "dk2")}
+        grads["dv"] = torch.empty((B, H, N, 2 * d), dtype=q1.dtype, device=dev)
+        grads["dlam"] = torch.empty(H, dtype=torch.float32, device=dev)
+        grads["dw"] = torch.zeros((H, 2 * d), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ts = [q1, k1, q2, k2, v, dy, grads["dq1"], grads["dk1"], grads["dq2"], grads["dk2"],
+          grads["dv"]]
+    w = 2 * d
+    shapes = [(B, H, N, d)] * 4 + [(B, H, N, w)] * 2 + [(B, H, N, d)] * 4 + [(B, H, N, w)]
+    arr = _view_strides(ts, shapes, q1.dtype)
+    _cuda_contig([lam, norm_w, saved, workspace, grads["dlam"], grads["dw"]])
+    desc = make_desc(B, H, N, d, _DTYPE_CODE.get(q1.dtype, -1), causal, headnorm, eps,
+                     lambda_init, status)
+    st = load().diffattn_bwd_strided(ctypes.byref(desc), _ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2),
+                                     _ptr(v), _ptr(lam), _ptr(norm_w), _ptr(saved), _ptr(dy),
+                                     _ptr(grads["dq1"]), _ptr(grads["dk1"]), _ptr(grads["dq2"]),
+                                     _ptr(grads["dk2"]), _ptr(grads["dv"]), _ptr(grads["dlam"]),
+                                     _ptr(grads["dw"]), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), arr,
+                                     _stream_handle(stream))
     if raw_status:
         return st
     _check(st)

@@ -302,9 +302,9 @@ diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, co
  * [H, 128] (written when headnorm is 1 or 2; may be NULL to skip it).
  * workspace: caller-owned scratch of at least workspace_bytes from
  * diffattn_train_sizes, 256-byte aligned (its contents on entry do not
- * matter).  dq and dv are summed over key tiles with fp32 atomic adds, so
- * their last bits can differ between runs; dk, dlambda order is fixed per
- * key tile.  Errors as for diffattn_fwd; DIFFATTN_ERR_INVALID_ARG also for a
+ * matter).  dq and dv are summed over key tiles, dlambda and dnorm_w over
+ * row blocks, with fp32 atomic adds, so their last bits can differ between
+ * runs; dk is written once per key tile and is deterministic.  Errors as for diffattn_fwd; DIFFATTN_ERR_INVALID_ARG also for a
  * missing or misaligned buffer or a short workspace.
  */
 diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,
@@ -313,6 +313,39 @@ diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const vo
                              const void *dy, void *dq1, void *dk1, void *dq2, void *dk2,
                              void *dv, float *dlambda, float *dnorm_w, void *workspace,
                              size_t workspace_bytes, void *stream);
+
+/*
+ * diffattn_fwd_train_strided — diffattn_fwd_train with caller-given strides
+ * for q1, k1, q2, k2, v and out (strides[0..5], the rules of
+ * diffattn_fwd_strided: contiguous rows, every stride a positive multiple of 8
+ * elements and below 2^39).  `out` is bitwise that of diffattn_fwd_strided and
+ * `saved` that of diffattn_fwd_train on contiguous copies; the saved buffer
+ * itself is the library's contiguous layout.  Domain and errors as for
+ * diffattn_fwd_train.
+ */
+diffattn_status diffattn_fwd_train_strided(const diffattn_desc *desc, const void *q1,
+                                           const void *k1, const void *q2, const void *k2,
+                                           const void *v, const float *lambda,
+                                           const float *norm_w, void *out, void *saved,
+                                           size_t saved_bytes,
+                                           const diffattn_strides *strides, void *stream);
+
+/*
+ * diffattn_bwd_strided — diffattn_bwd with caller-given strides, so that the
+ * inputs and the gradients may be views of other layouts (for example
+ * [B, N, H, d] storage) without copies.  strides[0..10] are those of q1, k1,
+ * q2, k2, v, dy, dq1, dk1, dq2, dk2, dv, in elements, with the rules of
+ * diffattn_fwd_strided.  The same gradients as diffattn_bwd on contiguous
+ * copies (dk bitwise; dq, dv, dlambda and dnorm_w up to the order of their
+ * fp32 atomic sums).  Domain, workspace and errors as for diffattn_bwd.
+ */
+diffattn_status diffattn_bwd_strided(const diffattn_desc *desc, const void *q1, const void *k1,
+                                     const void *q2, const void *k2, const void *v,
+                                     const float *lambda, const float *norm_w,
+                                     const void *saved, const void *dy, void *dq1, void *dk1,
+                                     void *dq2, void *dk2, void *dv, float *dlambda,
+                                     float *dnorm_w, void *workspace, size_t workspace_bytes,
+                                     const diffattn_strides *strides, void *stream);
 
 /* Size of the scratch area diffattn_fwd_kv_noalloc uses: 64 MiB. */
 #define DIFFATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)

@@ -20,6 +20,7 @@ EXPECTED_ENTRY_POINTS = {
     "diffattn_fwd_strided", "diffattn_fwd_kv_plan", "diffattn_fwd_kv",
     "diffattn_fwd_kv_strided",
     "diffattn_fwd_kv_noalloc", "diffattn_train_sizes", "diffattn_fwd_train", "diffattn_bwd",
+    "diffattn_fwd_train_strided", "diffattn_bwd_strided",
     "diffattn_headnorm", "diffattn_selftest_wait", "diffattn_lambda_init", "diffattn_strerror",
     "diffattn_version"}
 
@@ -308,3 +309,37 @@ def test_fwd_host_staging_and_validation(lib):
     # empty problem: nothing to do
     e = ops.make_desc(0, 3, 300, 64, ops.BF16, True, True, 1e-5, 0.2)
     assert lib.diffattn_fwd_host(ctypes.byref(e), *args, None, 0, None) == ops.OK
+
+
+def test_strided_training_validation_before_launch(lib):
+    """diffattn_fwd_train_strided / diffattn_bwd_strided: missing or bad strides and
+    unsupported dtypes or widths are refused before anything is launched."""
+    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, 1, 1e-5, 0.2)
+    f = ctypes.c_void_p(FAKE)
+    s64 = ops.Strides(2 * 256 * 64, 256 * 64, 64)
+    s128 = ops.Strides(2 * 256 * 128, 256 * 128, 128)
+    fwd_good = [s64] * 4 + [s128] * 2
+    assert lib.diffattn_fwd_train_strided(ctypes.byref(d), *[f] * 5, f, None, f, f, 1 << 40,
+                                          None, None) == ops.ERR_INVALID_ARG
+    arr = (ops.Strides * 6)(*(fwd_good[:4] + [ops.Strides(8, 8, 12)] + fwd_good[5:]))
+    assert lib.diffattn_fwd_train_strided(ctypes.byref(d), *[f] * 5, f, None, f, f, 1 << 40,
+                                          arr, None) == ops.ERR_INVALID_ARG
+    for dt, dh in ((ops.F32, 64), (ops.BF16, 128)):
+        other = ops.make_desc(1, 2, 256, dh, dt, True, 1, 1e-5, 0.2)
+        arr = (ops.Strides * 6)(*fwd_good)
+        assert lib.diffattn_fwd_train_strided(ctypes.byref(other), *[f] * 5, f, None, f, f,
+                                              1 << 40, arr, None) == ops.ERR_UNSUPPORTED
+    # q1 k1 q2 k2 v | lambda norm_w saved dy | dq1 dk1 dq2 dk2 dv | dlambda dnorm_w
+    args = [f] * 5 + [f, None, f, f] + [f] * 5 + [f, None]
+    bwd_good = [s64] * 4 + [s128] * 2 + [s64] * 4 + [s128]
+    assert lib.diffattn_bwd_strided(ctypes.byref(d), *args, f, 1 << 40, None,
+                                    None) == ops.ERR_INVALID_ARG
+    for i in range(11):  # a bad stride in any of the eleven positions
+        bad = list(bwd_good)
+        bad[i] = ops.Strides(bad[i].b, 0, bad[i].n)
+        arr = (ops.Strides * 11)(*bad)
+        assert lib.diffattn_bwd_strided(ctypes.byref(d), *args, f, 1 << 40, arr,
+                                        None) == ops.ERR_INVALID_ARG, i
+    arr = (ops.Strides * 11)(*bwd_good)
+    assert lib.diffattn_bwd_strided(ctypes.byref(d), *args, f, 16, arr,
+                                    None) == ops.ERR_INVALID_ARG  # short workspace

@@ -139,3 +139,48 @@ def test_bwd_group_norm(N, causal, lam):
     out, g = _run(w, dy)
     _cmp(g, _oracle(w, dy), f"group norm N={N} causal={causal} lambda={lam}")
     assert torch.equal(out, harness.run_gpu(w))
+
+
+def _bnhd(t):
+    """A [B, H, N, w] view of [B, N, H, w] storage holding the same values."""
+    return t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+
+
+@pytest.mark.parametrize("causal,headnorm,N", [(True, 1, 333), (False, 2, 256), (True, 0, 130)])
+def test_train_strided_matches_contiguous(causal, headnorm, N):
+    """fwd_train_strided / bwd_strided on [B, N, H, .] storage (inputs, dy and every
+    gradient): out, saved and dk bitwise equal to the contiguous calls; dq, dv,
+    dlambda and dw up to the order of their fp32 atomic sums; and the gradients within
+    the oracle tolerance."""
+    w = W.custom(900 + N, B=2, H=3, N=N, d=64, causal=causal, headnorm=headnorm,
+                 random_w=True, layer=5)
+    dy = _dy(w, 31)
+    li = harness.lambda_init_for(w, "gpu")
+    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device="cuda")
+    nw = None if w.w is None else torch.tensor(w.w, dtype=torch.float32, device="cuda")
+    dev = [t.cuda() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    kw = dict(causal=causal, headnorm=headnorm, norm_w=nw, eps=float(np.float32(w.eps)),
+              lambda_init=li)
+    out_c, saved_c = ops.fwd_train(*dev, lam, **kw)
+    g_c = ops.bwd(*dev, lam, saved_c, dy.cuda(), **kw)
+
+    views = [_bnhd(t) for t in dev]
+    assert not views[0].is_contiguous()
+    out_s = _bnhd(torch.empty_like(out_c))
+    out_s, saved_s = ops.fwd_train_strided(*views, lam, out=out_s, **kw)
+    grads = {k: _bnhd(torch.empty_like(g_c[k])) for k in ("dq1", "dk1", "dq2", "dk2", "dv")}
+    grads["dlam"] = torch.empty_like(g_c["dlam"])
+    grads["dw"] = torch.zeros_like(g_c["dw"])
+    g_s = ops.bwd_strided(*views, lam, saved_s, _bnhd(dy.cuda()), grads=grads, **kw)
+    torch.cuda.synchronize()
+
+    assert torch.equal(out_s, out_c)
+    assert torch.equal(saved_s, saved_c)
+    for k in ("dk1", "dk2"):
+        assert torch.equal(g_s[k], g_c[k]), k
+    for k in ("dq1", "dq2", "dv", "dlam", "dw"):
+        a, b = g_s[k].float(), g_c[k].float()
+        tol = 2 ** -7 * float(b.abs().max()) + 1e-6
+        assert float((a - b).abs().max()) <= tol, k
+    names = GRADS if headnorm else GRADS[:-1]
+    _cmp({k: v.contiguous() for k, v in g_s.items()}, _oracle(w, dy), f"strided N={N}", names)
