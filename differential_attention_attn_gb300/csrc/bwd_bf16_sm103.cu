@@ -778,13 +778,13 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_kernel(const 
   float acc_w[4] = {0.f, 0.f, 0.f, 0.f};
   float acc_l = 0.f;
   const int64_t plane = p.BH * static_cast<int64_t>(p.N) * DV;
+  const __nv_bfloat16 *dy_bh = p.dy + (bh / p.H) * p.dy_sb + h * p.dy_sh;  // this head's dy
   for (int i = blockIdx.y * PRE_ROWS + warp; i < (blockIdx.y + 1) * PRE_ROWS; i += PRE_WARPS) {
     if (i >= p.n_pad) break;
     float d1 = 0.f, d2 = 0.f;
     if (i < p.N) {
       const int64_t row = (bh * p.N + i) * DV + c;
-      const uint2 yb = *reinterpret_cast<const uint2 *>(p.dy + (bh / p.H) * p.dy_sb +
-                                                        h * p.dy_sh + i * p.dy_sn + c);
+      const uint2 yb = *reinterpret_cast<const uint2 *>(dy_bh + i * p.dy_sn + c);
       const float2 y01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&yb.x));
       const float2 y23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&yb.y));
       const float dy[4] = {y01.x, y01.y, y23.x, y23.y};
