@@ -18,13 +18,17 @@
 //   1. diffattn_bwd_pre_kernel: one warp per row: do (bf16, for the tensor
 //      cores), D_1 and D_2 from the bf16-rounded do, and per-head sums of
 //      dlambda and dw (block reduction, one atomic per head and column).
-//   2. diffattn_bwd_bf16_sm103_kernel: one CTA per (head, 128-key tile, map).
-//      P is recomputed from the forward's saved log2-sum-exp, with keys on the
-//      TMEM lanes (S^T = K Q^T), so dV and dK accumulate in tensor memory over
-//      the query tiles; dQ of each query tile goes to an fp32 accumulator with
+//   2. diffattn_bwd_bf16_sm103_kernel: persistent, one CTA per SM walking
+//      work items (128-key tile, head, map), heaviest first.  P is recomputed
+//      from the forward's saved log2-sum-exp, with keys on the TMEM lanes
+//      (S^T = K Q^T), so dV and dK accumulate in tensor memory over the query
+//      tiles of an item; dQ of each query tile goes to an fp32 accumulator with
 //      vector reductions.  TMEM (512 columns): S^T / P^T 0-127, dW^T 128-255,
-//      dV 256-383, dK 384-447, dQ 448-511.
-//   3. diffattn_bwd_finish_kernel: fp32 accumulators -> bf16 gradients.
+//      dV 256-383, dK 384-447, dQ 448-511.  Inputs are read through 4-D tensor
+//      maps ([B, H, N, width] views with any strides); a second instantiation
+//      also writes dk through strides.
+//   3. diffattn_bwd_finish_kernel: fp32 accumulators -> bf16 gradients (dq1,
+//      dq2, dv; contiguous, or through strides in a second instantiation).
 //
 // Roles in kernel 2 (512 threads): warp 0 TMA producer; warp 1 TMEM
 // allocator and MMA issuer (the converged warp, one elected lane issuing);
