@@ -14,7 +14,8 @@ N=4096, causal; value width 256).  needle_4k_fp8 is the headline shape with
 q1, k1, q2, k2 in fp8 e4m3 (v and out bf16).
 needle_4k_bwd times the backward pass (diffattn_bwd given the saved
 activations of diffattn_fwd_train) on the needle_4k shape, at 20*d
-algorithmic flops per visible pair.
+algorithmic flops per visible pair; wide_4k_bwd the same on the wide_4k
+shape (d = 128).
 decode_16k is one decoding step of 32 heads (B=1, H=32, one query each)
 against a 16384-key cache through diffattn_fwd_kv with the library's split
 count; it is bound by HBM, so its metric is algorithmic GB/s (the cache read
@@ -486,7 +487,8 @@ BWD_METRIC = "diff-attn bwd TFLOP/s (causal, bf16), 1 GPU"
 
 def run_bwd(args):
     """One backward pass per step (diffattn_bwd given diffattn_fwd_train's saved
-    activations) on the needle_4k shape; 20*d algorithmic flops per visible pair."""
+    activations) on the needle_4k shape (wide_4k_bwd: the wide_4k shape, d = 128);
+    20*d algorithmic flops per visible pair."""
     from differential_attention_attn_gb300 import ops
     from differential_attention_attn_gb300 import workloads as W
 
@@ -500,15 +502,22 @@ def run_bwd(args):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     ops.load()
-    w = W.make("needle_4k", seed_offset=rank)
+    wide = args.workload == "wide_4k_bwd"
+    if wide:
+        w = W.custom(3000 + rank, B=2, H=8, N=4096, d=128, causal=True, headnorm=True,
+                     random_w=True, layer=12)
+    else:
+        w = W.make("needle_4k", seed_offset=rank)
     B, H, N, d = w.B, w.H, w.N, w.d
-    li = float(np.float32(w.lambda_init_override))
+    li = float(np.float32(ops.lambda_init(w.layer) if wide else w.lambda_init_override))
     lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device=dev)
-    kw = dict(causal=True, headnorm=True, eps=float(np.float32(w.eps)), lambda_init=li)
+    nw = torch.tensor(np.asarray(w.w, dtype=np.float32), device=dev) if wide else None
+    kw = dict(causal=True, headnorm=True, norm_w=nw, eps=float(np.float32(w.eps)),
+              lambda_init=li)
     rng = np.random.default_rng(77 + rank)
     dy_host = torch.from_numpy(rng.standard_normal((B, H, N, 2 * d))).to(torch.bfloat16)
     host = [t.contiguous() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
-    saved_bytes, ws_bytes = ops.train_sizes(B, H, N)
+    saved_bytes, ws_bytes = ops.train_sizes(B, H, N, d=d)
     set_bytes = sum(t.numel() * t.element_size() for t in host) + saved_bytes + \
         dy_host.numel() * 2
     n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
@@ -562,7 +571,7 @@ def run_bwd(args):
         "median_ms_per_launch": med_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "needle_4k_bwd", "B": B, "H": H, "N": N, "d": d, "dv": 2 * d,
+        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "dv": 2 * d,
                    "causal": True, "headnorm": True,
                    "flops_convention": "20*d per visible pair (S1, S2, dW, dV, dQ, dK), "
                                        "B*H*N^2/2 pairs",
@@ -574,10 +583,13 @@ def run_bwd(args):
                      "peak": peak, "unit": UNIT,
                      "frac": flops_step / (launch_ms * 1e-3) / 1e12 / peak,
                      "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS bf16 GEMM)",
-                     "kernel": "diffattn_bwd_pre_kernel + diffattn_bwd_bf16_sm103_kernel + "
-                               "diffattn_bwd_finish_kernel (+ 4 memsets), timed together",
+                     "kernel": ("diffattn_bwd_pre_d128_kernel + diffattn_bwd_d128_sm103_kernel"
+                                "<dV> + <dK/dQ> + diffattn_bwd_finish_d128_kernel (+ 3 memsets)"
+                                if wide else
+                                "diffattn_bwd_pre_kernel + diffattn_bwd_bf16_sm103_kernel + "
+                                "diffattn_bwd_finish_kernel (+ 4 memsets)") + ", timed together",
                      "alg_flops_per_launch": flops_step, "traffic": None},
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps * (4 if wide else 3),
         "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
     }
     print(json.dumps(line), flush=True)
@@ -591,7 +603,7 @@ def run_ours(args):
 
     if args.workload in DECODE:
         return run_decode(args)
-    if args.workload == "needle_4k_bwd":
+    if args.workload in ("needle_4k_bwd", "wide_4k_bwd"):
         return run_bwd(args)
     WORKLOAD = args.workload
 
@@ -841,7 +853,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["needle_4k", "small_causal", "mid_causal", "long_16k", "rising_4k",
-                             *DECODE, "needle_4k_bwd", "wide_4k", "needle_4k_fp8"])
+                             *DECODE, "needle_4k_bwd", "wide_4k_bwd", "wide_4k",
+                             "needle_4k_fp8"])
     ap.add_argument("--scaling", choices=["strong", "weak"], default="strong",
                     help="with several GPUs: partition the heads (strong) or replicate (weak)")
     args = ap.parse_args()

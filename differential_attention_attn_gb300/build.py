@@ -24,7 +24,8 @@ LIB = os.path.join(HERE, "libdiffattn.so")
 BUILD_DEBUG = os.path.join(HERE, "_build_debug")
 LIB_DEBUG = os.path.join(HERE, "libdiffattn_debug.so")
 SOURCES = ["api.cu", "fwd_bf16_sm103.cu", "fwd_f32.cu", "headnorm.cu", "splitkv.cu",
-           "noalloc.cu", "bwd_bf16_sm103.cu", "fwd_d128_sm103.cu", "selftest.cu"]
+           "noalloc.cu", "bwd_bf16_sm103.cu", "fwd_d128_sm103.cu", "bwd_d128_sm103.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -316,8 +316,14 @@ diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_by
   diffattn_status st = check_desc(desc);
   if (st != DIFFATTN_OK) return st;
   if (saved_bytes == nullptr || workspace_bytes == nullptr) return DIFFATTN_ERR_INVALID_ARG;
-  if (desc->dtype != DIFFATTN_BF16 || desc->d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (desc->dtype != DIFFATTN_BF16 || (desc->d != 64 && desc->d != 128))
+    return DIFFATTN_ERR_UNSUPPORTED;
   const int64_t BH = desc->B * desc->H;
+  if (desc->d == 128) {
+    *saved_bytes = static_cast<size_t>(saved_bytes_d128(BH, desc->N));
+    *workspace_bytes = static_cast<size_t>(bwd_workspace_bytes_d128(BH, desc->N));
+    return DIFFATTN_OK;
+  }
   *saved_bytes = static_cast<size_t>(saved_floats(BH, desc->N)) * sizeof(float);
   *workspace_bytes = static_cast<size_t>(bwd_workspace_floats(BH, desc->N)) * sizeof(float);
   return DIFFATTN_OK;
@@ -336,6 +342,9 @@ diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, co
       !aligned16(out) || !aligned16(saved) || saved_bytes < need)
     return DIFFATTN_ERR_INVALID_ARG;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  if (desc->d == 128)
+    return launch_fwd_train_d128(*desc, q1, k1, q2, k2, v, lambda, norm_w, out, saved,
+                                 static_cast<cudaStream_t>(stream), nullptr);
   return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
                                static_cast<cudaStream_t>(stream), 1, nullptr,
                                static_cast<float *>(saved));
@@ -361,6 +370,10 @@ diffattn_status bwd_common(const diffattn_desc *desc, const void *q1, const void
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DIFFATTN_ERR_INVALID_ARG;
   if (strides != nullptr && (st = check_strides(strides, kBwdStrides)) != DIFFATTN_OK) return st;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  if (desc->d == 128)
+    return launch_bwd_d128_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w, saved, dy, dq1, dk1,
+                                 dq2, dk2, dv, dlambda, dnorm_w, workspace,
+                                 static_cast<cudaStream_t>(stream), strides);
   return launch_bwd_bf16_sm103(*desc, q1, k1, q2, k2, v, lambda, norm_w,
                                static_cast<const float *>(saved), dy, dq1, dk1, dq2, dk2, dv,
                                dlambda, dnorm_w, static_cast<float *>(workspace),
@@ -412,6 +425,9 @@ diffattn_status diffattn_fwd_train_strided(const diffattn_desc *desc, const void
   if ((st = check_strides(strides)) != DIFFATTN_OK) return st;
   if (desc->B > INT32_MAX || desc->H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
   if ((st = check_sm103()) != DIFFATTN_OK) return st;
+  if (desc->d == 128)
+    return launch_fwd_train_d128(*desc, q1, k1, q2, k2, v, lambda, norm_w, out, saved,
+                                 static_cast<cudaStream_t>(stream), strides);
   return launch_fwd_bf16_sm103(*desc, desc->N, q1, k1, q2, k2, v, lambda, norm_w, out,
                                static_cast<cudaStream_t>(stream), 1, nullptr,
                                static_cast<float *>(saved), strides);

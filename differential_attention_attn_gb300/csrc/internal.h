@@ -84,12 +84,34 @@ int auto_splits(int64_t BH, int64_t N, int64_t n_kv, bool causal, int sm_count);
 // (statistics, then one normalised accumulator) of N queries against n_kv
 // keys (causal: the queries are the last N positions); [B, H, rows, width]
 // with the element strides of q1, k1, q2, k2, v, out given (rows contiguous),
-// or contiguous when strides is null.
+// or contiguous when strides is null.  Training: save_lse (fp32
+// [2][BH][128 * n_qtiles]) receives each map's log2-sum-exp; with map_out
+// non-null, lambda is taken as 0 and map 1's normalised output is written there
+// in fp32 ([BH][N][256]) instead of `out`.
 diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
                                       const void *k1, const void *q2, const void *k2,
                                       const void *v, const float *lambda, const float *norm_w,
                                       void *out, cudaStream_t stream,
-                                      const diffattn_strides *strides = nullptr);
+                                      const diffattn_strides *strides = nullptr,
+                                      float *save_lse = nullptr, float *map_out = nullptr);
+
+// Backward pass for d = 128 (bwd_d128_sm103.cu): saved-activation and workspace
+// sizes in bytes, and the launch of its kernels (preprocess, the dV items, the
+// dK / dQ items, dq conversion).  The saved buffer holds each map's normalised
+// output o_k (bf16 [2][B*H][N][256]) and log2-sum-exp (fp32 [2][B*H][n_pad]).
+int64_t saved_bytes_d128(int64_t BH, int64_t N);
+int64_t bwd_workspace_bytes_d128(int64_t BH, int64_t N);
+diffattn_status launch_fwd_train_d128(const diffattn_desc &desc, const void *q1, const void *k1,
+                                      const void *q2, const void *k2, const void *v,
+                                      const float *lambda, const float *norm_w, void *out,
+                                      void *saved, cudaStream_t stream,
+                                      const diffattn_strides *strides);
+diffattn_status launch_bwd_d128_sm103(const diffattn_desc &desc, const void *q1, const void *k1,
+                                      const void *q2, const void *k2, const void *v,
+                                      const float *lambda, const float *norm_w, const void *saved,
+                                      const void *dy, void *dq1, void *dk1, void *dq2, void *dk2,
+                                      void *dv, float *dlambda, float *dnorm_w, void *workspace,
+                                      cudaStream_t stream, const diffattn_strides *strides);
 
 // Bounded-wait self-test (selftest.cu).
 diffattn_status launch_selftest_wait(int32_t *status, int64_t timeout_ns, cudaStream_t stream);

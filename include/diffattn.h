@@ -110,8 +110,8 @@ typedef struct diffattn_desc {
  *     otherwise).  Runs a fused tcgen05/TMEM/TMA kernel (for d == 128 a
  *     two-pass one: row statistics, then a single normalised accumulator);
  *     needs an sm_103 device.  diffattn_fwd_strided takes both head widths;
- *     so does the key/value-cache entry (diffattn_fwd_kv, single pass);
- *     training takes d == 64 only.
+ *     so does the key/value-cache entry (diffattn_fwd_kv, single pass), and
+ *     so does training.
  *   - DIFFATTN_F32: 1 <= d <= 128, N <= 4096.  Plain CUDA-core kernel
  *     (accurate expf, fp32 accumulation).
  *   - DIFFATTN_E4M3_QK: d == 64, headnorm 0 or 1: the d == 64 kernel with the
@@ -271,9 +271,13 @@ diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, in
  *   dS_1 = P_1 * (dW - do.o1),  dS_2 = -lambda P_2 * (dW - do.o2)  (per row)
  *   dQ_k = dS_k K_k / sqrt(d),  dK_k = dS_k^T Q_k / sqrt(d)
  *
- * Domain: DIFFATTN_BF16, d == 64, square attention (N queries = N keys),
- * causal or not, headnorm 0, 1 or 2 (the group form: the page's GroupNorm); an sm_103
- * device.
+ * Domain: DIFFATTN_BF16, d == 64 or d == 128, square attention (N queries =
+ * N keys), causal or not, headnorm 0, 1 or 2 (the group form: the page's
+ * GroupNorm); an sm_103 device.  d == 128 runs its own kernels: the saving
+ * forward is the d == 128 forward three times (the output with each map's
+ * log2-sum-exp, then each map's output alone), and the backward two kinds of
+ * work item (one computing dV from both maps, one computing one map's dK and
+ * dQ), since the d == 64 kernel's tensor-memory layout does not fit 2d = 256.
  */
 
 /* Bytes of the saved-activation buffer diffattn_fwd_train fills and of the
@@ -285,9 +289,10 @@ diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_by
  * diffattn_fwd_train — diffattn_fwd (same arguments, same `out`, bitwise)
  * that also writes `saved` (caller-owned device buffer of at least
  * saved_bytes from diffattn_train_sizes, 16-byte aligned): each map's
- * normalised output o_k (fp32 [2][B*H][N][128]) and log2-sum-exp
- * (fp32 [2][B*H][128 * ceil(N / 128)]).  Keep it unchanged until the
- * matching diffattn_bwd has run.
+ * normalised output o_k (fp32 [2][B*H][N][2d]) and log2-sum-exp
+ * (fp32 [2][B*H][128 * ceil(N / 128)]; for d == 128 each region starts on a
+ * 256-byte boundary).  Keep it unchanged until the matching diffattn_bwd has
+ * run.
  */
 diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, const void *k1,
                                    const void *q2, const void *k2, const void *v,
@@ -297,14 +302,15 @@ diffattn_status diffattn_fwd_train(const diffattn_desc *desc, const void *q1, co
 /*
  * diffattn_bwd — gradients given the forward inputs, the same desc, lambda
  * and norm_w, the `saved` buffer of diffattn_fwd_train and dy (bf16
- * [B, H, N, 128]).  Outputs (all device, overwritten): dq1, dk1, dq2, dk2
- * bf16 [B, H, N, 64]; dv bf16 [B, H, N, 128]; dlambda fp32 [H]; dnorm_w fp32
- * [H, 128] (written when headnorm is 1 or 2; may be NULL to skip it).
+ * [B, H, N, 2d]).  Outputs (all device, overwritten): dq1, dk1, dq2, dk2
+ * bf16 [B, H, N, d]; dv bf16 [B, H, N, 2d]; dlambda fp32 [H]; dnorm_w fp32
+ * [H, 2d] (written when headnorm is 1 or 2; may be NULL to skip it).
  * workspace: caller-owned scratch of at least workspace_bytes from
  * diffattn_train_sizes, 256-byte aligned (its contents on entry do not
- * matter).  dq and dv are summed over key tiles, dlambda and dnorm_w over
- * row blocks, with fp32 atomic adds, so their last bits can differ between
- * runs; dk is written once per key tile and is deterministic.  Errors as for diffattn_fwd; DIFFATTN_ERR_INVALID_ARG also for a
+ * matter).  dq (and, for d == 64, dv) is summed over key tiles, dlambda and
+ * dnorm_w over row blocks, with fp32 atomic adds, so their last bits can
+ * differ between runs; dk (and, for d == 128, dv) is written once per key
+ * tile and is deterministic.  Errors as for diffattn_fwd; DIFFATTN_ERR_INVALID_ARG also for a
  * missing or misaligned buffer or a short workspace.
  */
 diffattn_status diffattn_bwd(const diffattn_desc *desc, const void *q1, const void *k1,

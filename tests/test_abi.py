@@ -188,6 +188,17 @@ def test_train_sizes(lib):
     f32 = ops.make_desc(B, H, N, 8, ops.F32, True, True, 1e-5, 0.2)
     assert lib.diffattn_train_sizes(ctypes.byref(f32), ctypes.byref(a),
                                     ctypes.byref(b)) == ops.ERR_UNSUPPORTED
+    # d = 128: fp32 map outputs [2][BH][N][256] and fp32 log2-sum-exp, each region
+    # rounded to 256 bytes; the workspace holds dO, c D and the fp32 dq accumulator
+    r256 = lambda x: (x + 255) // 256 * 256
+    wide = ops.make_desc(B, H, N, 128, ops.BF16, True, True, 1e-5, 0.2)
+    assert lib.diffattn_train_sizes(ctypes.byref(wide), ctypes.byref(a), ctypes.byref(b)) == ops.OK
+    assert a.value == r256(2 * B * H * N * 256 * 4) + r256(2 * B * H * n_pad * 4)
+    assert b.value == (r256(B * H * N * 256 * 2) + r256(2 * B * H * n_pad * 4) +
+                       r256(2 * B * H * N * 128 * 4))
+    odd = ops.make_desc(B, H, N, 96, ops.BF16, True, True, 1e-5, 0.2)
+    assert lib.diffattn_train_sizes(ctypes.byref(odd), ctypes.byref(a),
+                                    ctypes.byref(b)) == ops.ERR_UNSUPPORTED
 
 
 def test_bwd_validation_before_launch(lib):
@@ -324,7 +335,7 @@ def test_strided_training_validation_before_launch(lib):
     arr = (ops.Strides * 6)(*(fwd_good[:4] + [ops.Strides(8, 8, 12)] + fwd_good[5:]))
     assert lib.diffattn_fwd_train_strided(ctypes.byref(d), *[f] * 5, f, None, f, f, 1 << 40,
                                           arr, None) == ops.ERR_INVALID_ARG
-    for dt, dh in ((ops.F32, 64), (ops.BF16, 128)):
+    for dt, dh in ((ops.F32, 64), (ops.BF16, 96)):
         other = ops.make_desc(1, 2, 256, dh, dt, True, 1, 1e-5, 0.2)
         arr = (ops.Strides * 6)(*fwd_good)
         assert lib.diffattn_fwd_train_strided(ctypes.byref(other), *[f] * 5, f, None, f, f,

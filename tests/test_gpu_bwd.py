@@ -2,7 +2,11 @@
 oracle's gradients.
 
 Tolerance per gradient tensor: max-abs <= 2e-2 * max|oracle| (bf16 inputs, P, dS and
-do on the tensor cores, fp32 accumulation; bf16 dq, dk, dv outputs).
+do on the tensor cores, fp32 accumulation; bf16 dq, dk, dv outputs).  dlambda =
+-sum_rows do . o_2 cancels heavily (the head norm leaves do nearly orthogonal to o), so
+its error is a sum of random-sign rounding errors of the rows' terms (the forward's
+bf16 P in o_k): it grows with the square root of the row width, and its bound is
+2e-2 * sqrt(d / 64) * max|oracle| (the d = 64 bound at d = 64).
 """
 import numpy as np
 import pytest
@@ -42,12 +46,14 @@ def _oracle(w, dy):
 
 
 def _cmp(g, ref, what, names=GRADS):
+    d = g["dq1"].shape[-1]
     for k in names:
         got = g[k].double().cpu().numpy()
         assert np.all(np.isfinite(got)), f"{what} {k}: non-finite"
         mx = float(np.max(np.abs(ref[k])))
         err = float(np.max(np.abs(got - ref[k])))
-        assert err <= 2e-2 * mx + 1e-6, f"{what} {k}: max-abs err {err:.3g} > 2e-2 * {mx:.3g}"
+        rel = 2e-2 * (np.sqrt(d / 64) if k == "dlam" else 1.0)
+        assert err <= rel * mx + 1e-6, f"{what} {k}: max-abs err {err:.3g} > {rel:.3g} * {mx:.3g}"
 
 
 @pytest.mark.parametrize("N", [1, 7, 128, 129, 200, 256, 384])
@@ -146,13 +152,15 @@ def _bnhd(t):
     return t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
 
 
-@pytest.mark.parametrize("causal,headnorm,N", [(True, 1, 333), (False, 2, 256), (True, 0, 130)])
-def test_train_strided_matches_contiguous(causal, headnorm, N):
+@pytest.mark.parametrize("causal,headnorm,N,d", [(True, 1, 333, 64), (False, 2, 256, 64),
+                                                 (True, 0, 130, 64), (True, 1, 200, 128),
+                                                 (False, 2, 256, 128)])
+def test_train_strided_matches_contiguous(causal, headnorm, N, d):
     """fwd_train_strided / bwd_strided on [B, N, H, .] storage (inputs, dy and every
     gradient): out, saved and dk bitwise equal to the contiguous calls; dq, dv,
     dlambda and dw up to the order of their fp32 atomic sums; and the gradients within
     the oracle tolerance."""
-    w = W.custom(900 + N, B=2, H=3, N=N, d=64, causal=causal, headnorm=headnorm,
+    w = W.custom(900 + N, B=2, H=3, N=N, d=d, causal=causal, headnorm=headnorm,
                  random_w=True, layer=5)
     dy = _dy(w, 31)
     li = harness.lambda_init_for(w, "gpu")
@@ -183,4 +191,29 @@ def test_train_strided_matches_contiguous(causal, headnorm, N):
         tol = 2 ** -7 * float(b.abs().max()) + 1e-6
         assert float((a - b).abs().max()) <= tol, k
     names = GRADS if headnorm else GRADS[:-1]
-    _cmp({k: v.contiguous() for k, v in g_s.items()}, _oracle(w, dy), f"strided N={N}", names)
+    _cmp({k: v.contiguous() for k, v in g_s.items()}, _oracle(w, dy), f"strided N={N} d={d}",
+         names)
+
+
+@pytest.mark.parametrize("N,causal,headnorm", [(128, True, 1), (200, True, 1), (256, False, 2),
+                                               (384, True, 0), (130, False, 1)])
+def test_bwd_d128(N, causal, headnorm):
+    """d = 128 (values 256 wide): the saving forward's output equals the plain
+    forward's bitwise, and every gradient is within the oracle tolerance."""
+    w = W.custom(1100 + N, B=2, H=2, N=N, d=128, causal=causal, headnorm=headnorm,
+                 random_w=True, layer=5)
+    dy = _dy(w, N + 3)
+    out, g = _run(w, dy)
+    names = GRADS if headnorm else GRADS[:-1]
+    _cmp(g, _oracle(w, dy), f"d=128 N={N} causal={causal} headnorm={headnorm}", names)
+    assert torch.equal(out, harness.run_gpu(w))
+
+
+def test_bwd_d128_many_items():
+    """d = 128 with more dV and dK/dQ items than SMs (B=3, H=4, N=1100 causal:
+    9 key tiles, a ragged last one, 108 dV and 216 dK/dQ items)."""
+    w = W.custom(1200, B=3, H=4, N=1100, d=128, causal=True, headnorm=1, random_w=True,
+                 layer=7)
+    dy = _dy(w, 1200)
+    _, g = _run(w, dy)
+    _cmp(g, _oracle(w, dy), "d=128 B3H4N1100")

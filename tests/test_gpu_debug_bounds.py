@@ -64,11 +64,12 @@ def test_kv_split_and_combine(dbg, Nq, Nkv, splits):
     _check(rel, got, st, f"kv {Nq}/{Nkv} splits {splits}")
 
 
-@pytest.mark.parametrize("N", [7, 129, 256])
-def test_training_forward_and_backward(dbg, N):
-    w = W.custom(1400 + N, B=1, H=2, N=N, d=64, causal=True, headnorm=True, random_w=True,
+@pytest.mark.parametrize("N,d", [(7, 64), (129, 64), (256, 64), (1, 128), (200, 128),
+                                 (257, 128)])
+def test_training_forward_and_backward(dbg, N, d):
+    w = W.custom(1400 + N, B=1, H=2, N=N, d=d, causal=True, headnorm=True, random_w=True,
                  layer=3)
-    dy = torch.from_numpy(np.random.default_rng(N).standard_normal((1, 2, N, 128))).to(
+    dy = torch.from_numpy(np.random.default_rng(N).standard_normal((1, 2, N, 2 * d))).to(
         torch.bfloat16).cuda()
     li = harness.lambda_init_for(w, "gpu")
     lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device="cuda")
@@ -84,7 +85,7 @@ def test_training_forward_and_backward(dbg, N):
         # are summed with atomic adds (their last bits may differ run to run).
         return {"out": out, "saved": saved, "dk1": g["dk1"], "dk2": g["dk2"]}
     rel, got, st = _both(dbg, run)
-    _check(rel, got, st, f"train N={N}")
+    _check(rel, got, st, f"train N={N} d={d}")
 
 
 @pytest.mark.parametrize("N", [1, 65, 200])
