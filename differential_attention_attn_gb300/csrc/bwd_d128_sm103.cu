@@ -20,8 +20,11 @@
 //                 dQ = dS K (drained to an fp32 accumulator)   (512 columns)
 // Both recompute P from the saved log2-sum-exp.  Each CTA streams its query
 // tiles through one shared-memory stage (a second would not fit beside the
-// K, V and dO tiles of this width), so a tile's loads wait for the previous
-// tile's products.
+// K, V and dO tiles of this width), refilled piecewise as each operand is
+// released: in dK/dQ items dO once dW^T is computed and Q once dK is (the
+// products run dK, dQ, then the next tile's dW^T before its S^T, so the next
+// dO streams in under the softmax and dK / dQ); in dV items Q once S^T is
+// computed and dO once dV is.
 //
 // The saving forward runs the d = 128 forward three times: the output (also
 // writing each map's log2-sum-exp), and map 1's and map 2's normalised outputs
@@ -62,11 +65,19 @@ constexpr uint32_t V_OFF_DO = 8 * BOX, V_OFF_VEC = 12 * BOX;
 constexpr uint32_t K_OFF_K = 0, K_OFF_V = 2 * BOX, K_OFF_Q = 6 * BOX, K_OFF_DO = 8 * BOX;
 constexpr uint32_t K_OFF_DS = 12 * BOX, K_OFF_VEC = 14 * BOX;
 constexpr uint32_t VEC_BYTES = 2 * BQ * 4;
+// dV items load a tile's vectors with its queries, which are released while
+// the previous tile's softmax may still read its own: two slots.
+template <bool kDV>
+constexpr int vec_slots() {
+  return kDV ? 2 : 1;
+}
 
 struct Ctrl {
   uint64_t kv_full;   // the item's key (and value) tiles
-  uint64_t qd_full;   // the tile's queries, dO and per-query vectors
-  uint64_t qd_empty;  // the tile's products are done: the stage may be refilled
+  uint64_t q_full;    // the tile's queries and per-query vectors
+  uint64_t q_empty;   // the tile's queries have been read (dV items: S^T; dK/dQ: dK)
+  uint64_t do_full;   // the tile's dO
+  uint64_t do_empty;  // the tile's dO has been read (dV items: dV; dK/dQ: dW^T)
   uint64_t s_full;    // S^T (and dW^T) of the tile
   uint64_t p_ready;   // the tile's packed operands are published (per thread)
   uint64_t acc_done;  // the item's dV or dK is complete
@@ -79,7 +90,7 @@ struct Ctrl {
 
 template <bool kDV>
 constexpr uint32_t off_ctrl() {
-  return (kDV ? V_OFF_VEC : K_OFF_VEC) + VEC_BYTES;
+  return (kDV ? V_OFF_VEC : K_OFF_VEC) + vec_slots<kDV>() * VEC_BYTES;
 }
 template <bool kDV>
 constexpr uint32_t smem_bytes() {
@@ -220,8 +231,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->kv_full, 1);
-    mbar_init(&ctrl->qd_full, 1);
-    mbar_init(&ctrl->qd_empty, 1);
+    mbar_init(&ctrl->q_full, 1);
+    mbar_init(&ctrl->q_empty, 1);
+    mbar_init(&ctrl->do_full, 1);
+    mbar_init(&ctrl->do_empty, 1);
     mbar_init(&ctrl->s_full, 1);
     mbar_init(&ctrl->p_ready, SOFTMAX_THREADS);
     mbar_init(&ctrl->acc_done, 1);
@@ -243,7 +256,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      uint32_t issued = 0;
       bool ok = true;
       if (kDV) {
         mbar_arrive_expect_tx(&ctrl->kv_full, 4 * BOX);
@@ -261,33 +273,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const float *lse_a = p.lse + (w.map * p.BH + w.bh) * n_pad;
       const float *lse_b = kDV ? p.lse + (p.BH + w.bh) * n_pad : p.dvec + (w.map * p.BH + w.bh) * n_pad;
-      for (int it = 0; it < w.n_q; ++it) {
-        if (it > 0 && !(ok = mbar_wait(&ctrl->qd_empty, (it - 1) & 1, abort_flag, WAIT_TIMEOUT_NS)))
-          break;
+      // Per tile: the queries (and vectors), then dO, each after the previous
+      // tile released it; in dK/dQ items dO is released first, so it goes first.
+      auto load_q = [&](int it) {
         const int q0 = (w.qt_first + it) * BQ;
-        uint64_t *bar = &ctrl->qd_full;
-        uint8_t *vec = smem + (kDV ? V_OFF_VEC : K_OFF_VEC);
-        mbar_arrive_expect_tx(bar, (kDV ? 8 : 6) * BOX + VEC_BYTES);
+        uint8_t *vec = smem + (kDV ? V_OFF_VEC : K_OFF_VEC) + (it % vec_slots<kDV>()) * VEC_BYTES;
+        mbar_arrive_expect_tx(&ctrl->q_full, (kDV ? 4 : 2) * BOX + VEC_BYTES);
         if (kDV) {
           for (int x = 0; x < 2; ++x) {
-            tma_load_4d(smem + V_OFF_Q1 + x * BOX, &tm_q1, bar, 64 * x, q0, w.h, w.b);
-            tma_load_4d(smem + V_OFF_Q2 + x * BOX, &tm_q2, bar, 64 * x, q0, w.h, w.b);
+            tma_load_4d(smem + V_OFF_Q1 + x * BOX, &tm_q1, &ctrl->q_full, 64 * x, q0, w.h, w.b);
+            tma_load_4d(smem + V_OFF_Q2 + x * BOX, &tm_q2, &ctrl->q_full, 64 * x, q0, w.h, w.b);
           }
         } else {
           const CUtensorMap *tq = w.map ? &tm_q2 : &tm_q1;
           for (int x = 0; x < 2; ++x)
-            tma_load_4d(smem + K_OFF_Q + x * BOX, tq, bar, 64 * x, q0, w.h, w.b);
+            tma_load_4d(smem + K_OFF_Q + x * BOX, tq, &ctrl->q_full, 64 * x, q0, w.h, w.b);
         }
+        bulk_g2s(vec, lse_a + q0, BQ * 4, &ctrl->q_full);
+        bulk_g2s(vec + BQ * 4, lse_b + q0, BQ * 4, &ctrl->q_full);
+      };
+      auto load_do = [&](int it) {
+        const int q0 = (w.qt_first + it) * BQ;
+        mbar_arrive_expect_tx(&ctrl->do_full, 4 * BOX);
         for (int x = 0; x < 4; ++x)
-          tma_load_4d(smem + (kDV ? V_OFF_DO : K_OFF_DO) + x * BOX, &tm_do, bar, 64 * x, q0, w.h,
-                      w.b);
-        bulk_g2s(vec, lse_a + q0, BQ * 4, bar);
-        bulk_g2s(vec + BQ * 4, lse_b + q0, BQ * 4, bar);
-        issued = it + 1;
+          tma_load_4d(smem + (kDV ? V_OFF_DO : K_OFF_DO) + x * BOX, &tm_do, &ctrl->do_full,
+                      64 * x, q0, w.h, w.b);
+      };
+      uint32_t issued_q = 0, issued_do = 0;
+      for (int it = 0; it < w.n_q; ++it) {
+        const uint32_t par = static_cast<uint32_t>(it - 1) & 1u;
+        if (kDV) {
+          if (it > 0 && !(ok = mbar_wait(&ctrl->q_empty, par, abort_flag, WAIT_TIMEOUT_NS))) break;
+          load_q(it);
+          issued_q = it + 1;
+          if (it > 0 && !(ok = mbar_wait(&ctrl->do_empty, par, abort_flag, WAIT_TIMEOUT_NS))) break;
+          load_do(it);
+          issued_do = it + 1;
+        } else {
+          if (it > 0 && !(ok = mbar_wait(&ctrl->do_empty, par, abort_flag, WAIT_TIMEOUT_NS))) break;
+          load_do(it);
+          issued_do = it + 1;
+          if (it > 0 && !(ok = mbar_wait(&ctrl->q_empty, par, abort_flag, WAIT_TIMEOUT_NS))) break;
+          load_q(it);
+          issued_q = it + 1;
+        }
       }
       // Loads still in flight land before the CTA exits.
       drain_wait(&ctrl->kv_full, 0);
-      if (issued > 0) drain_wait(&ctrl->qd_full, (issued - 1) & 1);
+      if (issued_q > 0) drain_wait(&ctrl->q_full, (issued_q - 1) & 1);
+      if (issued_do > 0) drain_wait(&ctrl->do_full, (issued_do - 1) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -303,13 +337,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto wait_all = [&](uint64_t *bar, uint32_t parity) {
       return mbar_wait_warp(bar, parity, abort_flag, WAIT_TIMEOUT_NS);
     };
-    bool ok = wait_all(&ctrl->kv_full, 0);
-    tc_fence_after_sync();
-    for (int it = 0; ok && it < w.n_q; ++it) {
-      if (!(ok = wait_all(&ctrl->qd_full, it & 1))) break;
+    constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);
+    // S^T of tile `it` (dV items: S1^T and S2^T), once its queries have landed.
+    auto issue_s = [&](int it) {
+      if (!wait_all(&ctrl->q_full, it & 1)) return false;
       tc_fence_after_sync();
       if (kDV) {
-        constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           umma_bf16_ss_lo_warp(tmem + TM_S, kmaj(V_OFF_K1) + kstep(kk), kmaj(V_OFF_Q1) + kstep(kk),
@@ -318,20 +351,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                kmaj(V_OFF_Q2) + kstep(kk), dhi, ID_S, kk > 0);
         }
       } else {
-        constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16_ss_lo_warp(tmem + TM_S, kmaj(K_OFF_K) + kstep(kk), kmaj(K_OFF_Q) + kstep(kk),
                                dhi, ID_S, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk)  // dW^T = V dO^T
-          umma_bf16_ss_lo_warp(tmem + TM_W, kmaj(K_OFF_V) + kstep(kk), kmaj(K_OFF_DO) + kstep(kk),
-                               dhi, ID_S, kk > 0);
       }
-      umma_commit_warp(&ctrl->s_full);
+      return true;
+    };
+    // dW^T = V dO^T of tile `it` (dK/dQ items), once its dO has landed.
+    auto issue_dw = [&](int it) {
+      if (!wait_all(&ctrl->do_full, it & 1)) return false;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < DV / 16; ++kk)
+        umma_bf16_ss_lo_warp(tmem + TM_W, kmaj(K_OFF_V) + kstep(kk), kmaj(K_OFF_DO) + kstep(kk),
+                             dhi, ID_S, kk > 0);
+      return true;
+    };
+    bool ok = wait_all(&ctrl->kv_full, 0);
+    tc_fence_after_sync();
+    if (ok) {  // the first tile's S^T (and dW^T)
+      if (kDV) {
+        if ((ok = issue_s(0))) {
+          umma_commit_warp(&ctrl->s_full);
+          umma_commit_warp(&ctrl->q_empty);
+        }
+      } else if ((ok = issue_dw(0) && issue_s(0))) {
+        umma_commit_warp(&ctrl->do_empty);
+        umma_commit_warp(&ctrl->s_full);
+      }
+    }
+    // Tile `it`'s products, then the next tile's S^T (and dW^T): the stage's
+    // operands are released as soon as their last product has read them.
+    for (int it = 0; ok && it < w.n_q; ++it) {
+      const bool more = it + 1 < w.n_q;
       if (!(ok = wait_all(&ctrl->p_ready, it & 1))) break;
       tc_fence_after_sync();
       if (kDV) {
+        if (!(ok = wait_all(&ctrl->do_full, it & 1))) break;
+        tc_fence_after_sync();
         // dV += W^T dO: A packed in TMEM, B = dO read MN-major (N = 256 in four
         // 64-column blocks); 16 queries = 2048 bytes of each block.
         constexpr uint32_t ID_DV = idesc_ab(BK, DV, false, true);
@@ -340,11 +398,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_bf16_ts_lo_warp(tmem + TM_DV, tmem + TM_S + tm_pack(kk),
                                mnmaj(V_OFF_DO) + ((2048u * kk) >> 4), dhi, ID_DV,
                                (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_warp(&ctrl->qd_empty);
+        umma_commit_warp(&ctrl->do_empty);
+        // The next S^T goes over this tile's packed W^T: MMAs run in issue order.
+        if (more) {
+          if (!(ok = issue_s(it + 1))) break;
+          umma_commit_warp(&ctrl->s_full);
+          umma_commit_warp(&ctrl->q_empty);
+        }
       } else {
-        // The previous tile's dQ must have been read before this one overwrites it.
-        if (it > 0 && !(ok = wait_all(&ctrl->dq_free, (it - 1) & 1))) break;
-        tc_fence_after_sync();
         // dK += dS^T Q: A packed in TMEM, B = Q MN-major (N = 128: two blocks).
         constexpr uint32_t ID_DK = idesc_ab(BK, HD, false, true);
 #pragma unroll
@@ -352,6 +413,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_bf16_ts_lo_warp(tmem + TM_DK, tmem + TM_S + tm_pack(kk),
                                mnmaj(K_OFF_Q) + ((2048u * kk) >> 4), dhi, ID_DK,
                                (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_warp(&ctrl->q_empty);
+        // The previous tile's dQ must have been read before this one overwrites it.
+        if (it > 0 && !(ok = wait_all(&ctrl->dq_free, (it - 1) & 1))) break;
+        tc_fence_after_sync();
         // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (N = d);
         // 16 keys = 2048 bytes of each block.
         constexpr uint32_t ID_DQ = idesc_ab(BQ, HD, true, true);
@@ -359,8 +424,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kk = 0; kk < BK / 16; ++kk)
           umma_bf16_ss_lo_warp(tmem + TM_DQ, mnmaj(K_OFF_DS) + ((2048u * kk) >> 4),
                                mnmaj(K_OFF_K) + ((2048u * kk) >> 4), dhi, ID_DQ, kk > 0);
-        umma_commit_warp(&ctrl->qd_empty);
         umma_commit_warp(&ctrl->dq_full);
+        // The next tile: dW^T (dO arrived under this tile's softmax), then S^T
+        // over this tile's packed dS^T (MMAs run in issue order).
+        if (more) {
+          if (!(ok = issue_dw(it + 1))) break;
+          umma_commit_warp(&ctrl->do_empty);
+          if (!(ok = issue_s(it + 1))) break;
+          umma_commit_warp(&ctrl->s_full);
+        }
       }
     }
     if (ok) umma_commit_warp(&ctrl->acc_done);
@@ -381,7 +453,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool key_ok = kpos < p.N;
     const float lam = p.lambda[w.h];
     const float coef = w.map ? -lam : 1.f;
-    const float *vec = reinterpret_cast<const float *>(smem + (kDV ? V_OFF_VEC : K_OFF_VEC));
+    const float *vec0 = reinterpret_cast<const float *>(smem + (kDV ? V_OFF_VEC : K_OFF_VEC));
     // dQ of tile `t` (query tile q0) into the fp32 accumulator: this thread's
     // query row, 64 columns, transposed across 8-lane groups so that each vector
     // reduction covers four 128-byte row segments.
@@ -431,6 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
+      const float *vec = vec0 + (it % vec_slots<kDV>()) * (VEC_BYTES / 4);
       // Query column c of the tile (query q0 + c) is visible iff lo <= c < hi.
       const int lo = p.causal ? (kpos - q0) : 0;
       const int hi = key_ok ? (p.N - q0) : 0;
