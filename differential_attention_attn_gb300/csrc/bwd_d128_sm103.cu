@@ -38,6 +38,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <cmath>
 #include <cstdint>
 
@@ -508,6 +509,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int lo = p.causal ? (kpos - q0) : 0;
       const int hi = key_ok ? (p.N - q0) : 0;
       const bool masked = (q0 + BQ > p.N) || !key_ok || (p.causal && q0 == w.k0);
+      // 16 query columns c0 .. c0 + 15 of this thread's key row, packed to bf16
+      // pairs; the mask is applied only on tiles that have masked columns.
+      auto element_chunk = [&](auto mask_tag, const uint32_t(&x)[16], const uint32_t(&y)[16],
+                               int c0, uint32_t(&pk)[8]) {
+        constexpr bool kMask = decltype(mask_tag)::value;
+        const float2 scale = make_float2(sl2, sl2);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 la4 = *reinterpret_cast<const float4 *>(vec + c0 + i);
+          const float4 lb4 = *reinterpret_cast<const float4 *>(vec + BQ + c0 + i);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int k = i + 2 * h;
+            const float2 la = h ? make_float2(la4.z, la4.w) : make_float2(la4.x, la4.y);
+            const float2 lb = h ? make_float2(lb4.z, lb4.w) : make_float2(lb4.x, lb4.y);
+            const float2 sx = make_float2(__uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+            const float2 sy = make_float2(__uint_as_float(y[k]), __uint_as_float(y[k + 1]));
+            float2 r;
+            if (kDV) {
+              // W^T = P1^T - lambda P2^T, each P from its map's log2-sum-exp.
+              const float2 e1 = __ffma2_rn(sx, scale, make_float2(-la.x, -la.y));
+              const float2 e2 = __ffma2_rn(sy, scale, make_float2(-lb.x, -lb.y));
+              r = __ffma2_rn(make_float2(ex2_approx(e2.x), ex2_approx(e2.y)),
+                             make_float2(-lam, -lam),
+                             make_float2(ex2_approx(e1.x), ex2_approx(e1.y)));
+            } else {
+              // dS^T = P^T (c dW^T - c D).
+              const float2 e = __ffma2_rn(sx, scale, make_float2(-la.x, -la.y));
+              const float2 t = __ffma2_rn(sy, make_float2(coef, coef), make_float2(-lb.x, -lb.y));
+              r = __fmul2_rn(make_float2(ex2_approx(e.x), ex2_approx(e.y)), t);
+            }
+            if (kMask) {
+              const int q = c0 + k;
+              r.x = (q >= lo && q < hi) ? r.x : 0.f;
+              r.y = (q + 1 >= lo && q + 1 < hi) ? r.y : 0.f;
+            }
+            pk[k / 2] = pack_bf16x2(r.x, r.y);
+          }
+        }
+      };
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         const int c0 = 64 * ch + 16 * c;  // first query column of the chunk
@@ -516,35 +557,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld16(t_lane + (kDV ? TM_S2 : TM_W) + c0, y);
         tmem_wait16x2(x, y);
         uint32_t pk[8];
-        const float2 scale = make_float2(sl2, sl2);
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const float2 la = make_float2(vec[c0 + i], vec[c0 + i + 1]);
-          const float2 lb = make_float2(vec[BQ + c0 + i], vec[BQ + c0 + i + 1]);
-          const bool va = !masked || (c0 + i >= lo && c0 + i < hi);
-          const bool vb = !masked || (c0 + i + 1 >= lo && c0 + i + 1 < hi);
-          float2 r;
-          if (kDV) {
-            // W^T = P1^T - lambda P2^T, each P from its map's log2-sum-exp.
-            const float2 e1 = __ffma2_rn(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])),
-                                         scale, make_float2(-la.x, -la.y));
-            const float2 e2 = __ffma2_rn(make_float2(__uint_as_float(y[i]), __uint_as_float(y[i + 1])),
-                                         scale, make_float2(-lb.x, -lb.y));
-            r.x = ex2_approx(e1.x) - lam * ex2_approx(e2.x);
-            r.y = ex2_approx(e1.y) - lam * ex2_approx(e2.y);
-          } else {
-            // dS^T = P^T (c dW^T - c D).
-            const float2 e = __ffma2_rn(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])),
-                                        scale, make_float2(-la.x, -la.y));
-            const float2 t = __ffma2_rn(make_float2(__uint_as_float(y[i]), __uint_as_float(y[i + 1])),
-                                        make_float2(coef, coef), make_float2(-lb.x, -lb.y));
-            r.x = ex2_approx(e.x) * t.x;
-            r.y = ex2_approx(e.y) * t.y;
-          }
-          r.x = va ? r.x : 0.f;
-          r.y = vb ? r.y : 0.f;
-          pk[i / 2] = pack_bf16x2(r.x, r.y);
-        }
+        if (masked)
+          element_chunk(std::true_type{}, x, y, c0, pk);
+        else
+          element_chunk(std::false_type{}, x, y, c0, pk);
         // Packed over this thread's own, already read S^T columns.
         tmem_st8(t_lane + TM_S + 64 * ch + 8 * c, pk);
         if (!kDV) {
