@@ -79,8 +79,10 @@ struct Ctrl {
   uint64_t q_empty;   // the tile's queries have been read (dV items: S^T; dK/dQ: dK)
   uint64_t do_full;   // the tile's dO
   uint64_t do_empty;  // the tile's dO has been read (dV items: dV; dK/dQ: dW^T)
-  uint64_t s_full;    // S^T (and dW^T) of the tile
-  uint64_t p_ready;   // the tile's packed operands are published (per thread)
+  uint64_t s_full;    // dK/dQ items: S^T and dW^T of the tile
+  uint64_t p_ready;   // dK/dQ items: the tile's packed operands are published (per thread)
+  uint64_t s_half[2];  // dV items: S1^T and S2^T of the tile's query half h
+  uint64_t p_half[2];  // dV items: query half h's packed W^T is published (per thread)
   uint64_t acc_done;  // the item's dV or dK is complete
   uint64_t dq_full;   // dQ of the tile (dK/dQ items)
   uint64_t dq_free;   // dQ read out of tensor memory (per thread)
@@ -238,6 +240,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(&ctrl->do_empty, 1);
     mbar_init(&ctrl->s_full, 1);
     mbar_init(&ctrl->p_ready, SOFTMAX_THREADS);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&ctrl->s_half[h], 1);
+      mbar_init(&ctrl->p_half[h], SOFTMAX_THREADS / 2);
+    }
     mbar_init(&ctrl->acc_done, 1);
     mbar_init(&ctrl->dq_full, 1);
     mbar_init(&ctrl->dq_free, SOFTMAX_THREADS);
@@ -339,25 +345,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return mbar_wait_warp(bar, parity, abort_flag, WAIT_TIMEOUT_NS);
     };
     constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);
-    // S^T of tile `it` (dV items: S1^T and S2^T), once its queries have landed.
+    // dK/dQ items: S^T of tile `it`, once its queries have landed.
     auto issue_s = [&](int it) {
       if (!wait_all(&ctrl->q_full, it & 1)) return false;
       tc_fence_after_sync();
-      if (kDV) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          umma_bf16_ss_lo_warp(tmem + TM_S, kmaj(V_OFF_K1) + kstep(kk), kmaj(V_OFF_Q1) + kstep(kk),
-                               dhi, ID_S, kk > 0);
-          umma_bf16_ss_lo_warp(tmem + TM_S2, kmaj(V_OFF_K2) + kstep(kk),
-                               kmaj(V_OFF_Q2) + kstep(kk), dhi, ID_S, kk > 0);
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16_ss_lo_warp(tmem + TM_S, kmaj(K_OFF_K) + kstep(kk), kmaj(K_OFF_Q) + kstep(kk),
-                               dhi, ID_S, kk > 0);
-      }
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16_ss_lo_warp(tmem + TM_S, kmaj(K_OFF_K) + kstep(kk), kmaj(K_OFF_Q) + kstep(kk),
+                             dhi, ID_S, kk > 0);
       return true;
+    };
+    // dV items: S1^T and S2^T of query half h (queries 64 h .., N = 64).
+    auto issue_s_half = [&](int h) {
+      constexpr uint32_t ID_S64 = idesc_ab(BK, 64, false, false);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        umma_bf16_ss_lo_warp(tmem + TM_S + 64 * h, kmaj(V_OFF_K1) + kstep(kk),
+                             kmaj(V_OFF_Q1 + 8192 * h) + kstep(kk), dhi, ID_S64, kk > 0);
+        umma_bf16_ss_lo_warp(tmem + TM_S2 + 64 * h, kmaj(V_OFF_K2) + kstep(kk),
+                             kmaj(V_OFF_Q2 + 8192 * h) + kstep(kk), dhi, ID_S64, kk > 0);
+      }
     };
     // dW^T = V dO^T of tile `it` (dK/dQ items), once its dO has landed.
     auto issue_dw = [&](int it) {
@@ -373,8 +380,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after_sync();
     if (ok) {  // the first tile's S^T (and dW^T)
       if (kDV) {
-        if ((ok = issue_s(0))) {
-          umma_commit_warp(&ctrl->s_full);
+        if ((ok = wait_all(&ctrl->q_full, 0))) {
+          tc_fence_after_sync();
+          issue_s_half(0);
+          umma_commit_warp(&ctrl->s_half[0]);
+          issue_s_half(1);
+          umma_commit_warp(&ctrl->s_half[1]);
           umma_commit_warp(&ctrl->q_empty);
         }
       } else if ((ok = issue_dw(0) && issue_s(0))) {
@@ -386,27 +397,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // operands are released as soon as their last product has read them.
     for (int it = 0; ok && it < w.n_q; ++it) {
       const bool more = it + 1 < w.n_q;
-      if (!(ok = wait_all(&ctrl->p_ready, it & 1))) break;
-      tc_fence_after_sync();
       if (kDV) {
-        if (!(ok = wait_all(&ctrl->do_full, it & 1))) break;
-        tc_fence_after_sync();
-        // dV += W^T dO: A packed in TMEM, B = dO read MN-major (N = 256 in four
-        // 64-column blocks); 16 queries = 2048 bytes of each block.
+        // Per query half h: dV += W^T dO over the half's queries, then the next
+        // tile's S1^T and S2^T of that half, over the half's packed W^T (MMAs
+        // run in issue order) while the other half's warps are still busy.
+        // dV: A packed in TMEM, B = dO read MN-major (N = 256 in four 64-column
+        // blocks); 16 queries = 2048 bytes of each block.
         constexpr uint32_t ID_DV = idesc_ab(BK, DV, false, true);
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = wait_all(&ctrl->p_half[h], it & 1))) break;
+          tc_fence_after_sync();
+          if (h == 0) {
+            if (!(ok = wait_all(&ctrl->do_full, it & 1))) break;
+            tc_fence_after_sync();
+          }
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_bf16_ts_lo_warp(tmem + TM_DV, tmem + TM_S + tm_pack(kk),
-                               mnmaj(V_OFF_DO) + ((2048u * kk) >> 4), dhi, ID_DV,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_warp(&ctrl->do_empty);
-        // The next S^T goes over this tile's packed W^T: MMAs run in issue order.
-        if (more) {
-          if (!(ok = issue_s(it + 1))) break;
-          umma_commit_warp(&ctrl->s_full);
-          umma_commit_warp(&ctrl->q_empty);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+            umma_bf16_ts_lo_warp(tmem + TM_DV, tmem + TM_S + tm_pack(kk),
+                                 mnmaj(V_OFF_DO) + ((2048u * kk) >> 4), dhi, ID_DV,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+          if (h == 1) umma_commit_warp(&ctrl->do_empty);
+          if (more) {
+            if (h == 0) {
+              if (!(ok = wait_all(&ctrl->q_full, (it + 1) & 1))) break;
+              tc_fence_after_sync();
+            }
+            issue_s_half(h);
+            umma_commit_warp(&ctrl->s_half[h]);
+            if (h == 1) umma_commit_warp(&ctrl->q_empty);
+          }
         }
+        if (!ok) break;
       } else {
+        if (!(ok = wait_all(&ctrl->p_ready, it & 1))) break;
+        tc_fence_after_sync();
         // dK += dS^T Q: A packed in TMEM, B = Q MN-major (N = 128: two blocks).
         constexpr uint32_t ID_DK = idesc_ab(BK, HD, false, true);
 #pragma unroll
@@ -500,7 +524,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int prev_q0 = 0;
     for (int it = 0; it < w.n_q; ++it) {
       const int q0 = (w.qt_first + it) * BQ;
-      ok = mbar_wait(&ctrl->s_full, it & 1, abort_flag, WAIT_TIMEOUT_NS);
+      ok = mbar_wait(kDV ? &ctrl->s_half[ch] : &ctrl->s_full, it & 1, abort_flag,
+                     WAIT_TIMEOUT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
@@ -575,7 +600,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_st_wait();
       if (!kDV) fence_proxy_async_smem();
       tc_fence_before_sync();
-      mbar_arrive(&ctrl->p_ready);
+      mbar_arrive(kDV ? &ctrl->p_half[ch] : &ctrl->p_ready);
       if (!kDV && it > 0 && !(ok = drain_dq(it - 1, prev_q0))) break;
       prev_q0 = q0;
     }
