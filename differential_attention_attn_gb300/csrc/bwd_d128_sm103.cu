@@ -21,10 +21,11 @@
 // Both recompute P from the saved log2-sum-exp.  Each CTA streams its query
 // tiles through one shared-memory stage (a second would not fit beside the
 // K, V and dO tiles of this width), refilled piecewise as each operand is
-// released: in dK/dQ items dO once dW^T is computed and Q once dK is (the
-// products run dK, dQ, then the next tile's dW^T before its S^T, so the next
-// dO streams in under the softmax and dK / dQ); in dV items Q once S^T is
-// computed and dO once dV is.
+// released: in dK/dQ items dO once dW^T is computed and each 64-query half of
+// Q once that half's dK product is; in dV items Q once S^T is computed and dO
+// once dV is.  Each query half of a tile (the softmax warps of one half) has
+// its own barriers, so one half's products, and the next tile's S^T (and dW^T)
+// of that half, run while the other half is still in its element loop.
 //
 // The saving forward runs the d = 128 forward three times: the output (also
 // writing each map's log2-sum-exp), and map 1's and map 2's normalised outputs
@@ -79,10 +80,10 @@ struct Ctrl {
   uint64_t q_empty;   // the tile's queries have been read (dV items: S^T; dK/dQ: dK)
   uint64_t do_full;   // the tile's dO
   uint64_t do_empty;  // the tile's dO has been read (dV items: dV; dK/dQ: dW^T)
-  uint64_t s_full;    // dK/dQ items: S^T and dW^T of the tile
-  uint64_t p_ready;   // dK/dQ items: the tile's packed operands are published (per thread)
-  uint64_t s_half[2];  // dV items: S1^T and S2^T of the tile's query half h
-  uint64_t p_half[2];  // dV items: query half h's packed W^T is published (per thread)
+  uint64_t q_half_full[2];   // dK/dQ items: query half h of Q and its vectors
+  uint64_t q_half_empty[2];  // dK/dQ items: query half h of Q has been read (dK)
+  uint64_t s_half[2];  // S^T (dK/dQ: and dW^T; dV: S1^T, S2^T) of the tile's query half h
+  uint64_t p_half[2];  // query half h's packed operand is published (per thread)
   uint64_t acc_done;  // the item's dV or dK is complete
   uint64_t dq_full;   // dQ of the tile (dK/dQ items)
   uint64_t dq_free;   // dQ read out of tensor memory (per thread)
@@ -221,7 +222,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                    const __grid_constant__ CUtensorMap tm_q2,
                                    const __grid_constant__ CUtensorMap tm_k2,
                                    const __grid_constant__ CUtensorMap tm_v,
-                                   const __grid_constant__ CUtensorMap tm_do, const Params p) {
+                                   const __grid_constant__ CUtensorMap tm_do,
+                                   const __grid_constant__ CUtensorMap tm_q1h,
+                                   const __grid_constant__ CUtensorMap tm_q2h, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -238,9 +241,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(&ctrl->q_empty, 1);
     mbar_init(&ctrl->do_full, 1);
     mbar_init(&ctrl->do_empty, 1);
-    mbar_init(&ctrl->s_full, 1);
-    mbar_init(&ctrl->p_ready, SOFTMAX_THREADS);
     for (int h = 0; h < 2; ++h) {
+      mbar_init(&ctrl->q_half_full[h], 1);
+      mbar_init(&ctrl->q_half_empty[h], 1);
       mbar_init(&ctrl->s_half[h], 1);
       mbar_init(&ctrl->p_half[h], SOFTMAX_THREADS / 2);
     }
@@ -281,23 +284,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float *lse_a = p.lse + (w.map * p.BH + w.bh) * n_pad;
       const float *lse_b = kDV ? p.lse + (p.BH + w.bh) * n_pad : p.dvec + (w.map * p.BH + w.bh) * n_pad;
       // Per tile: the queries (and vectors), then dO, each after the previous
-      // tile released it; in dK/dQ items dO is released first, so it goes first.
+      // tile released it; in dK/dQ items dO is released first, then each half of
+      // the queries, so they go in that order.
       auto load_q = [&](int it) {
         const int q0 = (w.qt_first + it) * BQ;
         uint8_t *vec = smem + (kDV ? V_OFF_VEC : K_OFF_VEC) + (it % vec_slots<kDV>()) * VEC_BYTES;
-        mbar_arrive_expect_tx(&ctrl->q_full, (kDV ? 4 : 2) * BOX + VEC_BYTES);
-        if (kDV) {
-          for (int x = 0; x < 2; ++x) {
-            tma_load_4d(smem + V_OFF_Q1 + x * BOX, &tm_q1, &ctrl->q_full, 64 * x, q0, w.h, w.b);
-            tma_load_4d(smem + V_OFF_Q2 + x * BOX, &tm_q2, &ctrl->q_full, 64 * x, q0, w.h, w.b);
-          }
-        } else {
-          const CUtensorMap *tq = w.map ? &tm_q2 : &tm_q1;
-          for (int x = 0; x < 2; ++x)
-            tma_load_4d(smem + K_OFF_Q + x * BOX, tq, &ctrl->q_full, 64 * x, q0, w.h, w.b);
+        mbar_arrive_expect_tx(&ctrl->q_full, 4 * BOX + VEC_BYTES);
+        for (int x = 0; x < 2; ++x) {
+          tma_load_4d(smem + V_OFF_Q1 + x * BOX, &tm_q1, &ctrl->q_full, 64 * x, q0, w.h, w.b);
+          tma_load_4d(smem + V_OFF_Q2 + x * BOX, &tm_q2, &ctrl->q_full, 64 * x, q0, w.h, w.b);
         }
         bulk_g2s(vec, lse_a + q0, BQ * 4, &ctrl->q_full);
         bulk_g2s(vec + BQ * 4, lse_b + q0, BQ * 4, &ctrl->q_full);
+      };
+      // dK/dQ items: rows 64 h .. 64 h + 63 of the tile's queries (64-row boxes,
+      // the lower half of each 128-row box) and their vector entries.
+      auto load_q_half = [&](int it, int h) {
+        const int q0 = (w.qt_first + it) * BQ + 64 * h;
+        uint64_t *bar = &ctrl->q_half_full[h];
+        float *vec = reinterpret_cast<float *>(smem + K_OFF_VEC);
+        mbar_arrive_expect_tx(bar, 2 * (BOX / 2) + 2 * 64 * 4);
+        const CUtensorMap *tq = w.map ? &tm_q2h : &tm_q1h;
+        for (int x = 0; x < 2; ++x)
+          tma_load_4d(smem + K_OFF_Q + x * BOX + (BOX / 2) * h, tq, bar, 64 * x, q0, w.h, w.b);
+        bulk_g2s(vec + 64 * h, lse_a + q0, 64 * 4, bar);
+        bulk_g2s(vec + BQ + 64 * h, lse_b + q0, 64 * 4, bar);
       };
       auto load_do = [&](int it) {
         const int q0 = (w.qt_first + it) * BQ;
@@ -306,7 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_4d(smem + (kDV ? V_OFF_DO : K_OFF_DO) + x * BOX, &tm_do, &ctrl->do_full,
                       64 * x, q0, w.h, w.b);
       };
-      uint32_t issued_q = 0, issued_do = 0;
+      uint32_t issued_q = 0, issued_do = 0, issued_qh[2] = {0, 0};
       for (int it = 0; it < w.n_q; ++it) {
         const uint32_t par = static_cast<uint32_t>(it - 1) & 1u;
         if (kDV) {
@@ -320,15 +331,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (it > 0 && !(ok = mbar_wait(&ctrl->do_empty, par, abort_flag, WAIT_TIMEOUT_NS))) break;
           load_do(it);
           issued_do = it + 1;
-          if (it > 0 && !(ok = mbar_wait(&ctrl->q_empty, par, abort_flag, WAIT_TIMEOUT_NS))) break;
-          load_q(it);
-          issued_q = it + 1;
+          for (int h = 0; ok && h < 2; ++h) {
+            if (it > 0 &&
+                !(ok = mbar_wait(&ctrl->q_half_empty[h], par, abort_flag, WAIT_TIMEOUT_NS)))
+              break;
+            load_q_half(it, h);
+            issued_qh[h] = it + 1;
+          }
+          if (!ok) break;
         }
       }
       // Loads still in flight land before the CTA exits.
       drain_wait(&ctrl->kv_full, 0);
       if (issued_q > 0) drain_wait(&ctrl->q_full, (issued_q - 1) & 1);
       if (issued_do > 0) drain_wait(&ctrl->do_full, (issued_do - 1) & 1);
+      for (int h = 0; h < 2; ++h)
+        if (issued_qh[h] > 0) drain_wait(&ctrl->q_half_full[h], (issued_qh[h] - 1) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -344,20 +362,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto wait_all = [&](uint64_t *bar, uint32_t parity) {
       return mbar_wait_warp(bar, parity, abort_flag, WAIT_TIMEOUT_NS);
     };
-    constexpr uint32_t ID_S = idesc_ab(BK, BQ, false, false);
-    // dK/dQ items: S^T of tile `it`, once its queries have landed.
-    auto issue_s = [&](int it) {
-      if (!wait_all(&ctrl->q_full, it & 1)) return false;
-      tc_fence_after_sync();
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16_ss_lo_warp(tmem + TM_S, kmaj(K_OFF_K) + kstep(kk), kmaj(K_OFF_Q) + kstep(kk),
-                             dhi, ID_S, kk > 0);
-      return true;
-    };
-    // dV items: S1^T and S2^T of query half h (queries 64 h .., N = 64).
+    constexpr uint32_t ID_S64 = idesc_ab(BK, 64, false, false);  // N = 64: one query half
+    // dV items: S1^T and S2^T of query half h (queries 64 h ..).
     auto issue_s_half = [&](int h) {
-      constexpr uint32_t ID_S64 = idesc_ab(BK, 64, false, false);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
         umma_bf16_ss_lo_warp(tmem + TM_S + 64 * h, kmaj(V_OFF_K1) + kstep(kk),
@@ -366,14 +373,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              kmaj(V_OFF_Q2 + 8192 * h) + kstep(kk), dhi, ID_S64, kk > 0);
       }
     };
-    // dW^T = V dO^T of tile `it` (dK/dQ items), once its dO has landed.
-    auto issue_dw = [&](int it) {
-      if (!wait_all(&ctrl->do_full, it & 1)) return false;
-      tc_fence_after_sync();
+    // dK/dQ items: S^T = K Q^T and dW^T = V dO^T of query half h.
+    auto issue_sk_half = [&](int h) {
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16_ss_lo_warp(tmem + TM_S + 64 * h, kmaj(K_OFF_K) + kstep(kk),
+                             kmaj(K_OFF_Q + 8192 * h) + kstep(kk), dhi, ID_S64, kk > 0);
+    };
+    auto issue_dw_half = [&](int h) {
 #pragma unroll
       for (int kk = 0; kk < DV / 16; ++kk)
-        umma_bf16_ss_lo_warp(tmem + TM_W, kmaj(K_OFF_V) + kstep(kk), kmaj(K_OFF_DO) + kstep(kk),
-                             dhi, ID_S, kk > 0);
+        umma_bf16_ss_lo_warp(tmem + TM_W + 64 * h, kmaj(K_OFF_V) + kstep(kk),
+                             kmaj(K_OFF_DO + 8192 * h) + kstep(kk), dhi, ID_S64, kk > 0);
+    };
+    // dK/dQ items: the tile's dW^T and S^T of half h (dO for both halves is
+    // already waited for), each half's S^T once that half of the queries landed.
+    auto issue_k_front = [&](int it, int h) {
+      issue_dw_half(h);
+      if (h == 1) umma_commit_warp(&ctrl->do_empty);
+      if (!wait_all(&ctrl->q_half_full[h], it & 1)) return false;
+      tc_fence_after_sync();
+      issue_sk_half(h);
+      umma_commit_warp(&ctrl->s_half[h]);
       return true;
     };
     bool ok = wait_all(&ctrl->kv_full, 0);
@@ -388,21 +409,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_commit_warp(&ctrl->s_half[1]);
           umma_commit_warp(&ctrl->q_empty);
         }
-      } else if ((ok = issue_dw(0) && issue_s(0))) {
-        umma_commit_warp(&ctrl->do_empty);
-        umma_commit_warp(&ctrl->s_full);
+      } else if ((ok = wait_all(&ctrl->do_full, 0))) {
+        tc_fence_after_sync();
+        ok = issue_k_front(0, 0) && issue_k_front(0, 1);
       }
     }
-    // Tile `it`'s products, then the next tile's S^T (and dW^T): the stage's
-    // operands are released as soon as their last product has read them.
+    // Per query half h of tile `it`: the half's products, then the next tile's
+    // S^T (and dW^T) of that half over the half's packed operand (MMAs run in
+    // issue order), while the other half's warps are still busy.
     for (int it = 0; ok && it < w.n_q; ++it) {
       const bool more = it + 1 < w.n_q;
       if (kDV) {
-        // Per query half h: dV += W^T dO over the half's queries, then the next
-        // tile's S1^T and S2^T of that half, over the half's packed W^T (MMAs
-        // run in issue order) while the other half's warps are still busy.
-        // dV: A packed in TMEM, B = dO read MN-major (N = 256 in four 64-column
-        // blocks); 16 queries = 2048 bytes of each block.
+        // dV += W^T dO over the half's queries: A packed in TMEM, B = dO read
+        // MN-major (N = 256 in four 64-column blocks); 16 queries = 2048 bytes
+        // of each block.
         constexpr uint32_t ID_DV = idesc_ab(BK, DV, false, true);
         for (int h = 0; h < 2; ++h) {
           if (!(ok = wait_all(&ctrl->p_half[h], it & 1))) break;
@@ -427,38 +447,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (h == 1) umma_commit_warp(&ctrl->q_empty);
           }
         }
-        if (!ok) break;
       } else {
-        if (!(ok = wait_all(&ctrl->p_ready, it & 1))) break;
-        tc_fence_after_sync();
-        // dK += dS^T Q: A packed in TMEM, B = Q MN-major (N = 128: two blocks).
         constexpr uint32_t ID_DK = idesc_ab(BK, HD, false, true);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_bf16_ts_lo_warp(tmem + TM_DK, tmem + TM_S + tm_pack(kk),
-                               mnmaj(K_OFF_Q) + ((2048u * kk) >> 4), dhi, ID_DK,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_warp(&ctrl->q_empty);
-        // The previous tile's dQ must have been read before this one overwrites it.
-        if (it > 0 && !(ok = wait_all(&ctrl->dq_free, (it - 1) & 1))) break;
-        tc_fence_after_sync();
-        // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major (N = d);
-        // 16 keys = 2048 bytes of each block.
         constexpr uint32_t ID_DQ = idesc_ab(BQ, HD, true, true);
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = wait_all(&ctrl->p_half[h], it & 1))) break;
+          tc_fence_after_sync();
+          // dK += dS^T Q over the half's queries: A packed in TMEM, B = Q
+          // MN-major (N = 128: two blocks); then that half of Q is free.
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_bf16_ss_lo_warp(tmem + TM_DQ, mnmaj(K_OFF_DS) + ((2048u * kk) >> 4),
-                               mnmaj(K_OFF_K) + ((2048u * kk) >> 4), dhi, ID_DQ, kk > 0);
-        umma_commit_warp(&ctrl->dq_full);
-        // The next tile: dW^T (dO arrived under this tile's softmax), then S^T
-        // over this tile's packed dS^T (MMAs run in issue order).
-        if (more) {
-          if (!(ok = issue_dw(it + 1))) break;
-          umma_commit_warp(&ctrl->do_empty);
-          if (!(ok = issue_s(it + 1))) break;
-          umma_commit_warp(&ctrl->s_full);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+            umma_bf16_ts_lo_warp(tmem + TM_DK, tmem + TM_S + tm_pack(kk),
+                                 mnmaj(K_OFF_Q) + ((2048u * kk) >> 4), dhi, ID_DK,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_warp(&ctrl->q_half_empty[h]);
+          if (h == 1) {
+            // dQ = dS K: A = dS^T read MN-major (M = queries), B = K MN-major
+            // (N = d); 16 keys = 2048 bytes of each block.  The previous tile's
+            // dQ must have been read before this one overwrites it.
+            if (it > 0 && !(ok = wait_all(&ctrl->dq_free, (it - 1) & 1))) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16_ss_lo_warp(tmem + TM_DQ, mnmaj(K_OFF_DS) + ((2048u * kk) >> 4),
+                                   mnmaj(K_OFF_K) + ((2048u * kk) >> 4), dhi, ID_DQ, kk > 0);
+            umma_commit_warp(&ctrl->dq_full);
+          }
+          if (more) {
+            if (h == 0) {
+              if (!(ok = wait_all(&ctrl->do_full, (it + 1) & 1))) break;
+              tc_fence_after_sync();
+            }
+            if (!(ok = issue_k_front(it + 1, h))) break;
+          }
         }
       }
+      if (!ok) break;
     }
     if (ok) umma_commit_warp(&ctrl->acc_done);
     umma_commit_warp(&ctrl->drain);
@@ -524,8 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int prev_q0 = 0;
     for (int it = 0; it < w.n_q; ++it) {
       const int q0 = (w.qt_first + it) * BQ;
-      ok = mbar_wait(kDV ? &ctrl->s_half[ch] : &ctrl->s_full, it & 1, abort_flag,
-                     WAIT_TIMEOUT_NS);
+      ok = mbar_wait(&ctrl->s_half[ch], it & 1, abort_flag, WAIT_TIMEOUT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
@@ -574,33 +597,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       };
-#pragma unroll 1
+      uint32_t pks[4][8];  // the half's packed operand, kept for the shared-memory copy
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int c0 = 64 * ch + 16 * c;  // first query column of the chunk
         uint32_t x[16], y[16];
         tmem_ld16(t_lane + TM_S + c0, x);
         tmem_ld16(t_lane + (kDV ? TM_S2 : TM_W) + c0, y);
         tmem_wait16x2(x, y);
-        uint32_t pk[8];
         if (masked)
-          element_chunk(std::true_type{}, x, y, c0, pk);
+          element_chunk(std::true_type{}, x, y, c0, pks[c]);
         else
-          element_chunk(std::false_type{}, x, y, c0, pk);
+          element_chunk(std::false_type{}, x, y, c0, pks[c]);
         // Packed over this thread's own, already read S^T columns.
-        tmem_st8(t_lane + TM_S + 64 * ch + 8 * c, pk);
-        if (!kDV) {
-          // dS^T row in shared memory for dQ: queries c0 .. c0 + 15 of key row kr.
-          uint8_t *sub = smem + K_OFF_DS + (c0 >> 6) * BOX;
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            *reinterpret_cast<uint4 *>(sub + sw128(kr, ((c0 & 63) >> 3) + j)) =
-                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        }
+        tmem_st8(t_lane + TM_S + 64 * ch + 8 * c, pks[c]);
       }
       tmem_st_wait();
-      if (!kDV) fence_proxy_async_smem();
+      if (!kDV) {
+        // dS^T rows in shared memory for dQ (this half's 64 queries of key row
+        // kr), once the previous tile's dQ product has read the buffer: the
+        // first half runs ahead of that product.
+        if (it > 0) {
+          ok = mbar_wait(&ctrl->dq_full, (it - 1) & 1, abort_flag, WAIT_TIMEOUT_NS);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
+        uint8_t *sub = smem + K_OFF_DS + ch * BOX;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<uint4 *>(sub + sw128(kr, 2 * c + j)) =
+                make_uint4(pks[c][4 * j], pks[c][4 * j + 1], pks[c][4 * j + 2], pks[c][4 * j + 3]);
+        fence_proxy_async_smem();
+      }
       tc_fence_before_sync();
-      mbar_arrive(kDV ? &ctrl->p_half[ch] : &ctrl->p_ready);
+      mbar_arrive(&ctrl->p_half[ch]);
       if (!kDV && it > 0 && !(ok = drain_dq(it - 1, prev_q0))) break;
       prev_q0 = q0;
     }
@@ -850,9 +882,9 @@ using EncodeTiledFnD = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32
                                     CUtensorMapFloatOOBfill);
 
 // 4-D view {inner, rows, H, B} of a bf16 tensor with element strides st (rows
-// contiguous); 128-row x 64-column boxes with 128-byte swizzle.
+// contiguous); box_rows x 64-column boxes with 128-byte swizzle.
 CUresult encode_map_d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t n, uint64_t H,
-                      uint64_t B, const diffattn_strides &st) {
+                      uint64_t B, const diffattn_strides &st, uint32_t box_rows) {
   static EncodeTiledFnD fn = [] {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -866,7 +898,7 @@ CUresult encode_map_d(CUtensorMap *map, const void *base, uint64_t inner, uint64
   cuuint64_t dims[4] = {inner, n, H, B};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
                            static_cast<cuuint64_t>(st.b) * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -978,14 +1010,17 @@ diffattn_status launch_bwd_d128_sm103(const diffattn_desc &desc, const void *q1,
   diffattn_bwd_pre_d128_kernel<<<pre_grid, PRE_WARPS * 32, 0, stream>>>(pp);
   if (cudaGetLastError() != cudaSuccess) return DIFFATTN_ERR_CUDA;
 
-  CUtensorMap maps[6];
-  const void *bases[6] = {q1, k1, q2, k2, v, dout};
+  // q1, k1, q2, k2, v, dO in 128-row boxes; q1 and q2 again in 64-row boxes
+  // (the dK/dQ items load each half of a query tile on its own).
+  CUtensorMap maps[8];
+  const void *bases[8] = {q1, k1, q2, k2, v, dout, q1, q2};
   const diffattn_strides dout_st{desc.H * N * DV, N * DV, DV};
-  for (int i = 0; i < 6; ++i) {
-    const uint64_t inner = (i >= 4) ? DV : HD;
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t inner = (i == 4 || i == 5) ? DV : HD;
+    const diffattn_strides &sti = i == 5 ? dout_st : i == 6 ? st[0] : i == 7 ? st[2] : st[i];
     if (encode_map_d(&maps[i], bases[i], inner, static_cast<uint64_t>(N),
-                     static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B),
-                     i == 5 ? dout_st : st[i]) != CUDA_SUCCESS)
+                     static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B), sti,
+                     i >= 6 ? 64u : 128u) != CUDA_SUCCESS)
       return DIFFATTN_ERR_CUDA;
   }
   static std::atomic<bool> attr_set[64];
@@ -1029,11 +1064,11 @@ diffattn_status launch_bwd_d128_sm103(const diffattn_desc &desc, const void *q1,
   p.status = desc.status_dev;
   diffattn_bwd_d128_sm103_kernel<true>
       <<<static_cast<unsigned>(BH * n_qtiles), NUM_THREADS, smem_bytes<true>(), stream>>>(
-          maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+          maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], p);
   if (cudaGetLastError() != cudaSuccess) return DIFFATTN_ERR_CUDA;
   diffattn_bwd_d128_sm103_kernel<false>
       <<<static_cast<unsigned>(2 * BH * n_qtiles), NUM_THREADS, smem_bytes<false>(), stream>>>(
-          maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+          maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], p);
   if (cudaGetLastError() != cudaSuccess) return DIFFATTN_ERR_CUDA;
   int sms = 148;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
