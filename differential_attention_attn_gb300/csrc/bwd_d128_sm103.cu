@@ -27,12 +27,13 @@
 // its own barriers, so one half's products, and the next tile's S^T (and dW^T)
 // of that half, run while the other half is still in its element loop.
 //
-// The saving forward runs the d = 128 forward three times: the output (also
-// writing each map's log2-sum-exp), and map 1's and map 2's normalised outputs
-// alone (lambda taken as 0, no norm; map 2 by swapping the query/key pairs),
-// stored in fp32.  (dlambda = -sum do . o_2 cancels heavily once the head norm
-// has made do nearly orthogonal to o; bf16 map outputs put its error above 2 %
-// of its size on ordinary inputs.)
+// The saving forward runs the d = 128 forward twice: the output (also writing
+// each map's log2-sum-exp and the row's o = o_1 - lambda o_2 before the norm),
+// then map 2's normalised output alone (lambda taken as 0, no norm, the
+// query/key pairs swapped); the preprocess rebuilds o_1 = o + lambda o_2.  Both
+// are stored in fp32: dlambda = -sum do . o_2 cancels heavily once the head
+// norm has made do nearly orthogonal to o, and bf16 map outputs put its error
+// above 2 % of its size on ordinary inputs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -715,7 +716,7 @@ struct PreParams {
   const float *lambda, *norm_w;
   const __nv_bfloat16 *dy;  // [B, H, N, 256] view
   int64_t dy_sb, dy_sh, dy_sn;
-  const float *o_n;          // [2][BH][N][256] normalised map outputs
+  const float *o_n;          // [2][BH][N][256]: o = o_1 - lambda o_2, then o_2
   __nv_bfloat16 *dout;       // [BH][N][256]
   float *dvec;               // [2][BH][n_pad] c_k D_k
   float *dlambda;            // [H], zeroed
@@ -771,10 +772,10 @@ __global__ void __launch_bounds__(PRE_WARPS * 32) diffattn_bwd_pre_d128_kernel(c
       const int64_t row = (bh * p.N + i) * DV + c;
       float dy[8], o1[8], o2[8], o[8], dout[8];
       load8_bf16(dy_bh + i * p.dy_sn + c, dy);
-      load8_f32(p.o_n + row, o1);
+      load8_f32(p.o_n + row, o);
       load8_f32(p.o_n + plane + row, o2);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] = o1[j] - lam * o2[j];
+      for (int j = 0; j < 8; ++j) o1[j] = fmaf(lam, o2[j], o[j]);
       if (p.headnorm) {
         if (p.headnorm == 2) {
           float sm = 0.f;
@@ -930,13 +931,13 @@ diffattn_status launch_fwd_train_d128(const diffattn_desc &desc, const void *q1,
   float *o1 = reinterpret_cast<float *>(sv);
   float *o2 = o1 + BH * N * DV;
   float *lse = reinterpret_cast<float *>(sv + r256(2 * BH * N * DV * 4));
-  // The output, and each map's log2-sum-exp.
+  // The output, each map's log2-sum-exp and the pre-norm o = o_1 - lambda o_2.
   diffattn_status st = launch_fwd_d128_sm103(desc, N, q1, k1, q2, k2, v, lambda, norm_w, out,
-                                             stream, strides, lse);
+                                             stream, strides, lse, nullptr, o1);
   if (st != DIFFATTN_OK) return st;
-  // Map 1's and map 2's normalised outputs alone: lambda taken as 0, no norm,
-  // fp32 into the saved buffer; map 2 with the query/key pairs swapped.  (`out`
-  // is passed for its strides only: nothing is written to it.)
+  // Map 2's normalised output alone: lambda taken as 0, no norm, the query/key
+  // pairs swapped, fp32 into the saved buffer.  (`out` is passed for its
+  // strides only: nothing is written to it.)
   diffattn_desc raw = desc;
   raw.headnorm = 0;
   const diffattn_strides cont64{desc.H * N * HD, N * HD, HD}, cont256{desc.H * N * DV, N * DV, DV};
@@ -948,9 +949,6 @@ diffattn_status launch_fwd_train_d128(const diffattn_desc &desc, const void *q1,
   s2[3] = s1[1];
   s2[4] = s1[4];
   s2[5] = s1[5];
-  st = launch_fwd_d128_sm103(raw, N, q1, k1, q2, k2, v, lambda, nullptr, out, stream, s1, nullptr,
-                             o1);
-  if (st != DIFFATTN_OK) return st;
   return launch_fwd_d128_sm103(raw, N, q2, k2, q1, k1, v, lambda, nullptr, out, stream, s2,
                                nullptr, o2);
 }

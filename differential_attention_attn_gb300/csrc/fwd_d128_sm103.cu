@@ -106,6 +106,9 @@ struct Params {
   // is written there in fp32 (contiguous [BH][N][256]).
   float *save_lse;
   float *map_out;
+  // Training: the row's o = o_1 - lambda o_2 before the norm, fp32
+  // (contiguous [BH][N][256]), when non-null.
+  float *o_save;
 };
 
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -497,6 +500,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             continue;
           }
+          if (kTrain && p.o_save != nullptr) {  // uniform: this thread's row, pre-norm
+            if (q0 + r < p.N &&
+                dbg_ok(q0 + r >= 0 && 128 * g + c64 + c32 + 32 <= DV, p.status, 52)) {
+              float4 *dst = reinterpret_cast<float4 *>(
+                  p.o_save + (bh * p.N + q0 + r) * static_cast<int64_t>(DV) + 128 * g + c64 +
+                  c32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 &pk = pkt[c32 / 8 + q];
@@ -564,7 +579,7 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, c
                                       const void *v, const float *lambda, const float *norm_w,
                                       void *out, cudaStream_t stream,
                                       const diffattn_strides *strides, float *save_lse,
-                                      float *map_out) {
+                                      float *map_out, float *o_save) {
   const int64_t BH = desc.B * desc.H, N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
   const int64_t n_ktiles = (n_kv + BN - 1) / BN;
@@ -625,8 +640,9 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.out_sn = st[5].n;
   p.save_lse = save_lse;
   p.map_out = map_out;
+  p.o_save = o_save;
   dim3 grid(static_cast<unsigned>(BH * n_qtiles));
-  if (save_lse != nullptr || map_out != nullptr)
+  if (save_lse != nullptr || map_out != nullptr || o_save != nullptr)
     diffattn_fwd_d128_sm103_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else

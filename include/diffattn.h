@@ -274,8 +274,8 @@ diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, in
  * Domain: DIFFATTN_BF16, d == 64 or d == 128, square attention (N queries =
  * N keys), causal or not, headnorm 0, 1 or 2 (the group form: the page's
  * GroupNorm); an sm_103 device.  d == 128 runs its own kernels: the saving
- * forward is the d == 128 forward three times (the output with each map's
- * log2-sum-exp, then each map's output alone), and the backward two kinds of
+ * forward is the d == 128 forward twice (the output with each map's
+ * log2-sum-exp and the pre-norm o, then map 2's output alone), and the backward two kinds of
  * work item (one computing dV from both maps, one computing one map's dK and
  * dQ), since the d == 64 kernel's tensor-memory layout does not fit 2d = 256.
  */
@@ -289,7 +289,8 @@ diffattn_status diffattn_train_sizes(const diffattn_desc *desc, size_t *saved_by
  * diffattn_fwd_train — diffattn_fwd (same arguments, same `out`, bitwise)
  * that also writes `saved` (caller-owned device buffer of at least
  * saved_bytes from diffattn_train_sizes, 16-byte aligned): each map's
- * normalised output o_k (fp32 [2][B*H][N][2d]) and log2-sum-exp
+ * normalised output o_k (fp32 [2][B*H][N][2d]; for d == 128 the first holds
+ * o = o_1 - lambda o_2 before the norm instead of o_1) and log2-sum-exp
  * (fp32 [2][B*H][128 * ceil(N / 128)]; for d == 128 each region starts on a
  * 256-byte boundary).  Keep it unchanged until the matching diffattn_bwd has
  * run.
