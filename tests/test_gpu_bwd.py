@@ -195,11 +195,18 @@ def test_train_strided_matches_contiguous(causal, headnorm, N, d):
          names)
 
 
-@pytest.mark.parametrize("N,causal,headnorm", [(128, True, 1), (200, True, 1), (256, False, 2),
-                                               (384, True, 0), (130, False, 1)])
+@pytest.mark.parametrize("N,causal,headnorm", [(2, True, 1), (7, False, 2), (128, True, 1),
+                                               (200, True, 1), (256, False, 2), (384, True, 0),
+                                               (130, False, 1)])
 def test_bwd_d128(N, causal, headnorm):
     """d = 128 (values 256 wide): the saving forward's output equals the plain
-    forward's bitwise, and every gradient is within the oracle tolerance."""
+    forward's bitwise, and every gradient is within the oracle tolerance.
+
+    N = 2 rather than 1: with one key every dq and dk is exactly zero (dS = dW - D
+    cancels), and the d = 128 path rebuilds o_1 = o + lambda o_2 from the forward's
+    bf16-weighted accumulator, so they come out at rounding level (about 1e-5) with no
+    scale for a relative bound; at N = 2 row 0 is that degenerate row and row 1 gives
+    the tensor its scale.  N = 1 runs in the bounds-checked build."""
     w = W.custom(1100 + N, B=2, H=2, N=N, d=128, causal=causal, headnorm=headnorm,
                  random_w=True, layer=5)
     dy = _dy(w, N + 3)
@@ -217,3 +224,18 @@ def test_bwd_d128_many_items():
     dy = _dy(w, 1200)
     _, g = _run(w, dy)
     _cmp(g, _oracle(w, dy), "d=128 B3H4N1100")
+
+
+@pytest.mark.parametrize("lam,headnorm", [(0.0, 1), (-0.5, 1), (0.8, 2), (1.0, 0), (-0.5, 0)])
+def test_bwd_d128_lambda_and_norm(lam, headnorm):
+    """d = 128 with lambda at 0, negative, and 1 (without the norm, as at d = 64: with it a
+    row whose maps agree has o = 0 and the norm amplifies P's rounding without bound)."""
+    w = W.custom(19, B=1, H=3, N=320, d=128, causal=True, headnorm=headnorm, random_w=True,
+                 layer=3)
+    w.lam_offset = np.full(w.H, lam)
+    dy = _dy(w, 6)
+    _, g = _run(w, dy)
+    names = GRADS if headnorm else GRADS[:-1]
+    _cmp(g, _oracle(w, dy), f"d=128 lambda={lam} headnorm={headnorm}", names)
+    if not headnorm:
+        assert float(g["dw"].abs().max()) == 0.0
