@@ -194,14 +194,6 @@ __device__ __forceinline__ void tmem_wait16x4(uint32_t (&a)[16], uint32_t (&b)[1
                     "+r"(d[8]), "+r"(d[9]), "+r"(d[10]), "+r"(d[11]), "+r"(d[12]), "+r"(d[13]),
                     "+r"(d[14]), "+r"(d[15]) : : "memory");
 }
-__device__ __forceinline__ void tmem_wait16(uint32_t (&a)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
-                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
-                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
-               :
-               : "memory");
-}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
