@@ -27,11 +27,11 @@
 // its own barriers, so one half's products, and the next tile's S^T (and dW^T)
 // of that half, run while the other half is still in its element loop.
 //
-// The saving forward runs the d = 128 forward twice: the output (also writing
-// each map's log2-sum-exp and the row's o = o_1 - lambda o_2 before the norm),
-// then map 2's normalised output alone (lambda taken as 0, no norm, the
-// query/key pairs swapped); the preprocess rebuilds o_1 = o + lambda o_2.  Both
-// are stored in fp32: dlambda = -sum do . o_2 cancels heavily once the head
+// The saving forward runs the d = 128 forward (the output, also writing each
+// map's log2-sum-exp and the row's o = o_1 - lambda o_2 before the norm), then
+// map 2's output alone from its saved log2-sum-exp in one pass over the keys
+// (diffattn_map_out_d128_kernel); the preprocess rebuilds o_1 = o + lambda o_2.
+// Both are stored in fp32: dlambda = -sum do . o_2 cancels heavily once the head
 // norm has made do nearly orthogonal to o, and bf16 map outputs put its error
 // above 2 % of its size on ordinary inputs.
 #include <cuda.h>
@@ -906,6 +906,258 @@ CUresult encode_map_d(CUtensorMap *map, const void *base, uint64_t inner, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+
+// ---------------------------------------------------------------- map output from saved statistics
+// o_k = map_k V of one map given its log2-sum-exp (the saving forward's second
+// pass): o_k[q] = sum_j 2^(S[q, j] log2e / sqrt(d) - lse[q]) v_j.  One CTA per
+// (128-query tile, head), heaviest tile first; queries on the TMEM lanes, S
+// double-buffered (columns 0-255) so that the element work on key tile j
+// overlaps S of tile j + 1 and P V of tile j - 1, O in columns 256-511; K and
+// V double-buffered in shared memory.  Warps: producer, MMA issuer, 2 idle, 8
+// element warps (warp 4 + 4 ch + q: lane quarter q, keys 64 ch .. of a tile).
+// K is released once S has read it and V once P V has, so K of tile j + 2
+// streams in while tile j's P V waits for its softmax.
+constexpr uint32_t M_OFF_Q = 0, M_OFF_K = 2 * BOX, M_OFF_V = 6 * BOX, M_OFF_VEC = 14 * BOX;
+constexpr uint32_t M_OFF_CTRL = M_OFF_VEC + BQ * 4;
+constexpr uint32_t TM_O = 256;
+
+struct MapCtrl {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];  // K of a key tile: released once S has read it
+  uint64_t v_full[2], v_empty[2];  // V of a key tile: released once P V has read it
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr uint32_t MAP_SMEM_BYTES = M_OFF_CTRL + static_cast<uint32_t>(sizeof(MapCtrl)) + 1024;
+static_assert(MAP_SMEM_BYTES <= 232448, "shared memory budget exceeded");
+
+struct MapParams {
+  int64_t BH;
+  int32_t H, N, n_qtiles, causal;
+  float scale_log2;
+  const float *lse;  // [BH][n_pad] this map's log2-sum-exp
+  float *out;        // [BH][N][256] fp32
+  int32_t *status;
+};
+
+__global__ void __launch_bounds__(384, 1)
+    diffattn_map_out_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                 const __grid_constant__ CUtensorMap tm_k,
+                                 const __grid_constant__ CUtensorMap tm_v, const MapParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  MapCtrl *ctrl = reinterpret_cast<MapCtrl *>(smem + M_OFF_CTRL);
+  volatile int *abort_flag = &ctrl->abort;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t n_bh = static_cast<uint32_t>(p.BH);
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x / n_bh);
+  const uint32_t bh32 = blockIdx.x % n_bh;
+  const int64_t bh = bh32;
+  const int hh = static_cast<int>(bh32 % static_cast<uint32_t>(p.H));
+  const int bb = static_cast<int>(bh32 / static_cast<uint32_t>(p.H));
+  const int q0 = qt * BQ;
+  const int n_kv = p.causal ? qt + 1 : p.n_qtiles;  // key tiles of 128 keys
+  const int64_t n_pad = static_cast<int64_t>(p.n_qtiles) * BQ;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctrl->k_full[s], 1);
+      mbar_init(&ctrl->k_empty[s], 1);
+      mbar_init(&ctrl->v_full[s], 1);
+      mbar_init(&ctrl->v_empty[s], 1);
+      mbar_init(&ctrl->s_full[s], 1);
+      mbar_init(&ctrl->p_ready[s], SOFTMAX_THREADS);
+    }
+    mbar_init(&ctrl->o_done, 1);
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int loaded = 0;  // key tiles whose loads were issued
+      mbar_arrive_expect_tx(&ctrl->q_full, 2 * BOX + BQ * 4);
+      for (int x = 0; x < 2; ++x)
+        tma_load_4d(smem + M_OFF_Q + x * BOX, &tm_q, &ctrl->q_full, 64 * x, q0, hh, bb);
+      bulk_g2s(smem + M_OFF_VEC, p.lse + bh * n_pad + q0, BQ * 4, &ctrl->q_full);
+      int loaded_v = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j & 1;
+        const uint32_t par = static_cast<uint32_t>((j >> 1) - 1) & 1u;
+        if (j >= 2 && !mbar_wait(&ctrl->k_empty[s], par, abort_flag, WAIT_TIMEOUT_NS)) break;
+        mbar_arrive_expect_tx(&ctrl->k_full[s], 2 * BOX);
+        for (int x = 0; x < 2; ++x)
+          tma_load_4d(smem + M_OFF_K + (2 * s + x) * BOX, &tm_k, &ctrl->k_full[s], 64 * x,
+                      j * BK, hh, bb);
+        loaded = j + 1;
+        if (j >= 2 && !mbar_wait(&ctrl->v_empty[s], par, abort_flag, WAIT_TIMEOUT_NS)) break;
+        mbar_arrive_expect_tx(&ctrl->v_full[s], 4 * BOX);
+        for (int x = 0; x < 4; ++x)
+          tma_load_4d(smem + M_OFF_V + (4 * s + x) * BOX, &tm_v, &ctrl->v_full[s], 64 * x,
+                      j * BK, hh, bb);
+        loaded_v = j + 1;
+      }
+      // Loads still in flight land before the CTA exits: the last tile issued
+      // into each buffer (tile t completes phase t >> 1 of buffer t & 1).
+      drain_wait(&ctrl->q_full, 0);
+      for (int t = loaded - 2; t < loaded; ++t)
+        if (t >= 0) drain_wait(&ctrl->k_full[t & 1], (t >> 1) & 1);
+      for (int t = loaded_v - 2; t < loaded_v; ++t)
+        if (t >= 0) drain_wait(&ctrl->v_full[t & 1], (t >> 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
+    const uint32_t base = smem_u32(smem);
+    const uint32_t dhi = static_cast<uint32_t>(smem_desc_sw128(base, 16, 1024) >> 32);
+    auto kmaj = [&](uint32_t off) { return lo(smem_desc_sw128(base + off, 16, 1024)); };
+    auto mnmaj = [&](uint32_t off) { return lo(smem_desc_sw128(base + off, BOX, 1024)); };
+    auto kstep = [](int kk) { return static_cast<uint32_t>((kk >> 2) * BOX + 32 * (kk & 3)) >> 4; };
+    auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+      return mbar_wait_warp(bar, parity, abort_flag, WAIT_TIMEOUT_NS);
+    };
+    constexpr uint32_t ID_S = idesc_ab(BQ, BK, false, false);   // S = Q K^T, both K-major
+    constexpr uint32_t ID_PV = idesc_ab(BQ, DV, false, true);   // O += P V, V MN-major
+    // S of key tile j into buffer j & 1, once K_j has landed.
+    auto issue_s = [&](int j) {
+      const int s = j & 1;
+      if (!wait_all(&ctrl->k_full[s], (j >> 1) & 1)) return false;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16_ss_lo_warp(tmem + 128 * s, kmaj(M_OFF_Q) + kstep(kk),
+                             kmaj(M_OFF_K + 2 * s * BOX) + kstep(kk), dhi, ID_S, kk > 0);
+      umma_commit_warp(&ctrl->k_empty[s]);
+      umma_commit_warp(&ctrl->s_full[s]);
+      return true;
+    };
+    bool ok = wait_all(&ctrl->q_full, 0);
+    tc_fence_after_sync();
+    if (ok) ok = issue_s(0);
+    if (ok && n_kv > 1) ok = issue_s(1);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j & 1;
+      if (!(ok = wait_all(&ctrl->p_ready[s], (j >> 1) & 1))) break;
+      if (!(ok = wait_all(&ctrl->v_full[s], (j >> 1) & 1))) break;
+      tc_fence_after_sync();
+      // O += P V: A = packed P in TMEM over buffer s, B = V_j MN-major (N = 256
+      // in four 64-column blocks); 16 keys = 2048 bytes of each block.
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        umma_bf16_ts_lo_warp(tmem + TM_O, tmem + 128 * s + tm_pack(kk),
+                             mnmaj(M_OFF_V + 4 * s * BOX) + ((2048u * kk) >> 4), dhi, ID_PV,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(&ctrl->v_empty[s]);
+      // S of tile j + 2 goes over this tile's packed P: MMAs run in issue order.
+      if (j + 2 < n_kv && !(ok = issue_s(j + 2))) break;
+    }
+    if (ok) umma_commit_warp(&ctrl->o_done);
+    umma_commit_warp(&ctrl->drain);
+    drain_wait(&ctrl->drain, 0);
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- element warps
+    const int sw = warp - 4;
+    const int quarter = warp & 3, ch = sw >> 2;
+    const int r = quarter * 32 + lane;  // query row in the tile = TMEM lane
+    const int qpos = q0 + r;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag, WAIT_TIMEOUT_NS);
+    ok = __all_sync(0xffffffffu, ok);
+    const float neg_lse = ok ? -reinterpret_cast<const float *>(smem + M_OFF_VEC)[r] : 0.f;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j & 1;
+      ok = mbar_wait(&ctrl->s_full[s], (j >> 1) & 1, abort_flag, WAIT_TIMEOUT_NS);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int k0 = j * BK;
+      // Key column c of the tile (key k0 + c) is visible iff c < hi.
+      const int hi = min(p.N - k0, p.causal ? qpos - k0 + 1 : BK);
+      const bool masked = (k0 + BK > p.N) || (p.causal && j == qt);
+      const float2 scale = make_float2(sl2, sl2), nl2 = make_float2(neg_lse, neg_lse);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int c0 = 64 * ch + 16 * c;
+        uint32_t x[16];
+        tmem_ld16(t_lane + 128 * s + c0, x);
+        tmem_wait16x2(x, x);
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const float2 e = __ffma2_rn(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])),
+                                      scale, nl2);
+          float pa = ex2_approx(e.x), pb = ex2_approx(e.y);
+          if (masked) {
+            pa = (c0 + i < hi) ? pa : 0.f;
+            pb = (c0 + i + 1 < hi) ? pb : 0.f;
+          }
+          pk[i / 2] = pack_bf16x2(pa, pb);
+        }
+        // Packed over this thread's own, already read S columns.
+        tmem_st8(t_lane + 128 * s + 64 * ch + 8 * c, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->p_ready[s]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok) ok = mbar_wait(&ctrl->o_done, 0, abort_flag, WAIT_TIMEOUT_NS);
+    ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);
+    if (ok) {
+      tc_fence_after_sync();
+      // This thread's query row, value columns 128 ch .. 128 ch + 127, stored
+      // transposed across 8-lane groups (four 128-byte row segments per store).
+      const int row0 = q0 + quarter * 32 + (lane & ~7);
+      float *col_base = p.out + bh * static_cast<int64_t>(p.N) * DV + 128 * ch + 4 * (lane & 7);
+#pragma unroll 1
+      for (int c32 = 0; c32 < 128; c32 += 32) {
+        uint32_t v[32];
+        tmem_ld_x32_nowait(t_lane + TM_O + 128 * ch + c32, v);
+        tmem_ld_wait_x32(v);
+        uint4 c8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c8[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        transpose8_chunks(c8, lane);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          if (row0 + jj < p.N &&
+              dbg_ok(row0 + jj >= 0 && 128 * ch + c32 + 4 * (lane & 7) + 4 <= DV, p.status, 84))
+            *reinterpret_cast<uint4 *>(col_base + static_cast<int64_t>(row0 + jj) * DV + c32) =
+                c8[jj];
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag && p.status != nullptr)
+    atomicExch(p.status, static_cast<int32_t>(DIFFATTN_ERR_TIMEOUT));
+}
+
 int64_t r256(int64_t bytes) { return (bytes + 255) / 256 * 256; }
 
 }  // namespace
@@ -933,24 +1185,45 @@ diffattn_status launch_fwd_train_d128(const diffattn_desc &desc, const void *q1,
   float *lse = reinterpret_cast<float *>(sv + r256(2 * BH * N * DV * 4));
   // The output, each map's log2-sum-exp and the pre-norm o = o_1 - lambda o_2.
   diffattn_status st = launch_fwd_d128_sm103(desc, N, q1, k1, q2, k2, v, lambda, norm_w, out,
-                                             stream, strides, lse, nullptr, o1);
+                                             stream, strides, lse, o1);
   if (st != DIFFATTN_OK) return st;
-  // Map 2's normalised output alone: lambda taken as 0, no norm, the query/key
-  // pairs swapped, fp32 into the saved buffer.  (`out` is passed for its
-  // strides only: nothing is written to it.)
-  diffattn_desc raw = desc;
-  raw.headnorm = 0;
+  // Map 2's output alone, from its saved log2-sum-exp: one pass over the keys.
+  const int64_t n_qtiles = (N + BQ - 1) / BQ;
+  if (BH * n_qtiles > INT32_MAX || desc.H > INT32_MAX) return DIFFATTN_ERR_UNSUPPORTED;
   const diffattn_strides cont64{desc.H * N * HD, N * HD, HD}, cont256{desc.H * N * DV, N * DV, DV};
-  diffattn_strides s1[6], s2[6];
-  for (int i = 0; i < 6; ++i) s1[i] = strides ? strides[i] : (i >= 4 ? cont256 : cont64);
-  s2[0] = s1[2];
-  s2[1] = s1[3];
-  s2[2] = s1[0];
-  s2[3] = s1[1];
-  s2[4] = s1[4];
-  s2[5] = s1[5];
-  return launch_fwd_d128_sm103(raw, N, q2, k2, q1, k1, v, lambda, nullptr, out, stream, s2,
-                               nullptr, o2);
+  CUtensorMap maps[3];
+  const void *bases[3] = {q2, k2, v};
+  for (int i = 0; i < 3; ++i) {
+    const diffattn_strides sti = strides ? strides[i == 2 ? 4 : 2 + i] : (i == 2 ? cont256 : cont64);
+    if (encode_map_d(&maps[i], bases[i], i == 2 ? DV : HD, static_cast<uint64_t>(N),
+                     static_cast<uint64_t>(desc.H), static_cast<uint64_t>(desc.B), sti, 128u) !=
+        CUDA_SUCCESS)
+      return DIFFATTN_ERR_CUDA;
+  }
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return DIFFATTN_ERR_UNSUPPORTED;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(diffattn_map_out_d128_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(MAP_SMEM_BYTES)) != cudaSuccess)
+      return DIFFATTN_ERR_CUDA;
+    attr_set[dev].store(true, std::memory_order_release);
+  }
+  MapParams mp;
+  mp.BH = BH;
+  mp.H = static_cast<int32_t>(desc.H);
+  mp.N = static_cast<int32_t>(N);
+  mp.n_qtiles = static_cast<int32_t>(n_qtiles);
+  mp.causal = desc.causal ? 1 : 0;
+  mp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
+  mp.lse = lse + BH * n_qtiles * BQ;  // map 2's rows
+  mp.out = o2;
+  mp.status = desc.status_dev;
+  diffattn_map_out_d128_kernel<<<static_cast<unsigned>(BH * n_qtiles), 384, MAP_SMEM_BYTES,
+                                 stream>>>(maps[0], maps[1], maps[2], mp);
+  return cudaGetLastError() == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 
 diffattn_status launch_bwd_d128_sm103(const diffattn_desc &desc, const void *q1, const void *k1,

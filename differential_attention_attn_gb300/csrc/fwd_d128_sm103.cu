@@ -101,11 +101,8 @@ struct Params {
   int32_t *status;
   int64_t out_sb, out_sh, out_sn;  // element strides of `out` (rows of 256 contiguous)
   // Training: each map's log2-sum-exp m_k + log2 l_k per row (fp32
-  // [2][BH][128 * n_qtiles]) when non-null.  When map_out is non-null, lambda
-  // is taken as 0 and, instead of `out`, map 1's normalised output o_1 alone
-  // is written there in fp32 (contiguous [BH][N][256]).
+  // [2][BH][128 * n_qtiles]) when non-null.
   float *save_lse;
-  float *map_out;
   // Training: the row's o = o_1 - lambda o_2 before the norm, fp32
   // (contiguous [BH][N][256]), when non-null.
   float *o_save;
@@ -120,7 +117,7 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
-// kTrain: the saving forward's instantiation (save_lse, map_out); the plain
+// kTrain: the saving forward's instantiation (save_lse, o_save); the plain
 // forward's has neither path.
 template <bool kTrain>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -381,7 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           named_barrier_sync(1, 256);
           m1 = ctrl->xch[0][r];
           m2 = ctrl->xch[1][r];
-          c2 = (kTrain && p.map_out != nullptr) ? 0.f : p.lambda[h];
+          c2 = p.lambda[h];
         }
       } else {
         // Keys 64g .. 64g+63 of both maps in two 32-key chunks:
@@ -488,18 +485,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] = (__uint_as_float(v[c]) - mu) * rr;
           }
-          if (kTrain && p.map_out != nullptr) {  // uniform: this thread's row, 32 fp32 columns
-            if (q0 + r < p.N &&
-                dbg_ok(q0 + r >= 0 && 128 * g + c64 + c32 + 32 <= DV, p.status, 51)) {
-              float4 *dst = reinterpret_cast<float4 *>(
-                  p.map_out + (bh * p.N + q0 + r) * static_cast<int64_t>(DV) + 128 * g + c64 +
-                  c32);
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
-            }
-            continue;
-          }
           if (kTrain && p.o_save != nullptr) {  // uniform: this thread's row, pre-norm
             if (q0 + r < p.N &&
                 dbg_ok(q0 + r >= 0 && 128 * g + c64 + c32 + 32 <= DV, p.status, 52)) {
@@ -521,7 +506,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             pk.w = pack_bf16x2(y[8 * q + 6], y[8 * q + 7]);
           }
         }
-        if (kTrain && p.map_out != nullptr) continue;  // uniform
         transpose8_chunks(pkt, lane);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -579,7 +563,7 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, c
                                       const void *v, const float *lambda, const float *norm_w,
                                       void *out, cudaStream_t stream,
                                       const diffattn_strides *strides, float *save_lse,
-                                      float *map_out, float *o_save) {
+                                      float *o_save) {
   const int64_t BH = desc.B * desc.H, N = desc.N;
   const int64_t n_qtiles = (N + BM - 1) / BM;
   const int64_t n_ktiles = (n_kv + BN - 1) / BN;
@@ -639,10 +623,9 @@ diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, c
   p.out_sh = st[5].h;
   p.out_sn = st[5].n;
   p.save_lse = save_lse;
-  p.map_out = map_out;
   p.o_save = o_save;
   dim3 grid(static_cast<unsigned>(BH * n_qtiles));
-  if (save_lse != nullptr || map_out != nullptr || o_save != nullptr)
+  if (save_lse != nullptr || o_save != nullptr)
     diffattn_fwd_d128_sm103_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], p);
   else

@@ -85,17 +85,14 @@ int auto_splits(int64_t BH, int64_t N, int64_t n_kv, bool causal, int sm_count);
 // keys (causal: the queries are the last N positions); [B, H, rows, width]
 // with the element strides of q1, k1, q2, k2, v, out given (rows contiguous),
 // or contiguous when strides is null.  Training: save_lse (fp32
-// [2][BH][128 * n_qtiles]) receives each map's log2-sum-exp; with map_out
-// non-null, lambda is taken as 0 and map 1's normalised output is written there
-// in fp32 ([BH][N][256]) instead of `out`; o_save (fp32 [BH][N][256]) receives
-// each row's o = o_1 - lambda o_2 before the norm.
+// [2][BH][128 * n_qtiles]) receives each map's log2-sum-exp; o_save (fp32
+// [BH][N][256]) each row's o = o_1 - lambda o_2 before the norm.
 diffattn_status launch_fwd_d128_sm103(const diffattn_desc &desc, int64_t n_kv, const void *q1,
                                       const void *k1, const void *q2, const void *k2,
                                       const void *v, const float *lambda, const float *norm_w,
                                       void *out, cudaStream_t stream,
                                       const diffattn_strides *strides = nullptr,
-                                      float *save_lse = nullptr, float *map_out = nullptr,
-                                      float *o_save = nullptr);
+                                      float *save_lse = nullptr, float *o_save = nullptr);
 
 // Backward pass for d = 128 (bwd_d128_sm103.cu): saved-activation and workspace
 // sizes in bytes, and the launch of its kernels (preprocess, the dV items, the

@@ -274,8 +274,9 @@ diffattn_status diffattn_fwd_kv_plan(const diffattn_desc *desc, int64_t n_kv, in
  * Domain: DIFFATTN_BF16, d == 64 or d == 128, square attention (N queries =
  * N keys), causal or not, headnorm 0, 1 or 2 (the group form: the page's
  * GroupNorm); an sm_103 device.  d == 128 runs its own kernels: the saving
- * forward is the d == 128 forward twice (the output with each map's
- * log2-sum-exp and the pre-norm o, then map 2's output alone), and the backward two kinds of
+ * forward is the d == 128 forward (the output with each map's log2-sum-exp
+ * and the pre-norm o) and then one pass over the keys for map 2's output from
+ * its saved statistics, and the backward two kinds of
  * work item (one computing dV from both maps, one computing one map's dK and
  * dQ), since the d == 64 kernel's tensor-memory layout does not fit 2d = 256.
  */
