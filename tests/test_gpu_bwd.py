@@ -239,3 +239,42 @@ def test_bwd_d128_lambda_and_norm(lam, headnorm):
     _cmp(g, _oracle(w, dy), f"d=128 lambda={lam} headnorm={headnorm}", names)
     if not headnorm:
         assert float(g["dw"].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("N,causal", [(200, True), (130, False)])
+def test_saved_d128_matches_oracle(N, causal):
+    """The d = 128 saved activations themselves: the pre-norm o = o_1 - lambda o_2 (the
+    oracle's forward without the norm), o_2 (its forward with lambda = 0 and the query/key
+    pairs swapped) and each map's log2-sum-exp, log2 sum_j 2^(q.k_j log2e / sqrt(d)) over
+    the visible keys, written out in float64 here."""
+    w = W.custom(1300 + N, B=2, H=2, N=N, d=128, causal=causal, headnorm=1, random_w=True,
+                 layer=4)
+    li = harness.lambda_init_for(w, "gpu")
+    lam_np = np.asarray(w.lambdas(li), dtype=np.float32)
+    lam = torch.tensor(lam_np, device="cuda")
+    nw = torch.tensor(w.w, dtype=torch.float32, device="cuda")
+    dev = [t.cuda() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    _, saved = ops.fwd_train(*dev, lam, causal=causal, headnorm=1, norm_w=nw,
+                             eps=float(np.float32(w.eps)), lambda_init=li)
+    torch.cuda.synchronize()
+    B, H, d, BH = w.B, w.H, w.d, w.B * w.H
+    n_pad = -(-N // 128) * 128
+    f = saved.view(torch.float32).cpu().numpy().astype(np.float64)
+    o_all = f[:2 * BH * N * 2 * d].reshape(2, B, H, N, 2 * d)
+    off = (2 * BH * N * 2 * d * 4 + 255) // 256 * 256 // 4
+    lse = f[off:off + 2 * BH * n_pad].reshape(2, B, H, n_pad)[..., :N]
+    q1, k1, q2, k2, v = (t.double().numpy() for t in (w.q1, w.k1, w.q2, w.k2, w.v))
+    o_ref = oracle.fwd(q1, k1, q2, k2, v, lam_np.astype(np.float64), causal=causal,
+                       headnorm=False)
+    o2_ref = oracle.fwd(q2, k2, q1, k1, v, np.zeros(H), causal=causal, headnorm=False)
+    for got, ref, name in ((o_all[0], o_ref, "o"), (o_all[1], o2_ref, "o2")):
+        err = float(np.max(np.abs(got - ref)))
+        assert err <= 2e-2 * float(np.max(np.abs(ref))), f"{name}: max-abs err {err:.3g}"
+    for k, (q, kk) in enumerate(((q1, k1), (q2, k2))):
+        s = np.einsum("bhid,bhjd->bhij", q, kk) / np.sqrt(d)
+        if causal:
+            s = np.where(np.tril(np.ones((N, N), dtype=bool)), s, -np.inf)
+        m = s.max(axis=-1, keepdims=True)
+        ref = (m[..., 0] + np.log(np.exp(s - m).sum(axis=-1))) / np.log(2.0)
+        err = float(np.max(np.abs(lse[k] - ref)))
+        assert err <= 2e-3, f"lse of map {k + 1}: max-abs err {err:.3g}"
