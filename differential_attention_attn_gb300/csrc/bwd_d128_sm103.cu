@@ -77,8 +77,8 @@ constexpr int vec_slots() {
 
 struct Ctrl {
   uint64_t kv_full;   // the item's key (and value) tiles
-  uint64_t q_full;    // the tile's queries and per-query vectors
-  uint64_t q_empty;   // the tile's queries have been read (dV items: S^T; dK/dQ: dK)
+  uint64_t q_full;    // dV items: the tile's queries and per-query vectors
+  uint64_t q_empty;   // dV items: the tile's queries have been read (S1^T, S2^T)
   uint64_t do_full;   // the tile's dO
   uint64_t do_empty;  // the tile's dO has been read (dV items: dV; dK/dQ: dW^T)
   uint64_t q_half_full[2];   // dK/dQ items: query half h of Q and its vectors
@@ -87,7 +87,7 @@ struct Ctrl {
   uint64_t p_half[2];  // query half h's packed operand is published (per thread)
   uint64_t acc_done;  // the item's dV or dK is complete
   uint64_t dq_full;   // dQ of the tile (dK/dQ items)
-  uint64_t dq_free;   // dQ read out of tensor memory (per thread)
+  uint64_t dq_free;   // dQ read out of tensor memory (per softmax thread)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
