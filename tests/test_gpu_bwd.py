@@ -278,3 +278,46 @@ def test_saved_d128_matches_oracle(N, causal):
         ref = (m[..., 0] + np.log(np.exp(s - m).sum(axis=-1))) / np.log(2.0)
         err = float(np.max(np.abs(lse[k] - ref)))
         assert err <= 2e-3, f"lse of map {k + 1}: max-abs err {err:.3g}"
+
+
+def _full_size(name):
+    if name == "needle_4k":  # the needle_4k_bwd bench configuration (d = 64)
+        w = W.make("needle_4k")
+        return w, float(np.float32(w.lambda_init_override))
+    # the wide_4k_bwd bench configuration (d = 128)
+    w = W.custom(3000, B=2, H=8, N=4096, d=128, causal=True, headnorm=True, random_w=True,
+                 layer=12)
+    return w, float(np.float32(ops.lambda_init(w.layer)))
+
+
+@pytest.mark.parametrize("name", ["needle_4k", "wide_4k"])
+@pytest.mark.parametrize("headnorm", [1, 0])
+def test_bwd_full_size_invariants(name, headnorm):
+    """The backward at the bench's full sizes, through properties that hold at any size.
+
+    Each row of dS sums to zero (sum_j P (dW - D) = D - D), so for every head and map the
+    sum of dK over all keys vanishes; without the norm (do = dy) the rows of P sum to one,
+    so the sum of dV over all keys is (1 - lambda) sum_q dy_q.  Each sum's terms carry the
+    bf16 rounding of P, dS and do (2^-8 of a term at most), so the residual is bounded by
+    2^-8 of the sum of the terms' magnitudes even if every error had the same sign."""
+    w, li = _full_size(name)
+    lam = torch.tensor(w.lambdas(li), dtype=torch.float32, device="cuda")
+    nw = (torch.tensor(np.asarray(w.w, dtype=np.float32), device="cuda")
+          if headnorm and w.w is not None else None)
+    kw = dict(causal=True, headnorm=headnorm, norm_w=nw, eps=float(np.float32(w.eps)),
+              lambda_init=li)
+    dev = [t.cuda() for t in (w.q1, w.k1, w.q2, w.k2, w.v)]
+    dy = _dy(w, 77).cuda()
+    _, saved = ops.fwd_train(*dev, lam, **kw)
+    g = ops.bwd(*dev, lam, saved, dy, **kw)
+    torch.cuda.synchronize()
+    bound = 2.0 ** -8
+    for k in ("dk1", "dk2"):
+        t = g[k].double()
+        resid = t.sum(dim=2).abs() / t.abs().sum(dim=2).clamp_min(1e-30)
+        assert float(resid.max()) <= bound, f"{name} {k}: sum over keys {float(resid.max()):.3g}"
+    if not headnorm:
+        t = g["dv"].double()
+        ref = (1.0 - lam.double())[None, :, None] * dy.double().sum(dim=2)
+        resid = (t.sum(dim=2) - ref).abs() / t.abs().sum(dim=2).clamp_min(1e-30)
+        assert float(resid.max()) <= bound, f"{name} dv: sum over keys {float(resid.max()):.3g}"
