@@ -392,6 +392,35 @@ def pin_bwd_lambda_zero_is_sdpa_grad(lib):
     return worst < 1e-12, f"max err {worst:.3e}"
 
 
+def pin_bwd_d128_is_sdpa_grad(lib):
+    """The backward oracle at the d = 128 head width (values 256 wide): with lambda = 0
+    and no norm, map 1's gradients and dv are the float64 autograd gradient of torch
+    scaled_dot_product_attention, map 2's are zero; with lambda = 1 and identical maps
+    the output (1 - lambda) SDPA is identically zero, so dv and the two maps' summed dq
+    and dk vanish, while dlambda = -sum(SDPA * dy)."""
+    worst = 0.0
+    for seed, causal in [(68, True), (69, False)]:
+        rng, q1, k1, q2, k2, v = _rand(seed, 1, 2, 6, 128)
+        dy = rng.standard_normal(v.shape)
+        g = oracle.bwd(q1, k1, q2, k2, v, np.zeros(2), dy, causal=causal, headnorm=False,
+                       lib=lib)
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_() for x in (q1, k1, v))
+        out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal)
+        out.backward(torch.from_numpy(dy))
+        worst = max(worst, float(np.max(np.abs(g["dq1"] - tq.grad.numpy()))),
+                    float(np.max(np.abs(g["dk1"] - tk.grad.numpy()))),
+                    float(np.max(np.abs(g["dv"] - tv.grad.numpy()))),
+                    float(np.max(np.abs(g["dq2"]))), float(np.max(np.abs(g["dk2"]))))
+        g = oracle.bwd(q1, k1, q1, k1, v, np.ones(2), dy, causal=causal, headnorm=False,
+                       lib=lib)
+        dlam_ref = -np.sum(_sdpa(q1, k1, v, causal) * dy, axis=(0, 2, 3))
+        worst = max(worst, float(np.max(np.abs(g["dv"]))),
+                    float(np.max(np.abs(g["dlam"] - dlam_ref))),
+                    float(np.max(np.abs(g["dq1"] + g["dq2"]))),
+                    float(np.max(np.abs(g["dk1"] + g["dk2"]))))
+    return worst < 1e-11, f"max err {worst:.3e}"
+
+
 def pin_bwd_identical_maps_lambda(lib):
     """q2 = q1, k2 = k1, no norm: y = (1 - lambda) SDPA, so dL/dlambda = -sum(SDPA * dy)."""
     rng, q1, k1, _, _, v = _rand(67, 2, 3, 7, 4)
