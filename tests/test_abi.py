@@ -201,8 +201,9 @@ def test_train_sizes(lib):
                                     ctypes.byref(b)) == ops.ERR_UNSUPPORTED
 
 
-def test_bwd_validation_before_launch(lib):
-    d = ops.make_desc(1, 2, 256, 64, ops.BF16, True, True, 1e-5, 0.2)
+@pytest.mark.parametrize("dh", [64, 128])
+def test_bwd_validation_before_launch(lib, dh):
+    d = ops.make_desc(1, 2, 256, dh, ops.BF16, True, True, 1e-5, 0.2)
     f = ctypes.c_void_p(FAKE)
     # q1 k1 q2 k2 v | lambda norm_w saved dy | dq1 dk1 dq2 dk2 dv | dlambda dnorm_w
     args = [f] * 5 + [f, None, f, f] + [f] * 5 + [f, None]
@@ -215,9 +216,23 @@ def test_bwd_validation_before_launch(lib):
     bad = list(args)
     bad[8] = None
     assert lib.diffattn_bwd(ctypes.byref(d), *bad, f, 1 << 40, None) == ops.ERR_INVALID_ARG
-    # fwd_train needs the saved buffer
+    # fwd_train needs the saved buffer, large enough and aligned
     assert lib.diffattn_fwd_train(ctypes.byref(d), *[f] * 5, f, None, f, None, 1 << 40,
                                   None) == ops.ERR_INVALID_ARG
+    saved, ws = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.diffattn_train_sizes(ctypes.byref(d), ctypes.byref(saved),
+                                    ctypes.byref(ws)) == ops.OK
+    assert lib.diffattn_fwd_train(ctypes.byref(d), *[f] * 5, f, None, f, f, saved.value - 1,
+                                  None) == ops.ERR_INVALID_ARG
+    assert lib.diffattn_fwd_train(ctypes.byref(d), *[f] * 5, f, None, f,
+                                  ctypes.c_void_p(FAKE + 8), saved.value,
+                                  None) == ops.ERR_INVALID_ARG
+    # the backward's workspace one byte short
+    assert lib.diffattn_bwd(ctypes.byref(d), *args, f, ws.value - 1, None) == ops.ERR_INVALID_ARG
+    # a misaligned gradient
+    bad = list(args)
+    bad[10] = ctypes.c_void_p(FAKE + 4)
+    assert lib.diffattn_bwd(ctypes.byref(d), *bad, f, 1 << 40, None) == ops.ERR_INVALID_ARG
 
 
 def test_headnorm_mode_validation(lib):
