@@ -216,14 +216,15 @@ def test_bwd_d128(N, causal, headnorm):
     assert torch.equal(out, harness.run_gpu(w))
 
 
-def test_bwd_d128_many_items():
-    """d = 128 with more dV and dK/dQ items than SMs (B=3, H=4, N=1100 causal:
-    9 key tiles, a ragged last one, 108 dV and 216 dK/dQ items)."""
-    w = W.custom(1200, B=3, H=4, N=1100, d=128, causal=True, headnorm=1, random_w=True,
+@pytest.mark.parametrize("causal", [True, False])
+def test_bwd_d128_many_items(causal):
+    """d = 128 with more dV and dK/dQ items than SMs (B=3, H=4, N=1100: 9 key tiles, a
+    ragged last one, 108 dV and 216 dK/dQ items; non-causal, every item the same length)."""
+    w = W.custom(1200, B=3, H=4, N=1100, d=128, causal=causal, headnorm=1, random_w=True,
                  layer=7)
     dy = _dy(w, 1200)
     _, g = _run(w, dy)
-    _cmp(g, _oracle(w, dy), "d=128 B3H4N1100")
+    _cmp(g, _oracle(w, dy), f"d=128 B3H4N1100 causal={causal}")
 
 
 @pytest.mark.parametrize("lam,headnorm", [(0.0, 1), (-0.5, 1), (0.8, 2), (1.0, 0), (-0.5, 0)])
